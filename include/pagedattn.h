@@ -1,0 +1,235 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * One decode step of attention over a block-paged KV cache:
+ *
+ *   paged_kv_append                 write the step's new K/V row of every
+ *                                   (sequence, kv head) into the pool slot
+ *                                   that block_table assigns
+ *   paged_attention_decode          attention of each query head over the
+ *                                   sequence's valid tokens, reading K/V
+ *                                   through block_table
+ *   paged_attention_decode_partial  the same over fixed token partitions,
+ *   paged_attention_decode_reduce   then a log-sum-exp merge (split-KV, for
+ *                                   long contexts or few sequences)
+ *
+ * Sources (web pages on paged KV caches), cited by title and section:
+ *   "KV Cache and BlockManager" (dpshk.com/news/5906718)            [BM]
+ *   vLLM memory-management course, ch. 3 "KV Block design"           [KB]
+ *   "A strange KV Cache bug" (dpshk.com/news/5937191)                [BUG]
+ *   "KV Cache paging in LLM inference" (intelliparadigm.com)         [PG]
+ *
+ * ---------------------------------------------------------------------------
+ * Memory layout (all tensors row-major, element type `dtype`)
+ * ---------------------------------------------------------------------------
+ *   q, out            [batch][num_heads][head_dim]
+ *   k_new, v_new      [batch][num_kv_heads][head_dim]
+ *   block_table       int32 [batch][max_blocks_per_seq]; entry j of row b is
+ *                     the physical block holding logical block j (tokens
+ *                     j*block_size .. j*block_size+block_size-1) of sequence
+ *                     b ([BM] s2, [KB] s3.3).  Entries at or past
+ *                     ceil(len/block_size) are never read and may be -1, the
+ *                     "unallocated" marker of [BM] s5.1.
+ *   seq_lens          int32 [batch]: VALID token count of each sequence,
+ *                     never the allocated or padded length ([BUG] s2.4).
+ *   k_pool, v_pool    element (blk, kv_head, slot, d) of a pool is at
+ *                       blk*block_stride + kv_head*block_size*head_dim
+ *                         + slot*head_dim + d
+ *                     The [num_blocks][2][num_kv_heads][block_size][head_dim]
+ *                     cache of [BM] s5.1 (one layer, K and V co-located per
+ *                     block as [KB] s3.2 recommends) is passed as
+ *                       k_pool = base, v_pool = base + num_kv_heads*block_size*head_dim,
+ *                       block_stride = 2*num_kv_heads*block_size*head_dim;
+ *                     separate K and V pools use block_stride =
+ *                     num_kv_heads*block_size*head_dim.  Each (block, kv
+ *                     head) K or V chunk is block_size*head_dim contiguous
+ *                     elements.  Block starts should be 128-byte aligned
+ *                     ([KB] s3.7); 16-byte alignment is required.
+ *
+ * Query head h reads kv head h / (num_heads / num_kv_heads) (grouped-query
+ * attention; num_heads must be a multiple of num_kv_heads).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions shared by every entry point
+ * ---------------------------------------------------------------------------
+ * Ownership   Every data pointer is DEVICE memory owned by the caller.  The
+ *             library never allocates, frees or retains memory.
+ * Streams     Work is enqueued on `stream` (NULL = legacy default stream) and
+ *             runs asynchronously; nothing synchronises the host.  The block
+ *             table never round-trips to the host ([BM] s2).
+ * Host checks Arguments are validated before anything is enqueued; a failure
+ *             returns a PA_ERR_* status synchronously and launches nothing.
+ * Device checks
+ *             A sequence whose length is negative or exceeds
+ *             max_blocks_per_seq*block_size, or whose first
+ *             ceil(len/block_size) table entries include one outside
+ *             [0, num_blocks), is not read: its output rows are written as
+ *             zeros and the matching PA_DEVERR_* bit is OR-ed into *err_word
+ *             (when err_word is not NULL).  Kernels never trap; every
+ *             device-side wait is bounded and reports PA_DEVERR_TIMEOUT.
+ *             This is the "graceful" handling [BM] s4.1 asks for instead of
+ *             a silent out-of-range access.
+ * Sharing     Several table rows may name the same physical block (prefix
+ *             sharing with reference counts, [KB] s3.4); reads from shared
+ *             blocks are fine, appends into a shared block are a caller
+ *             error (copy on write is the caller's job).
+ * Numerics    Scores, softmax and accumulation run in fp32; out is rounded
+ *             to `dtype` (round to nearest even).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA
+ * include. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent shape    */
+    PA_ERR_UNSUPPORTED = 2,  /* head_dim / dtype combination not compiled in  */
+    PA_ERR_MISALIGNED = 3,   /* a pointer or stride breaks the 16-byte rule   */
+    PA_ERR_WORKSPACE = 4,    /* split-KV workspace smaller than required      */
+    PA_ERR_CUDA = 5          /* the CUDA runtime reported an error at launch  */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_F32 = 0,
+    PA_F16 = 1,
+    PA_BF16 = 2
+} pa_dtype;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define PA_DEVERR_BAD_LEN   1  /* seq_len < 0 or > max_blocks_per_seq*block_size */
+#define PA_DEVERR_BAD_BLOCK 2  /* a needed table entry is outside [0, num_blocks) */
+#define PA_DEVERR_BAD_POS   4  /* append position outside the table row         */
+#define PA_DEVERR_TIMEOUT   8  /* a bounded wait for a copy gave up              */
+
+typedef struct pa_shape {
+    int32_t batch;              /* sequences B (0 is allowed: nothing to do) */
+    int32_t num_heads;          /* query heads H                             */
+    int32_t num_kv_heads;       /* kv heads Hkv, H % Hkv == 0                */
+    int32_t head_dim;           /* D                                         */
+    int32_t block_size;         /* tokens per block                          */
+    int32_t max_blocks_per_seq; /* row length MB of block_table              */
+    int64_t num_blocks;         /* physical blocks NB in the pool            */
+    int64_t block_stride;       /* elements from block j to block j+1        */
+    int32_t dtype;              /* pa_dtype of q, out, k/v_new and the pools */
+} pa_shape;
+
+/* Supported shapes: head_dim*element_size in {64, 128, 256, 512} bytes
+ * (f16/bf16: D = 32, 64, 128, 256; f32: D = 16, 32, 64, 128) and
+ * head_dim*element_size a multiple of 16 for the append. */
+
+/* Human-readable name of a status. Never NULL. */
+const char *pa_status_string(pa_status status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int32_t pa_version(void);
+
+/*
+ * paged_kv_append -- the reshape-and-cache write path.
+ *
+ * For every sequence b and kv head h, with pos = positions[b] (the valid
+ * length before this step), copy k_new[b][h][:] and v_new[b][h][:] into
+ * slot pos % block_size of physical block block_table[b][pos / block_size]:
+ * tokens keep their logical order inside a block ([BM] s4.4) and the cache
+ * grows exactly like the contiguous append of [BUG] s4.1.  The copy is
+ * bit-exact.  A sequence with pos outside [0, max_blocks_per_seq*block_size)
+ * is skipped with PA_DEVERR_BAD_POS; one whose target entry is outside
+ * [0, num_blocks) is skipped with PA_DEVERR_BAD_BLOCK.  positions is not
+ * modified (the caller advances seq_lens).
+ *
+ * k_new, v_new: device [B][Hkv][D]; k_pool, v_pool: device pools (layout
+ * above); block_table: device int32 [B][MB]; positions: device int32 [B];
+ * err_word: device int32 or NULL.
+ */
+pa_status paged_kv_append(const pa_shape *shape, const void *k_new, const void *v_new,
+                          void *k_pool, void *v_pool, const int32_t *block_table,
+                          const int32_t *positions, int32_t *err_word, pa_stream_t stream);
+
+/*
+ * paged_attention_decode -- one decode token per sequence.
+ *
+ * out[b][h][:] = sum_t w_t V[t][:] / sum_t w_t,  w_t = exp(x_t - max x),
+ * x_t = scale * <q[b][h][:], K[t][:]>, over t in [0, seq_lens[b]) only, where
+ * K[t], V[t] are row t of kv head h/(H/Hkv) found through block_table ([BM]
+ * s5.2: the translation happens inside the kernel).  seq_lens[b] == 0 gives
+ * out = 0.  The computation is the per-block decomposition of [PG] s2.2:
+ * scores per block, running softmax statistics, weighted sum of V blocks.
+ *
+ * Grouped-query shapes with 16-bit types, D in {64, 128}, and block_size a
+ * multiple of 16 (or 8) run on the tensor cores; everything else on the
+ * SIMT path.  paged_attention_decode_path() tells which.
+ *
+ * out, q: device [B][H][D]; pools, block_table as above; seq_lens: device
+ * int32 [B]; scale: usually 1/sqrt(D); err_word: device int32 or NULL.
+ */
+pa_status paged_attention_decode(const pa_shape *shape, void *out, const void *q,
+                                 const void *k_pool, const void *v_pool,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 float scale, int32_t *err_word, pa_stream_t stream);
+
+/* Which kernel family paged_attention_decode and _partial use for `shape`. */
+typedef enum pa_path {
+    PA_PATH_INVALID = 0,     /* shape rejected                                  */
+    PA_PATH_SIMT = 1,        /* fp32 CUDA-core path, one (sequence, head) per CTA */
+    PA_PATH_TENSOR_GQA = 2   /* tensor-core path, one (sequence, kv head) per CTA */
+} pa_path;
+pa_path paged_attention_decode_path(const pa_shape *shape);
+
+/*
+ * Split-KV ("flash decoding") pair for long contexts.
+ *
+ * paged_attention_decode_partial splits each sequence's valid tokens into
+ * partitions of partition_tokens tokens (a positive multiple of 16) and,
+ * for every (b, h, partition p) that holds at least one valid token,
+ * writes into the workspace
+ *   m[b][h][p]      = max over the partition of x_t * log2(e)
+ *   l[b][h][p]      = sum over the partition of 2^(x_t*log2(e) - m)
+ *   acc[b][h][p][:] = sum over the partition of 2^(x_t*log2(e) - m) V[t][:]
+ * in fp32 (x_t as in paged_attention_decode).  paged_attention_decode_reduce
+ * then merges the ceil(seq_lens[b]/partition_tokens) partitions of each
+ * (b, h):
+ *   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,
+ * which equals paged_attention_decode up to rounding.  Both calls must get the
+ * same shape, seq_lens and partition_tokens, on the same stream (or be
+ * ordered by the caller).
+ *
+ * Workspace: device memory of at least paged_attention_partial_workspace()
+ * bytes, 16-byte aligned, owned by the caller, holding, with
+ * P = ceil(max_blocks_per_seq*block_size / partition_tokens):
+ *   float m[B][H][P]; float l[B][H][P]; float acc[B][H][P][D]
+ * at byte offsets 0, 4*B*H*P and 8*B*H*P rounded up to 16.  Only the slots
+ * of partitions that hold valid tokens are written; the reduce reads only
+ * those.  A partition that met a bad table entry stores l = -1, and the
+ * reduce then writes zeros for the whole sequence.
+ *
+ * paged_attention_partial_workspace returns 0 for an invalid shape or
+ * partition size.
+ */
+size_t paged_attention_partial_workspace(const pa_shape *shape, int32_t partition_tokens);
+
+pa_status paged_attention_decode_partial(const pa_shape *shape, const void *q,
+                                         const void *k_pool, const void *v_pool,
+                                         const int32_t *block_table, const int32_t *seq_lens,
+                                         float scale, int32_t partition_tokens,
+                                         void *workspace, size_t workspace_bytes,
+                                         int32_t *err_word, pa_stream_t stream);
+
+pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
+                                        const void *workspace, size_t workspace_bytes,
+                                        const int32_t *seq_lens, int32_t partition_tokens,
+                                        int32_t *err_word, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,201 @@
+"""Python binding of libpagedattn.so (include/pagedattn.h), via ctypes.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of the library.  Tensors are torch CUDA tensors; their data pointers
+and torch's current CUDA stream are handed to the C ABI unchanged.  If the
+library has not been built, importing works but every call raises -- there is
+no CPU fallback.
+
+Names follow the C ABI: paged_kv_append, paged_attention_decode,
+paged_attention_partial_workspace, paged_attention_decode_partial,
+paged_attention_decode_reduce, paged_attention_decode_path.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_lib" / "libpagedattn.so"
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_PATH_INVALID, PA_PATH_SIMT, PA_PATH_TENSOR_GQA = 0, 1, 2
+DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attention_decode",
+            "paged_attention_decode_path", "paged_attention_partial_workspace",
+            "paged_attention_decode_partial", "paged_attention_decode_reduce")
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class Shape(ctypes.Structure):
+    """Mirror of pa_shape."""
+    _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64), ("block_stride", ctypes.c_int64),
+                ("dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(str(LIB_PATH))
+            vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+            sp = ctypes.POINTER(Shape)
+            lib.pa_status_string.restype = ctypes.c_char_p
+            lib.pa_status_string.argtypes = [ctypes.c_int]
+            lib.pa_version.restype = i32
+            lib.pa_version.argtypes = []
+            lib.paged_kv_append.restype = ctypes.c_int
+            lib.paged_kv_append.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.paged_attention_decode.restype = ctypes.c_int
+            lib.paged_attention_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
+            lib.paged_attention_decode_path.restype = ctypes.c_int
+            lib.paged_attention_decode_path.argtypes = [sp]
+            lib.paged_attention_partial_workspace.restype = sz
+            lib.paged_attention_partial_workspace.argtypes = [sp, i32]
+            lib.paged_attention_decode_partial.restype = ctypes.c_int
+            lib.paged_attention_decode_partial.argtypes = [sp, vp, vp, vp, vp, vp, f32, i32, vp, sz,
+                                                           vp, vp]
+            lib.paged_attention_decode_reduce.restype = ctypes.c_int
+            lib.paged_attention_decode_reduce.argtypes = [sp, vp, vp, sz, vp, i32, vp, vp]
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().pa_version())
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    try:
+        return {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}[dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {dtype}") from None
+
+
+def make_shape(*, batch, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+               num_blocks, block_stride, dtype) -> Shape:
+    return Shape(int(batch), int(num_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                 int(max_blocks_per_seq), int(num_blocks), int(block_stride),
+                 dtype if isinstance(dtype, int) else dtype_code(dtype))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(status, what)
+
+
+def decode_shape(q, block_table, *, num_kv_heads, block_size, num_blocks, block_stride) -> Shape:
+    B, H, D = q.shape
+    return make_shape(batch=B, num_heads=H, num_kv_heads=num_kv_heads, head_dim=D,
+                      block_size=block_size, max_blocks_per_seq=block_table.shape[1],
+                      num_blocks=num_blocks, block_stride=block_stride, dtype=q.dtype)
+
+
+def paged_kv_append(k_new, v_new, k_pool, v_pool, block_table, positions, *, block_size,
+                    num_blocks, block_stride, err_word=None, stream=None) -> None:
+    """Write k_new/v_new [B][Hkv][D] at positions[b] through block_table."""
+    B, Hkv, D = k_new.shape
+    shape = make_shape(batch=B, num_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=block_size,
+                       max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
+                       block_stride=block_stride, dtype=k_new.dtype)
+    _check(load().paged_kv_append(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                  _ptr(v_pool), _ptr(block_table), _ptr(positions),
+                                  _ptr(err_word), _stream(stream)), "paged_kv_append")
+
+
+def paged_attention_decode(out, q, k_pool, v_pool, block_table, seq_lens, scale, *, num_kv_heads,
+                           block_size, num_blocks, block_stride, err_word=None,
+                           stream=None) -> None:
+    """out[B][H][D] = attention of q over the valid tokens of each sequence."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    _check(load().paged_attention_decode(ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool),
+                                         _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                         float(scale), _ptr(err_word), _stream(stream)),
+           "paged_attention_decode")
+
+
+def paged_attention_decode_path(shape: Shape) -> int:
+    return int(load().paged_attention_decode_path(ctypes.byref(shape)))
+
+
+def paged_attention_partial_workspace(shape: Shape, partition_tokens: int) -> int:
+    return int(load().paged_attention_partial_workspace(ctypes.byref(shape), int(partition_tokens)))
+
+
+def paged_attention_decode_partial(q, k_pool, v_pool, block_table, seq_lens, scale,
+                                   partition_tokens, workspace, *, num_kv_heads, block_size,
+                                   num_blocks, block_stride, err_word=None, stream=None) -> None:
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().paged_attention_decode_partial(ctypes.byref(shape), _ptr(q), _ptr(k_pool),
+                                                 _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                                 float(scale), int(partition_tokens),
+                                                 _ptr(workspace), nbytes, _ptr(err_word),
+                                                 _stream(stream)),
+           "paged_attention_decode_partial")
+
+
+def paged_attention_decode_reduce(out, workspace, seq_lens, partition_tokens, *, num_kv_heads,
+                                  block_size, num_blocks, block_stride, max_blocks_per_seq,
+                                  err_word=None, stream=None) -> None:
+    B, H, D = out.shape
+    shape = make_shape(batch=B, num_heads=H, num_kv_heads=num_kv_heads, head_dim=D,
+                       block_size=block_size, max_blocks_per_seq=max_blocks_per_seq,
+                       num_blocks=num_blocks, block_stride=block_stride, dtype=out.dtype)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().paged_attention_decode_reduce(ctypes.byref(shape), _ptr(out), _ptr(workspace),
+                                                nbytes, _ptr(seq_lens), int(partition_tokens),
+                                                _ptr(err_word), _stream(stream)),
+           "paged_attention_decode_reduce")
+
+
+def workspace_for(q, block_table, partition_tokens, *, num_kv_heads, block_size, num_blocks,
+                  block_stride) -> torch.Tensor:
+    """Allocate (through torch) a workspace big enough for the split-KV pair."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    n = paged_attention_partial_workspace(shape, partition_tokens)
+    if n == 0:
+        raise PagedAttnError(PA_ERR_INVALID_ARG, "paged_attention_partial_workspace")
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=q.device)

@@ -1,0 +1,308 @@
+// api.cu -- the extern "C" entry points of include/pagedattn.h: host-side
+// validation, kernel-family selection, tensor-map encoding and launches.
+// Nothing here allocates device memory or synchronises the host.
+#include <math.h>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+size_t gqa_tc_smem_bytes(int head_dim, int table_cap);
+}
+
+namespace {
+
+constexpr int32_t kVersion = 10000;    // 1.0.0
+constexpr int kTableCap = 2048;        // block_table entries staged in shared memory
+constexpr int kMaxPartitions = 1 << 20;
+
+int elem_size(int32_t dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every entry point.
+pa_status check_shape(const pa_shape *s) {
+    if (s == nullptr) return PA_ERR_INVALID_ARG;
+    if (s->dtype != PA_F32 && s->dtype != PA_F16 && s->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (s->batch < 0 || s->num_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 ||
+        s->block_size <= 0 || s->max_blocks_per_seq <= 0 || s->num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (s->num_heads % s->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int64_t chunk = (int64_t)s->num_kv_heads * s->block_size * s->head_dim;
+    if (s->block_stride < chunk) return PA_ERR_INVALID_ARG;
+    // positions and lengths are int32: the row must address fewer than 2^31 tokens
+    if ((int64_t)s->max_blocks_per_seq * s->block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if (((int64_t)s->head_dim * elem_size(s->dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if ((s->block_stride * elem_size(s->dtype)) % 16 != 0) return PA_ERR_MISALIGNED;
+    return PA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps for the tensor-core path
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int box_rows_for(const pa_shape *s) { return s->block_size % 16 == 0 ? 16 : 8; }
+
+bool tc_eligible(const pa_shape *s) {
+    if (!pa::gqa_tc_supported(s->dtype, s->head_dim)) return false;
+    if (s->num_heads / s->num_kv_heads < 2) return false;
+    if (!(s->block_size % 16 == 0 || s->block_size == 8)) return false;
+    if (s->block_stride % s->head_dim != 0) return false;
+    const int64_t rows_per_block = s->block_stride / s->head_dim;
+    // TMA row coordinates are signed 32-bit
+    if (s->num_blocks * rows_per_block > (int64_t)INT32_MAX) return false;
+    return true;
+}
+
+// View a pool as a [rows][head_dim] matrix; boxes of 64 x box_rows elements,
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const int64_t rows_per_block = s->block_stride / s->head_dim;
+    const int64_t rows = (s->num_blocks - 1) * rows_per_block +
+                         (int64_t)s->num_kv_heads * s->block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)s->head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)s->head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows_for(s)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return fn(map, dt, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t num_partitions(const pa_shape *s, int32_t ptok) {
+    return ((int64_t)s->max_blocks_per_seq * s->block_size + ptok - 1) / ptok;
+}
+
+struct WsLayout {
+    size_t off_m, off_l, off_acc, total;
+};
+
+WsLayout ws_layout(const pa_shape *s, int64_t P) {
+    const size_t n = (size_t)s->batch * s->num_heads * (size_t)P;
+    WsLayout w;
+    w.off_m = 0;
+    w.off_l = 4 * n;
+    w.off_acc = (8 * n + 15) & ~(size_t)15;
+    w.total = w.off_acc + 4 * n * (size_t)s->head_dim;
+    return w;
+}
+
+pa::DecodeParams base_params(const pa_shape *s, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *block_table,
+                             const int32_t *seq_lens, float scale, int32_t *err_word) {
+    pa::DecodeParams p{};
+    p.q = q;
+    p.k_pool = static_cast<const char *>(k_pool);
+    p.v_pool = static_cast<const char *>(v_pool);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.err_word = err_word;
+    p.num_blocks = s->num_blocks;
+    p.block_stride_bytes = s->block_stride * elem_size(s->dtype);
+    p.rows_per_block = (int32_t)(s->block_stride / s->head_dim);
+    p.B = s->batch;
+    p.H = s->num_heads;
+    p.Hkv = s->num_kv_heads;
+    p.D = s->head_dim;
+    p.MB = s->max_blocks_per_seq;
+    p.bs = s->block_size;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+    return p;
+}
+
+// Launch the decode kernel family chosen for `s` (final or split mode).
+pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cudaStream_t stream) {
+    cudaError_t e;
+    if (tc_eligible(s)) {
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map(&kmap, s, p.k_pool) || !encode_pool_map(&vmap, s, p.v_pool))
+            return PA_ERR_CUDA;
+        e = pa::launch_decode_gqa_tc(s->dtype, p, kmap, vmap, box_rows_for(s), split, stream);
+    } else {
+        e = pa::launch_decode_simt(s->dtype, p, split, stream);
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status check_decode_args(const pa_shape *s, const void *q, const void *k_pool,
+                            const void *v_pool, const int32_t *block_table,
+                            const int32_t *seq_lens) {
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (s->batch == 0) return PA_OK;
+    if (!pa::simt_supported(s->dtype, s->head_dim)) return PA_ERR_UNSUPPORTED;
+    if (q == nullptr || k_pool == nullptr || v_pool == nullptr || block_table == nullptr ||
+        seq_lens == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_MISALIGNED;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported head_dim/dtype combination";
+        case PA_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+        case PA_ERR_WORKSPACE: return "split-KV workspace too small";
+        case PA_ERR_CUDA: return "CUDA runtime error at launch";
+    }
+    return "unknown status";
+}
+
+int32_t pa_version(void) { return kVersion; }
+
+pa_status paged_kv_append(const pa_shape *shape, const void *k_new, const void *v_new,
+                          void *k_pool, void *v_pool, const int32_t *block_table,
+                          const int32_t *positions, int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        block_table == nullptr || positions == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_MISALIGNED;
+    pa::AppendParams p{};
+    p.k_new = static_cast<const char *>(k_new);
+    p.v_new = static_cast<const char *>(v_new);
+    p.k_pool = static_cast<char *>(k_pool);
+    p.v_pool = static_cast<char *>(v_pool);
+    p.block_table = block_table;
+    p.positions = positions;
+    p.err_word = err_word;
+    p.num_blocks = shape->num_blocks;
+    p.block_stride_bytes = shape->block_stride * elem_size(shape->dtype);
+    p.B = shape->batch;
+    p.Hkv = shape->num_kv_heads;
+    p.MB = shape->max_blocks_per_seq;
+    p.bs = shape->block_size;
+    p.row_bytes = shape->head_dim * elem_size(shape->dtype);
+    return pa::launch_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                          : PA_ERR_CUDA;
+}
+
+pa_path paged_attention_decode_path(const pa_shape *shape) {
+    if (check_shape(shape) != PA_OK || !pa::simt_supported(shape->dtype, shape->head_dim))
+        return PA_PATH_INVALID;
+    return tc_eligible(shape) ? PA_PATH_TENSOR_GQA : PA_PATH_SIMT;
+}
+
+pa_status paged_attention_decode(const pa_shape *shape, void *out, const void *q,
+                                 const void *k_pool, const void *v_pool,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 float scale, int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK || shape->batch == 0) return st;
+    if (out == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PA_ERR_MISALIGNED;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.out = out;
+    p.partition_tokens = 0;
+    p.num_partitions = 1;
+    p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
+    return launch_decode(shape, p, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t paged_attention_partial_workspace(const pa_shape *shape, int32_t partition_tokens) {
+    if (check_shape(shape) != PA_OK || partition_tokens <= 0 || partition_tokens % 16 != 0) return 0;
+    const int64_t P = num_partitions(shape, partition_tokens);
+    if (P > kMaxPartitions) return 0;
+    return ws_layout(shape, P).total;
+}
+
+pa_status paged_attention_decode_partial(const pa_shape *shape, const void *q,
+                                         const void *k_pool, const void *v_pool,
+                                         const int32_t *block_table, const int32_t *seq_lens,
+                                         float scale, int32_t partition_tokens,
+                                         void *workspace, size_t workspace_bytes,
+                                         int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK) return st;
+    if (partition_tokens <= 0 || partition_tokens % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    const int64_t P = num_partitions(shape, partition_tokens);
+    if (P > kMaxPartitions || (int64_t)shape->batch * shape->num_heads * P > INT32_MAX)
+        return PA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(shape, P);
+    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return PA_ERR_MISALIGNED;
+    if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    char *ws = static_cast<char *>(workspace);
+    p.ws_m = reinterpret_cast<float *>(ws + w.off_m);
+    p.ws_l = reinterpret_cast<float *>(ws + w.off_l);
+    p.ws_acc = reinterpret_cast<float *>(ws + w.off_acc);
+    p.partition_tokens = partition_tokens;
+    p.num_partitions = (int32_t)P;
+    const int64_t need = partition_tokens / shape->block_size + 2;
+    p.table_cap = (int)(need < kTableCap ? need : kTableCap);
+    return launch_decode(shape, p, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
+                                        const void *workspace, size_t workspace_bytes,
+                                        const int32_t *seq_lens, int32_t partition_tokens,
+                                        int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (partition_tokens <= 0 || partition_tokens % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    if (!pa::simt_supported(shape->dtype, shape->head_dim)) return PA_ERR_UNSUPPORTED;
+    if (out == nullptr || workspace == nullptr || seq_lens == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(workspace)) return PA_ERR_MISALIGNED;
+    const int64_t P = num_partitions(shape, partition_tokens);
+    if (P > kMaxPartitions) return PA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(shape, P);
+    if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+    const char *ws = static_cast<const char *>(workspace);
+    pa::ReduceParams p{};
+    p.out = out;
+    p.ws_m = reinterpret_cast<const float *>(ws + w.off_m);
+    p.ws_l = reinterpret_cast<const float *>(ws + w.off_l);
+    p.ws_acc = reinterpret_cast<const float *>(ws + w.off_acc);
+    p.seq_lens = seq_lens;
+    p.err_word = err_word;
+    p.B = shape->batch;
+    p.H = shape->num_heads;
+    p.D = shape->head_dim;
+    p.MB = shape->max_blocks_per_seq;
+    p.bs = shape->block_size;
+    p.partition_tokens = partition_tokens;
+    p.num_partitions = (int32_t)P;
+    return pa::launch_reduce(shape->dtype, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,463 @@
+// decode_simt.cu -- decode attention on the CUDA cores (one CTA per
+// (sequence, query head[, partition])), and the split-KV reduce.
+//
+// The computation is the per-block decomposition of attention described in
+// "KV Cache paging in LLM inference" (intelliparadigm.com) s2.2: the query
+// meets every block of its sequence, per-block dot products give scores, the
+// softmax statistics are aggregated across blocks (here as a running maximum
+// and sum, rescaled as they go), and V blocks are summed with the weights.
+// The logical-to-physical translation happens inside the kernel from a
+// shared-memory copy of the block_table row ("KV Cache and BlockManager",
+// dpshk.com/news/5906718, s2 and s5.2), and only the valid tokens
+// [0, seq_len) are read ("A strange KV Cache bug", dpshk.com/news/5937191,
+// s2.4): the tail of the last block is never fetched.
+//
+// Data movement: each warp owns a ring of kStages tiles.  A tile is the K and
+// V rows of kTileBytes/row_bytes consecutive tokens of one kv head; within a
+// physical block those rows are contiguous, so lane 0 fetches them with 1-D
+// bulk copies (cp.async.bulk, completion on an mbarrier), split only where
+// the tile crosses a block boundary.  Warps take tiles round-robin and merge
+// their softmax states through shared memory at the end.
+//
+// Thread mapping inside a warp: a token row of row_bytes is read by
+// LPT = row_bytes/16 lanes with one 16-byte load each, RPW = 32/LPT rows per
+// instruction, so every shared-memory wavefront reads contiguous bytes.
+// The per-row partial dot products are reduced with a transposing butterfly
+// that halves the number of live values at each shuffle step.
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kSimtWarps = 4;
+constexpr int kSimtStages = 3;
+constexpr int kTileBytes = 4096;  // K bytes per tile (V the same)
+
+template <typename T, int D>
+struct SimtCfg {
+    static constexpr int S = sizeof(T);
+    static constexpr int ROWB = D * S;             // bytes per token row
+    static constexpr int VEC = 16 / S;             // elements per 16-byte load
+    static constexpr int LPT = ROWB / 16;          // lanes per token row
+    static constexpr int RPW = 32 / LPT;           // rows per warp instruction
+    static constexpr int TILE = kTileBytes / ROWB; // tokens per tile
+    static constexpr int NVALS = TILE / RPW;       // rows per lane per tile
+    static constexpr int NFIN = NVALS >= LPT ? NVALS / LPT : 1;  // scores per lane after reduce
+    static constexpr int LOG_LPT = LPT == 4 ? 2 : LPT == 8 ? 3 : LPT == 16 ? 4 : 5;
+    static constexpr int LOG_NVALS = NVALS == 8 ? 3 : NVALS == 4 ? 2 : NVALS == 16 ? 4 : 1;
+    static_assert(LPT == 4 || LPT == 8 || LPT == 16 || LPT == 32, "row must be 64..512 bytes");
+    static_assert(NVALS == 8, "tile holds 8 rows per lane");
+};
+
+// Transposing butterfly: v[0..N) per lane are partial sums of N different
+// rows; after the call each lane holds complete sums of fewer rows (see
+// row_of_value below for which ones).
+template <int N, int O>
+struct Butterfly {
+    static __device__ __forceinline__ void run(float *v, int lane) {
+        if constexpr (O == 0) {
+            return;
+        } else if constexpr (N > 1) {
+            constexpr int HALF = N / 2;
+            const bool upper = (lane & O) != 0;
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                const float send = upper ? v[k] : v[k + HALF];
+                const float keep = upper ? v[k + HALF] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            Butterfly<HALF, O / 2>::run(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            Butterfly<1, O / 2>::run(v, lane);
+        }
+    }
+};
+
+// Index (0..NVALS) of the k-th value a lane holds after the butterfly.
+template <typename C>
+__device__ __forceinline__ int row_of_value(int c, int k) {
+    if constexpr (C::NVALS >= C::LPT) {
+        return c * C::NFIN + k;
+    } else {
+        return c >> (C::LOG_LPT - C::LOG_NVALS);
+    }
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+template <typename T, int D>
+struct SimtSmem {
+    using C = SimtCfg<T, D>;
+    static constexpr size_t kStages = (size_t)kSimtWarps * kSimtStages * 2 * kTileBytes;
+    static constexpr size_t kBars = (size_t)kSimtWarps * kSimtStages * 8;
+    static constexpr size_t kP = (size_t)kSimtWarps * C::TILE * 4;
+    static constexpr size_t kRed = (size_t)kSimtWarps * (D + 2) * 4;
+    static constexpr size_t kFlags = 16;
+    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags;
+    static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 4; }
+};
+
+template <typename T, int D, bool SPLIT>
+__global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeParams p) {
+    using C = SimtCfg<T, D>;
+    using L = SimtSmem<T, D>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kStages);
+    float *pbuf = reinterpret_cast<float *>(smem + L::kStages + L::kBars);
+    float *red_m = reinterpret_cast<float *>(smem + L::kStages + L::kBars + L::kP);
+    float *red_l = red_m + kSimtWarps;
+    float *red_acc = red_l + kSimtWarps;
+    int *flags = reinterpret_cast<int *>(smem + L::kStages + L::kBars + L::kP + L::kRed);
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kFixed);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // unit = (b fastest, then h, then partition): CTAs that read the same
+    // shared prefix blocks for different sequences run side by side.
+    int unit = blockIdx.x;
+    const int b = unit % p.B;
+    unit /= p.B;
+    const int h = unit % p.H;
+    const int part = unit / p.H;
+    const int hk = h / (p.H / p.Hkv);
+    const int64_t bh = (int64_t)b * p.H + h;
+    T *out = reinterpret_cast<T *>(p.out);
+
+    const int32_t len = p.seq_lens[b];
+    if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
+        if (threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+        if (!SPLIT)
+            for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
+        return;
+    }
+    const int t_begin = SPLIT ? part * p.partition_tokens : 0;
+    const int t_end = SPLIT ? min(len, t_begin + p.partition_tokens) : len;
+    if (t_end <= t_begin) {
+        // nothing to attend to: final mode writes zeros, split mode leaves
+        // the partition's slots unused (the reduce never reads them)
+        if (!SPLIT)
+            for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
+        return;
+    }
+
+    // stage the needed part of the block_table row in shared memory
+    const int j0 = t_begin / p.bs;
+    const int nblk = (t_end - 1) / p.bs + 1 - j0;
+    const int ncache = min(nblk, p.table_cap);
+    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
+    for (int j = threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
+    if (threadIdx.x == 0) flags[0] = 0;
+    if (threadIdx.x < kSimtWarps * kSimtStages) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
+    mbar_init_fence();
+    __syncthreads();
+
+    const int ntiles = (t_end - t_begin + C::TILE - 1) / C::TILE;
+    const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kSimtWarps + 1 : 0;
+    const int r = lane / C::LPT;   // row group
+    const int c = lane % C::LPT;   // 16-byte column
+
+    // lane 0 of the warp fetches local tile k into ring slot k % kSimtStages
+    auto issue = [&](int k) {
+        const int t0 = t_begin + (warp + k * kSimtWarps) * C::TILE;
+        const int t1 = min(t0 + C::TILE, t_end);
+        const int slot = k % kSimtStages;
+        const uint32_t dst_k = smem_u32(stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes);
+        const uint32_t dst_v = dst_k + kTileBytes;
+        const uint32_t bar = smem_u32(&bars[warp * kSimtStages + slot]);
+        uint32_t bytes = 0;
+        bool ok = true;
+        for (int t = t0; t < t1;) {
+            const int j = t / p.bs;
+            const int e = min(t1, (j + 1) * p.bs);
+            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
+            if (blk < 0 || (int64_t)blk >= p.num_blocks) ok = false;
+            else bytes += (uint32_t)(e - t) * C::ROWB * 2;
+            t = e;
+        }
+        if (!ok) {
+            flags[0] = 1;
+            report(p.err_word, PA_DEVERR_BAD_BLOCK);
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int t = t0; t < t1;) {
+            const int j = t / p.bs;
+            const int e = min(t1, (j + 1) * p.bs);
+            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
+            if (blk >= 0 && (int64_t)blk < p.num_blocks) {
+                const int64_t off = (int64_t)blk * p.block_stride_bytes +
+                                    ((int64_t)hk * p.bs + (t - j * p.bs)) * C::ROWB;
+                const uint32_t n = (uint32_t)(e - t) * C::ROWB;
+                const uint32_t so = (uint32_t)(t - t0) * C::ROWB;
+                bulk_g2s(dst_k + so, p.k_pool + off, n, bar);
+                bulk_g2s(dst_v + so, p.v_pool + off, n, bar);
+            }
+            t = e;
+        }
+    };
+
+    // this lane's slice of the query, in fp32
+    float qf[C::VEC];
+    {
+        const uint4 qv = *reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const char *>(p.q) + (bh * D + c * C::VEC) * C::S);
+        Elem<T>::unpack(qv, qf);
+    }
+
+    if (lane == 0)
+        for (int k = 0; k < min(kSimtStages, my_tiles); ++k) issue(k);
+
+    float m_run = -INFINITY;  // running max of log2-scaled scores
+    float l_run = 0.f;        // running sum of 2^(s - m_run), this lane's rows
+    float acc[C::VEC];
+#pragma unroll
+    for (int e = 0; e < C::VEC; ++e) acc[e] = 0.f;
+    float *pw = pbuf + warp * C::TILE;
+
+    int k = 0;
+    bool aborted = false;
+    for (; k < my_tiles; ++k) {
+        const int slot = k % kSimtStages;
+        const uint32_t bar = smem_u32(&bars[warp * kSimtStages + slot]);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar, (k / kSimtStages) & 1))) {
+            aborted = true;
+            break;
+        }
+        const unsigned char *ks = stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes;
+        const unsigned char *vs = ks + kTileBytes;
+        const int t0 = t_begin + (warp + k * kSimtWarps) * C::TILE;
+        const int nrows = min(C::TILE, t_end - t0);
+
+        // scores: partial dot products of 8 rows, then the butterfly
+        float v[C::NVALS];
+#pragma unroll
+        for (int j = 0; j < C::NVALS; ++j) {
+            const int row = j * C::RPW + r;
+            const uint4 kv = *reinterpret_cast<const uint4 *>(ks + row * C::ROWB + c * 16);
+            float kf[C::VEC];
+            Elem<T>::unpack(kv, kf);
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::VEC; ++e) s = fmaf(qf[e], kf[e], s);
+            v[j] = s;
+        }
+        Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
+
+        float sc[C::NFIN];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int kk = 0; kk < C::NFIN; ++kk) {
+            const int row = row_of_value<C>(c, kk) * C::RPW + r;
+            sc[kk] = row < nrows ? v[kk] * p.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, sc[kk]);
+        }
+        tmax = warp_max(tmax);
+        const float m_new = fmaxf(m_run, tmax);
+        const float corr = exp2f(m_run - m_new);
+#pragma unroll
+        for (int kk = 0; kk < C::NFIN; ++kk) {
+            const int row = row_of_value<C>(c, kk) * C::RPW + r;
+            pw[row] = exp2f(sc[kk] - m_new);
+        }
+        __syncwarp();
+        l_run *= corr;
+#pragma unroll
+        for (int e = 0; e < C::VEC; ++e) acc[e] *= corr;
+#pragma unroll
+        for (int j = 0; j < C::NVALS; ++j) {
+            const int row = j * C::RPW + r;
+            if (row < nrows) {
+                const float pj = pw[row];
+                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + row * C::ROWB + c * 16);
+                float vf[C::VEC];
+                Elem<T>::unpack(vv, vf);
+#pragma unroll
+                for (int e = 0; e < C::VEC; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+                l_run += pj;
+            }
+        }
+        m_run = m_new;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && k + kSimtStages < my_tiles) issue(k + kSimtStages);
+    }
+    if (aborted) {
+        if (lane == 0) {
+            flags[0] = 1;
+            report(p.err_word, PA_DEVERR_TIMEOUT);
+        }
+        // let the copies already in flight land before the CTA can exit
+        for (int kk = k; kk < min(my_tiles, k + kSimtStages); ++kk)
+            mbar_wait(smem_u32(&bars[warp * kSimtStages + kk % kSimtStages]), (kk / kSimtStages) & 1);
+    }
+
+    // combine the row groups of the warp, then the warps of the CTA
+#pragma unroll
+    for (int o = C::LPT; o < 32; o <<= 1) {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
+#pragma unroll
+        for (int e = 0; e < C::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    }
+    if (lane < C::LPT) {
+#pragma unroll
+        for (int e = 0; e < C::VEC; ++e) red_acc[warp * D + lane * C::VEC + e] = acc[e];
+    }
+    if (lane == 0) {
+        red_m[warp] = m_run;
+        red_l[warp] = l_run;
+    }
+    __syncthreads();
+
+    const bool bad = flags[0] != 0;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSimtWarps; ++w) M = fmaxf(M, red_m[w]);
+    float wsc[kSimtWarps];
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSimtWarps; ++w) {
+        wsc[w] = exp2f(red_m[w] - M);   // warps without tiles: 2^-inf = 0
+        lsum = fmaf(red_l[w], wsc[w], lsum);
+    }
+    if (!SPLIT) {
+        const float inv = 1.f / lsum;
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSimtWarps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
+            out[bh * D + d] = Elem<T>::from_float(bad ? 0.f : a * inv);
+        }
+    } else {
+        const int64_t slot = bh * p.num_partitions + part;
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSimtWarps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
+            p.ws_acc[slot * D + d] = a;
+        }
+        if (threadIdx.x == 0) {
+            p.ws_m[slot] = M;
+            p.ws_l[slot] = bad ? -1.f : lsum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// split-KV reduce: log-sum-exp merge of the partitions of each (b, h)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(128) reduce_kernel(ReduceParams p) {
+    const int64_t bh = blockIdx.x;
+    const int b = (int)(bh / p.H);
+    T *out = reinterpret_cast<T *>(p.out);
+    const int32_t len = p.seq_lens[b];
+    const bool bad_len = len < 0 || (int64_t)len > (int64_t)p.MB * p.bs;
+    if (bad_len && threadIdx.x == 0 && (bh % p.H) == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+    const int np = bad_len || len == 0 ? 0 : (len + p.partition_tokens - 1) / p.partition_tokens;
+    const float *m = p.ws_m + bh * p.num_partitions;
+    const float *l = p.ws_l + bh * p.num_partitions;
+    const float *acc = p.ws_acc + bh * p.num_partitions * p.D;
+    float M = -INFINITY;
+    bool bad = false;
+    for (int q = 0; q < np; ++q) {
+        M = fmaxf(M, m[q]);
+        bad |= l[q] < 0.f;
+    }
+    float lsum = 0.f;
+    for (int q = 0; q < np; ++q) lsum = fmaf(l[q], exp2f(m[q] - M), lsum);
+    const float inv = 1.f / lsum;
+    for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
+        float o = 0.f;
+        for (int q = 0; q < np; ++q) o = fmaf(acc[(int64_t)q * p.D + d], exp2f(m[q] - M), o);
+        out[bh * p.D + d] = Elem<T>::from_float((np == 0 || bad) ? 0.f : o * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side dispatch
+// ---------------------------------------------------------------------------
+
+template <typename T, int D, bool SPLIT>
+static cudaError_t launch_simt_t(const DecodeParams &p, cudaStream_t stream) {
+    const size_t smem = SimtSmem<T, D>::bytes(p.table_cap);
+    auto kern = decode_simt_kernel<T, D, SPLIT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)p.B * p.H * p.num_partitions;
+    if (grid == 0) return cudaSuccess;
+    kern<<<(unsigned)grid, kSimtWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, bool SPLIT>
+static cudaError_t launch_simt_d(const DecodeParams &p, cudaStream_t stream) {
+    if constexpr (sizeof(T) == 4) {
+        switch (p.D) {
+            case 16: return launch_simt_t<T, 16, SPLIT>(p, stream);
+            case 32: return launch_simt_t<T, 32, SPLIT>(p, stream);
+            case 64: return launch_simt_t<T, 64, SPLIT>(p, stream);
+            case 128: return launch_simt_t<T, 128, SPLIT>(p, stream);
+        }
+    } else {
+        switch (p.D) {
+            case 32: return launch_simt_t<T, 32, SPLIT>(p, stream);
+            case 64: return launch_simt_t<T, 64, SPLIT>(p, stream);
+            case 128: return launch_simt_t<T, 128, SPLIT>(p, stream);
+            case 256: return launch_simt_t<T, 256, SPLIT>(p, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool simt_supported(int dtype, int head_dim) {
+    if (dtype == PA_F32) return head_dim == 16 || head_dim == 32 || head_dim == 64 || head_dim == 128;
+    if (dtype == PA_F16 || dtype == PA_BF16)
+        return head_dim == 32 || head_dim == 64 || head_dim == 128 || head_dim == 256;
+    return false;
+}
+
+size_t simt_smem_bytes(int dtype, int head_dim, int table_cap) {
+    // the fixed part depends on (dtype, D) only through the P and reduction
+    // buffers; evaluate it for the matching instantiation
+    const int s = dtype == PA_F32 ? 4 : 2;
+    const size_t tile = (size_t)kTileBytes / ((size_t)head_dim * s);
+    return (size_t)kSimtWarps * kSimtStages * 2 * kTileBytes + (size_t)kSimtWarps * kSimtStages * 8 +
+           (size_t)kSimtWarps * tile * 4 + (size_t)kSimtWarps * (head_dim + 2) * 4 + 16 +
+           (size_t)table_cap * 4;
+}
+
+cudaError_t launch_decode_simt(int dtype, const DecodeParams &p, bool split, cudaStream_t stream) {
+    switch (dtype) {
+        case PA_F32:
+            return split ? launch_simt_d<float, true>(p, stream) : launch_simt_d<float, false>(p, stream);
+        case PA_F16:
+            return split ? launch_simt_d<__half, true>(p, stream) : launch_simt_d<__half, false>(p, stream);
+        case PA_BF16:
+            return split ? launch_simt_d<__nv_bfloat16, true>(p, stream)
+                         : launch_simt_d<__nv_bfloat16, false>(p, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream) {
+    const int64_t grid = (int64_t)p.B * p.H;
+    if (grid == 0) return cudaSuccess;
+    switch (dtype) {
+        case PA_F32: reduce_kernel<float><<<(unsigned)grid, 128, 0, stream>>>(p); break;
+        case PA_F16: reduce_kernel<__half><<<(unsigned)grid, 128, 0, stream>>>(p); break;
+        case PA_BF16: reduce_kernel<__nv_bfloat16><<<(unsigned)grid, 128, 0, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pa

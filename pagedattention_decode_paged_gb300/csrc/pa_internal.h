@@ -1,0 +1,81 @@
+// pa_internal.h -- parameter blocks and launcher declarations shared between
+// the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Everything a decode kernel needs, passed by value (fits the 4 KB parameter
+// space together with the tensor maps of the tensor-core path).
+struct DecodeParams {
+    const void *q;
+    void *out;                 // final mode: [B][H][D] in dtype
+    const char *k_pool;        // byte pointers into the pools
+    const char *v_pool;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    float *ws_m;               // split mode: [B][H][P]
+    float *ws_l;               // split mode: [B][H][P]
+    float *ws_acc;             // split mode: [B][H][P][D]
+    int32_t *err_word;
+    int64_t num_blocks;
+    int64_t block_stride_bytes;
+    int32_t rows_per_block;    // block_stride / head_dim (tensor-map row pitch per block)
+    int32_t B, H, Hkv, D, MB, bs;
+    int32_t partition_tokens;  // 0: whole sequence (final mode)
+    int32_t num_partitions;    // P (1 in final mode)
+    int32_t table_cap;         // block_table entries staged in shared memory
+    float scale_log2;          // scale * log2(e)
+};
+
+struct AppendParams {
+    const char *k_new;
+    const char *v_new;
+    char *k_pool;
+    char *v_pool;
+    const int32_t *block_table;
+    const int32_t *positions;
+    int32_t *err_word;
+    int64_t num_blocks;
+    int64_t block_stride_bytes;
+    int32_t B, Hkv, MB, bs;
+    int32_t row_bytes;         // head_dim * element size
+};
+
+struct ReduceParams {
+    void *out;
+    const float *ws_m;
+    const float *ws_l;
+    const float *ws_acc;
+    const int32_t *seq_lens;
+    int32_t *err_word;
+    int32_t B, H, D, MB, bs;
+    int32_t partition_tokens;
+    int32_t num_partitions;
+};
+
+// Launchers (return the launch's cudaError_t).  `split` selects the partial
+// (workspace) mode.
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+
+// SIMT decode: grid = B*H*P CTAs.  Returns cudaErrorInvalidValue if the
+// (dtype, D) pair has no instantiation.
+cudaError_t launch_decode_simt(int dtype, const DecodeParams &p, bool split,
+                               cudaStream_t stream);
+bool simt_supported(int dtype, int head_dim);
+size_t simt_smem_bytes(int dtype, int head_dim, int table_cap);
+
+// Tensor-core GQA decode: grid = B*Hkv*ceil(g/16)*P CTAs.
+cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
+                                 const CUtensorMap &vmap, int box_rows, bool split,
+                                 cudaStream_t stream);
+bool gqa_tc_supported(int dtype, int head_dim);
+
+cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,151 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every
+function include/pagedattn.h declares, and host-side validation rejects bad
+arguments before anything is enqueued.  Only calls that fail validation are
+made here (they return before touching the CUDA runtime), so no GPU is
+needed."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import pagedattention_decode_paged_gb300 as pa
+from pagedattention_decode_paged_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("paged_kv_append", "paged_attention_decode", "paged_attention_decode_partial",
+              "paged_attention_decode_reduce", "paged_attention_partial_workspace",
+              "pa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(pa.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(pa.EXPORTED) <= exported
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "pagedattn.h"\nint main(void){ pa_shape s; (void)s; return 0; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", f"-I{ROOT}/include", "-c", str(src),
+                    "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_version_and_status_strings(lib):
+    assert pa.version() == 10000
+    for s in range(6):
+        assert pa.status_string(s)
+    assert pa.status_string(0) == "ok"
+    assert "unknown" in pa.status_string(99)
+
+
+def base_shape(**over):
+    d = dict(batch=2, num_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+             max_blocks_per_seq=8, num_blocks=64, block_stride=2 * 2 * 16 * 128, dtype=pa.PA_BF16)
+    d.update(over)
+    return pa.make_shape(**d)
+
+
+def test_path_selection(lib):
+    assert pa.paged_attention_decode_path(base_shape()) == pa.PA_PATH_TENSOR_GQA
+    assert pa.paged_attention_decode_path(base_shape(num_kv_heads=8, block_stride=2 * 8 * 16 * 128)) \
+        == pa.PA_PATH_SIMT                                             # MHA
+    assert pa.paged_attention_decode_path(base_shape(dtype=pa.PA_F32)) == pa.PA_PATH_SIMT
+    assert pa.paged_attention_decode_path(base_shape(block_size=4, block_stride=2 * 2 * 4 * 128)) \
+        == pa.PA_PATH_SIMT                                             # block too small for TMA boxes
+    assert pa.paged_attention_decode_path(base_shape(head_dim=256, block_stride=2 * 2 * 16 * 256)) \
+        == pa.PA_PATH_SIMT
+    assert pa.paged_attention_decode_path(base_shape(num_heads=7)) == pa.PA_PATH_INVALID
+    assert pa.paged_attention_decode_path(base_shape(head_dim=96, block_stride=2 * 2 * 16 * 96)) \
+        == pa.PA_PATH_INVALID
+
+
+def test_workspace_size(lib):
+    s = base_shape()
+    n = pa.paged_attention_partial_workspace(s, 32)
+    P = (8 * 16 + 31) // 32
+    BH = 2 * 8
+    assert n == ((8 * BH * P + 15) // 16) * 16 + 4 * BH * P * 128
+    assert pa.paged_attention_partial_workspace(s, 0) == 0
+    assert pa.paged_attention_partial_workspace(s, 24) == 0          # not a multiple of 16
+
+
+FAKE = 1 << 20          # a 16-byte aligned address that is never dereferenced on the host
+
+
+def call_decode(lib, shape, out=FAKE, q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, sl=FAKE, scale=0.1):
+    return lib.paged_attention_decode(ctypes.byref(shape) if shape is not None else None,
+                                      out, q, kp, vp, bt, sl, scale, None, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert call_decode(lib, None) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(num_heads=7)) == pa.PA_ERR_INVALID_ARG   # H % Hkv
+    assert call_decode(lib, base_shape(dtype=7)) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(block_stride=10)) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(head_dim=96, block_stride=2 * 2 * 16 * 96)) \
+        == pa.PA_ERR_UNSUPPORTED
+    assert call_decode(lib, base_shape(), q=None) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(), out=None) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(), kp=FAKE + 8) == pa.PA_ERR_MISALIGNED
+    assert call_decode(lib, base_shape(), out=FAKE + 2) == pa.PA_ERR_MISALIGNED
+    assert call_decode(lib, base_shape(), scale=float("nan")) == pa.PA_ERR_INVALID_ARG
+    assert call_decode(lib, base_shape(block_stride=2 * 2 * 16 * 128 + 1)) == pa.PA_ERR_MISALIGNED
+    assert call_decode(lib, base_shape(max_blocks_per_seq=1 << 28, block_size=16)) == pa.PA_ERR_INVALID_ARG
+    # an empty batch is valid and enqueues nothing
+    assert call_decode(lib, base_shape(batch=0), q=None, out=None) == pa.PA_OK
+
+
+def test_append_rejects_bad_arguments(lib):
+    s = base_shape()
+    f = lib.paged_kv_append
+    assert f(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == pa.PA_ERR_MISALIGNED
+    assert f(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_split_rejects_bad_arguments(lib):
+    s = base_shape()
+    need = pa.paged_attention_partial_workspace(s, 32)
+    part = lib.paged_attention_decode_partial
+    red = lib.paged_attention_decode_reduce
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, 0.1)
+    assert part(ctypes.byref(s), *args, 24, FAKE, need, None, None) == pa.PA_ERR_INVALID_ARG
+    assert part(ctypes.byref(s), *args, 32, FAKE, need - 1, None, None) == pa.PA_ERR_WORKSPACE
+    assert part(ctypes.byref(s), *args, 32, None, need, None, None) == pa.PA_ERR_INVALID_ARG
+    assert part(ctypes.byref(s), *args, 32, FAKE + 8, need, None, None) == pa.PA_ERR_MISALIGNED
+    assert red(ctypes.byref(s), FAKE, FAKE, need - 1, FAKE, 32, None, None) == pa.PA_ERR_WORKSPACE
+    assert red(ctypes.byref(s), FAKE, FAKE, need, FAKE, 0, None, None) == pa.PA_ERR_INVALID_ARG
+    assert red(ctypes.byref(s), None, FAKE, need, FAKE, 32, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
+    monkeypatch.setattr(pa, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        pa.load()

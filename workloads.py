@@ -269,3 +269,59 @@ def unshare(w: Workload) -> Workload:
     out.NB = pool.shape[0]
     out.block_table = torch.stack(rows).to(w.block_table.device)
     return out
+
+
+def make_generic(*, B, H, Hkv, D, bs, dtype, lens, seed=0, device="cpu", poison=True,
+                 extra_blocks=3, separate_pools=False, name="generic") -> Workload:
+    """Any shape: lens (pre-append) per sequence, shuffled distinct block ids.
+
+    With separate_pools the K and V halves of each block are placed in two
+    different regions of one buffer (block_stride = Hkv*bs*D), exercising the
+    non-co-located layout.
+    """
+    gen = torch.Generator().manual_seed(seed)
+    lens = torch.as_tensor(lens, dtype=torch.int32)
+    nblk = [_ceil_div(int(L) + 1, bs) for L in lens]
+    MB = max(nblk) + 2
+    NB = sum(nblk) + extra_blocks
+    table = _alloc_tables(nblk, NB, MB, gen)
+    pool = _randn((NB, 2, Hkv, bs, D), gen, dtype, "cpu")
+    q = _randn((B, H, D), gen, dtype, "cpu")
+    k_new = _randn((B, Hkv, D), gen, dtype, "cpu")
+    v_new = _randn((B, Hkv, D), gen, dtype, "cpu")
+    w = Workload(name, B, H, Hkv, D, bs, NB, MB, dtype, lens, table, pool, q, k_new, v_new,
+                 1.0 / math.sqrt(D), {"seed": seed, "separate_pools": separate_pools})
+    if poison:
+        poison_pool(w)
+    if separate_pools:
+        w = SeparatePoolWorkload(**w.__dict__)
+    return w.to(device) if str(device) != "cpu" else w
+
+
+@dataclass
+class SeparatePoolWorkload(Workload):
+    """Same data as a co-located pool, stored as [2][NB][Hkv][bs][D]: all K
+    blocks first, then all V blocks."""
+
+    @property
+    def block_stride(self) -> int:
+        return self.Hkv * self.bs * self.D
+
+    @property
+    def v_offset(self) -> int:
+        return self.NB * self.Hkv * self.bs * self.D
+
+    def __post_init__(self):
+        if not self.meta.get("k_blocks_first"):
+            self.pool = self.pool.transpose(0, 1).contiguous()
+            self.meta = dict(self.meta, k_blocks_first=True)
+
+    def to(self, device):
+        moved = {k: (v.to(device) if isinstance(v, torch.Tensor) else v)
+                 for k, v in self.__dict__.items()}
+        return SeparatePoolWorkload(**moved)
+
+    def clone(self):
+        copied = {k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                  for k, v in self.__dict__.items()}
+        return SeparatePoolWorkload(**copied)
