@@ -1,0 +1,457 @@
+"""Benchmark of one decode step of paged attention on GB300.
+
+A step is one pass of the hot path over one batch: paged_kv_append of the
+step's K/V row for every (sequence, kv head), then paged_attention_decode
+over the L + 1 valid tokens (split-KV partial + reduce where the workload
+uses it).  The default workload is the Llama-7B-like layer: 64 sequences,
+32 heads (MHA), head_dim 128, fp16, block_size 16, lengths uniform in
+450..520, 4096-block pool with shuffled ids.
+
+Metric: algorithmic bytes of the step / step time in GB/s, where the bytes
+are the valid K/V rows read (never padding), the block_table entries the
+step needs, seq_lens, Q and O, plus the append's reads and writes.  Also
+reported: query tokens/s, microseconds per layer-step, the decode kernel's
+fraction of measured HBM bandwidth, an end-to-end figure with host buffers,
+and the CPU oracle's throughput on the host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+       [--block-size BS] [--impl reference]
+Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); attention tokens/s"
+UNIT = "GB/s"
+DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+SPLIT_PTOK = {5: 1024}          # workloads timed through the split-KV pair
+PROFILE_DIR = ROOT / "profiles"
+KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic byte counts
+# ---------------------------------------------------------------------------
+
+def decode_bytes(w, lens_after) -> int:
+    """Valid K/V rows + needed table entries + seq_lens + Q + O of one decode.
+
+    Blocks shared by several table rows are counted once (they need to cross
+    HBM once).
+    """
+    s = w.q.element_size()
+    lens = [int(x) for x in lens_after]
+    tab = w.block_table.cpu()
+    row_bytes = w.Hkv * w.D * s            # one token, all kv heads, K or V
+    seen = {}
+    for b, L in enumerate(lens):
+        for j in range(-(-L // w.bs)):
+            blk = int(tab[b, j])
+            seen[blk] = max(seen.get(blk, 0), min(w.bs, L - j * w.bs))
+    kv = 2 * row_bytes * sum(seen.values())
+    table = 4 * sum(-(-L // w.bs) for L in lens)
+    return kv + table + 4 * w.B + 2 * w.B * w.H * w.D * s
+
+
+def logical_kv_bytes(w, lens_after) -> int:
+    s = w.q.element_size()
+    return 2 * w.Hkv * w.D * s * sum(int(x) for x in lens_after)
+
+
+def append_bytes(w) -> int:
+    s = w.k_new.element_size()
+    return 2 * 2 * w.B * w.Hkv * w.D * s + 4 * w.B + 4 * w.B
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict | None:
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "out", "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes per launch from a committed ncu summary, if still current.
+
+    The summary records the sha256 of the kernel's source file; when the
+    source has changed since the counters were taken, the figure is stale
+    and None is returned.
+    """
+    src = ROOT / "pagedattention_decode_paged_gb300" / "csrc" / KERNEL_SOURCES[kernel]
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()
+    for f in sorted(PROFILE_DIR.glob(f"{kernel}*{workload}*.md")):
+        text = f.read_text()
+        m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        if m_src and m_tr and m_src.group(1) == digest:
+            return int(m_tr.group(1))
+    return None
+
+
+def local_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+def describe(w, index) -> dict:
+    lens = [int(x) for x in w.lens]
+    return {"workload": f"{w.name} (workload {index})", "batch": w.B, "num_heads": w.H,
+            "num_kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs, "num_blocks": w.NB,
+            "seq_len_min": min(lens) + 1, "seq_len_max": max(lens) + 1,
+            "seq_len_mean": round(sum(lens) / len(lens) + 1, 1),
+            "split_kv_partition": SPLIT_PTOK.get(index)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args) -> None:
+    import pagedattention_decode_paged_gb300 as pa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pa.load()
+
+    # each rank holds its own replica of the workload (weak scaling)
+    w = workloads.make_workload(args.workload, block_size=args.block_size, device=dev,
+                                seed=1000 + args.workload + 7 * rank)
+    kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
+    shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
+                          block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
+                          block_stride=w.block_stride, dtype=w.dtype)
+    path = pa.paged_attention_decode_path(shape)
+    kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
+    ptok = SPLIT_PTOK.get(args.workload)
+    positions = w.lens.clone()
+    lens_after = (w.lens + 1).clone()
+    out = torch.empty_like(w.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = (pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
+          if ptok else None)
+    stream = torch.cuda.current_stream()
+
+    def append():
+        pa.paged_kv_append(w.k_new, w.v_new, w.k_flat(), w.v_flat(), w.block_table, positions,
+                           err_word=err, **kw)
+
+    def decode():
+        if ptok:
+            pa.paged_attention_decode_partial(w.q, w.k_flat(), w.v_flat(), w.block_table,
+                                              lens_after, w.scale, ptok, ws, num_kv_heads=w.Hkv,
+                                              err_word=err, **kw)
+            pa.paged_attention_decode_reduce(out, ws, lens_after, ptok, num_kv_heads=w.Hkv,
+                                             max_blocks_per_seq=w.MB, err_word=err, **kw)
+        else:
+            pa.paged_attention_decode(out, w.q, w.k_flat(), w.v_flat(), w.block_table,
+                                      lens_after, w.scale, num_kv_heads=w.Hkv, err_word=err,
+                                      **kw)
+
+    launches_per_step = 1 + (2 if ptok else 1)
+    for _ in range(args.warmup):
+        append()
+        decode()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_gpu_index(local_rank)) as clk:
+        t0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            append()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # inputs from pinned memory, append + decode, D2H of the output
+    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "block_table")}
+    host["positions"] = positions.cpu().pin_memory()
+    host["lens_after"] = lens_after.cpu().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    Ke = max(3, min(K, 2000))
+
+    def e2e_step():
+        w.q.copy_(host["q"], non_blocking=True)
+        w.k_new.copy_(host["k_new"], non_blocking=True)
+        w.v_new.copy_(host["v_new"], non_blocking=True)
+        w.block_table.copy_(host["block_table"], non_blocking=True)
+        positions.copy_(host["positions"], non_blocking=True)
+        lens_after.copy_(host["lens_after"], non_blocking=True)
+        append()
+        decode()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during timing")
+
+    dbytes = decode_bytes(w, lens_after)
+    step_bytes = dbytes + append_bytes(w)
+    peaks = measured_peaks()
+    achieved = dbytes / (decode_ms * 1e-3) / 1e9
+    ms_step = total_ms / K
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (e2e_ms / Ke * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w.to("cpu"), lens_after.cpu(), budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        cfg = describe(w, args.workload)
+        cfg["l2"] = ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2; no flush"
+                     % (dbytes / 1e6)) if dbytes > 2 * 129e6 else "L2 flushed: no (small workload)"
+        cfg["parallelism"] = f"replicas x{world}"
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_NAME[w.dtype], "data": "synthetic (seeded N(0,1) Q/K/V, shuffled block ids)",
+            "config": cfg,
+            "tokens_per_s": round(world * w.B / (ms_step * 1e-3), 1),
+            "us_per_layer_step": round(ms_step * 1e3, 3),
+            "decode_us": round(decode_ms * 1e3, 3), "append_us": round(append_ms * 1e3, 3),
+            "decode_bytes": dbytes, "logical_kv_bytes": logical_kv_bytes(w, lens_after),
+            "decode_path": kernel,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": kernel_traffic(kernel, f"w{args.workload}"),
+                         "kernel": kernel},
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": Ke,
+                    "ms_per_step": round(e2e_ms / Ke, 6)},
+            "gpu_launches": K * launches_per_step,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(w, lens_after, seqs):
+    """Oracle decode of the sequences `seqs` (all heads); returns bytes read."""
+    import oracle
+    sub = torch.tensor(seqs, dtype=torch.long)
+    q = w.q.index_select(0, sub).contiguous()
+    table = w.block_table.index_select(0, sub).contiguous()
+    lens = lens_after.index_select(0, sub).contiguous()
+    flat = w.pool.view(-1)
+    t = time.perf_counter()
+    oracle.attention_decode(q, flat, flat[w.v_offset:], table, lens, w.scale,
+                            num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
+                            num_blocks=w.NB, threads=os.cpu_count() or 1)
+    dt = time.perf_counter() - t
+    s = w.q.element_size()
+    nbytes = sum(2 * w.Hkv * w.D * s * int(L) + 4 * -(-int(L) // w.bs) + 4 + 2 * w.H * w.D * s
+                 for L in lens)
+    return nbytes, dt
+
+
+def cpu_baseline(w, lens_after, budget_s=10.0) -> dict:
+    done_bytes, done_s, seqs = 0, 0.0, 0
+    b = 0
+    while done_s < budget_s and seqs < 50 * w.B:
+        nbytes, dt = _oracle_sample(w, lens_after, [b % w.B])
+        done_bytes += nbytes
+        done_s += dt
+        seqs += 1
+        b += 1
+    return {"value": round(done_bytes / done_s / 1e9, 4), "unit": UNIT,
+            "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"{seqs} sequence decodes (all {w.H} heads each) of the same workload, "
+                      f"fp64 C oracle with OpenMP over (sequence, kv head), {done_s:.1f} s"}
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    w = workloads.make_workload(args.workload, block_size=args.block_size, device="cpu")
+    lens_after = w.lens + 1
+    for i in range(args.warmup):
+        _oracle_sample(w, lens_after, [i % w.B])
+    total_bytes, total_s = 0, 0.0
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        nbytes, dt = _oracle_sample(w, lens_after, [i % w.B])
+        total_bytes += nbytes
+        total_s += dt
+    wall = time.perf_counter() - t_start
+    value = total_bytes / total_s / 1e9
+    cfg = describe(w, args.workload)
+    cfg["parallelism"] = "host cores"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
+        "data": "synthetic (seeded N(0,1) Q/K/V, shuffled block ids)", "config": cfg,
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": os.cpu_count() or 1,
+                         "kind": "oracle",
+                         "sample": "each step: the fp64 C oracle's decode of one sequence "
+                                   f"(all {w.H} heads) of the workload, cycling through the batch"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
