@@ -53,7 +53,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------------------------------------------
  * Ownership   Every data pointer is DEVICE memory owned by the caller.  The
- *             library never allocates, frees or retains memory.
+ *             library never allocates or frees memory at run time; the only
+ *             device memory it owns is the fixed scratch array of
+ *             paged_attention_decode_split_static.
  * Streams     Work is enqueued on `stream` (NULL = legacy default stream) and
  *             runs asynchronously; nothing synchronises the host.  The block
  *             table never round-trips to the host ([BM] s2).
@@ -227,6 +229,46 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
                                         const void *workspace, size_t workspace_bytes,
                                         const int32_t *seq_lens, int32_t partition_tokens,
                                         int32_t *err_word, pa_stream_t stream);
+
+/*
+ * paged_attention_decode_split_static -- the split-KV pair without any
+ * caller-provided workspace.
+ *
+ * The sources have no counterpart for this entry point: it exists for
+ * callers that cannot allocate device memory, e.g. code running inside a
+ * memory pool or allocator callback, a plugin handed only its input and
+ * output buffers by a host framework, or a stream being captured where an
+ * allocation would break the capture.  It computes exactly what
+ * paged_attention_decode_partial followed by paged_attention_decode_reduce
+ * compute, but keeps the partial results in a fixed scratch buffer owned by
+ * the library: a file-scope device array of PA_STATIC_SCRATCH_BYTES bytes
+ * that every GPU which loads the library holds until the process exits.
+ * The caller passes only inputs and outputs (same layouts as
+ * paged_attention_decode); the call allocates nothing.
+ *
+ * Limit: a shape whose split-KV workspace (paged_attention_partial_workspace)
+ * exceeds PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
+ * anything is enqueued; use the partial/reduce pair with your own workspace
+ * for such shapes.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * scratch array (with that device current) and caches it; make that first
+ * call before any stream capture.
+ *
+ * Sharing: all calls on a device use the same scratch array, and it keeps
+ * whatever the previous call left in it.  Nothing in it needs to start at
+ * zero: the partial pass writes every slot the reduce pass reads.  Calls
+ * that can overlap on the GPU (different streams without ordering, or
+ * several host threads) race on the array; order them on one stream or
+ * with events.
+ */
+#define PA_STATIC_SCRATCH_BYTES (8u << 20)
+pa_status paged_attention_decode_split_static(const pa_shape *shape, void *out, const void *q,
+                                              const void *k_pool, const void *v_pool,
+                                              const int32_t *block_table,
+                                              const int32_t *seq_lens, float scale,
+                                              int32_t partition_tokens, int32_t *err_word,
+                                              pa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -306,3 +306,89 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// split-KV without a caller workspace: library-owned scratch in device memory
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// The scratch array every paged_attention_decode_split_static call on a
+// device uses.  Host code only ever sees it through the address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_split_scratch[PA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_split_scratch on the current device, looked up once per
+// device and cached.  Returns nullptr (and the error) if the lookup fails.
+void *split_scratch_for_current_device(cudaError_t *err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        *err = cudaGetSymbolAddress(&addr, g_split_scratch);
+        if (*err != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = addr;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" pa_status paged_attention_decode_split_static(
+    const pa_shape *shape, void *out, const void *q, const void *k_pool, const void *v_pool,
+    const int32_t *block_table, const int32_t *seq_lens, float scale, int32_t partition_tokens,
+    int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK) return st;
+    if (partition_tokens <= 0 || partition_tokens % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    if (out == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PA_ERR_MISALIGNED;
+    const int64_t P = num_partitions(shape, partition_tokens);
+    if (P > kMaxPartitions || (int64_t)shape->batch * shape->num_heads * P > INT32_MAX)
+        return PA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(shape, P);
+    if (w.total > (size_t)PA_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    cudaError_t e;
+    char *ws = static_cast<char *>(split_scratch_for_current_device(&e));
+    if (ws == nullptr) return PA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.ws_m = reinterpret_cast<float *>(ws + w.off_m);
+    p.ws_l = reinterpret_cast<float *>(ws + w.off_l);
+    p.ws_acc = reinterpret_cast<float *>(ws + w.off_acc);
+    p.partition_tokens = partition_tokens;
+    p.num_partitions = (int32_t)P;
+    const int64_t need = partition_tokens / shape->block_size + 2;
+    p.table_cap = (int)(need < kTableCap ? need : kTableCap);
+    st = launch_decode(shape, p, true, s);
+    if (st != PA_OK) return st;
+
+    pa::ReduceParams r{};
+    r.out = out;
+    r.ws_m = p.ws_m;
+    r.ws_l = p.ws_l;
+    r.ws_acc = p.ws_acc;
+    r.seq_lens = seq_lens;
+    r.err_word = err_word;
+    r.B = shape->batch;
+    r.H = shape->num_heads;
+    r.D = shape->head_dim;
+    r.MB = shape->max_blocks_per_seq;
+    r.bs = shape->block_size;
+    r.partition_tokens = partition_tokens;
+    r.num_partitions = (int32_t)P;
+    return pa::launch_reduce(shape->dtype, r, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
