@@ -130,6 +130,9 @@ pa::DecodeParams base_params(const pa_shape *s, const void *q, const void *k_poo
     p.D = s->head_dim;
     p.MB = s->max_blocks_per_seq;
     p.bs = s->block_size;
+    p.bs_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == s->block_size) p.bs_shift = sh;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
     return p;
 }

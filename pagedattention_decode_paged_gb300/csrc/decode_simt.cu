@@ -31,9 +31,16 @@
 
 namespace pa {
 
+// Tiles in flight per warp.  Two stages keep the CTA at 72 KB of shared
+// memory so three CTAs (12 warps) share an SM.
+#ifndef PA_SIMT_STAGES
+#define PA_SIMT_STAGES 2
+#endif
 constexpr int kSimtWarps = 4;
-constexpr int kSimtStages = 3;
-constexpr int kTileBytes = 4096;  // K bytes per tile (V the same)
+constexpr int kSimtStages = PA_SIMT_STAGES;
+constexpr int kSimtMinBlocks = kSimtStages <= 2 ? 3 : 2;
+constexpr int kTileBytes = 4096;    // K bytes per tile (V the same)
+constexpr int kSimtTableCap = 1024; // table entries staged per CTA (rest read from global)
 
 template <typename T, int D>
 struct SimtCfg {
@@ -46,7 +53,7 @@ struct SimtCfg {
     static constexpr int NVALS = TILE / RPW;       // rows per lane per tile
     static constexpr int NFIN = NVALS >= LPT ? NVALS / LPT : 1;  // scores per lane after reduce
     static constexpr int LOG_LPT = LPT == 4 ? 2 : LPT == 8 ? 3 : LPT == 16 ? 4 : 5;
-    static constexpr int LOG_NVALS = NVALS == 8 ? 3 : NVALS == 4 ? 2 : NVALS == 16 ? 4 : 1;
+    static constexpr int LOG_NVALS = 3;
     static_assert(LPT == 4 || LPT == 8 || LPT == 16 || LPT == 32, "row must be 64..512 bytes");
     static_assert(NVALS == 8, "tile holds 8 rows per lane");
 };
@@ -86,12 +93,6 @@ __device__ __forceinline__ int row_of_value(int c, int k) {
     }
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
-
 template <typename T, int D>
 struct SimtSmem {
     using C = SimtCfg<T, D>;
@@ -105,7 +106,7 @@ struct SimtSmem {
 };
 
 template <typename T, int D, bool SPLIT>
-__global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_kernel(DecodeParams p) {
     using C = SimtCfg<T, D>;
     using L = SimtSmem<T, D>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -164,6 +165,14 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
     const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kSimtWarps + 1 : 0;
     const int r = lane / C::LPT;   // row group
     const int c = lane % C::LPT;   // 16-byte column
+    const int64_t head_off = (int64_t)hk * p.bs * C::ROWB;
+
+    auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow[j]; };
+    auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
+    auto bad_block = [&]() {
+        flags[0] = 1;
+        report(p.err_word, PA_DEVERR_BAD_BLOCK);
+    };
 
     // lane 0 of the warp fetches local tile k into ring slot k % kSimtStages
     auto issue = [&](int k) {
@@ -173,53 +182,64 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes);
         const uint32_t dst_v = dst_k + kTileBytes;
         const uint32_t bar = smem_u32(&bars[warp * kSimtStages + slot]);
+        const int j = p.bs_shift >= 0 ? (t0 >> p.bs_shift) : t0 / p.bs;
+        const int in_blk = t0 - j * p.bs;
+        if (in_blk + (t1 - t0) <= p.bs) {
+            // the whole tile lies in one block: one copy for K, one for V
+            const int32_t blk = lookup(j);
+            if (!good(blk)) {
+                bad_block();
+                mbar_arrive_expect_tx(bar, 0);
+                return;
+            }
+            const uint32_t n = (uint32_t)(t1 - t0) * C::ROWB;
+            mbar_arrive_expect_tx(bar, 2 * n);
+            const int64_t off = (int64_t)blk * p.block_stride_bytes + head_off + (int64_t)in_blk * C::ROWB;
+            bulk_g2s(dst_k, p.k_pool + off, n, bar);
+            bulk_g2s(dst_v, p.v_pool + off, n, bar);
+            return;
+        }
+        // the tile crosses block boundaries: one copy per block segment
         uint32_t bytes = 0;
         bool ok = true;
-        for (int t = t0; t < t1;) {
-            const int j = t / p.bs;
-            const int e = min(t1, (j + 1) * p.bs);
-            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) ok = false;
-            else bytes += (uint32_t)(e - t) * C::ROWB * 2;
-            t = e;
+        for (int t = t0, jj = j, e; t < t1; t = e, ++jj) {
+            e = min(t1, (jj + 1) * p.bs);
+            if (good(lookup(jj))) bytes += (uint32_t)(e - t) * C::ROWB * 2;
+            else ok = false;
         }
-        if (!ok) {
-            flags[0] = 1;
-            report(p.err_word, PA_DEVERR_BAD_BLOCK);
-        }
+        if (!ok) bad_block();
         mbar_arrive_expect_tx(bar, bytes);
-        for (int t = t0; t < t1;) {
-            const int j = t / p.bs;
-            const int e = min(t1, (j + 1) * p.bs);
-            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
-            if (blk >= 0 && (int64_t)blk < p.num_blocks) {
-                const int64_t off = (int64_t)blk * p.block_stride_bytes +
-                                    ((int64_t)hk * p.bs + (t - j * p.bs)) * C::ROWB;
-                const uint32_t n = (uint32_t)(e - t) * C::ROWB;
-                const uint32_t so = (uint32_t)(t - t0) * C::ROWB;
-                bulk_g2s(dst_k + so, p.k_pool + off, n, bar);
-                bulk_g2s(dst_v + so, p.v_pool + off, n, bar);
-            }
-            t = e;
+        for (int t = t0, jj = j, e; t < t1; t = e, ++jj) {
+            e = min(t1, (jj + 1) * p.bs);
+            const int32_t blk = lookup(jj);
+            if (!good(blk)) continue;
+            const int64_t off = (int64_t)blk * p.block_stride_bytes + head_off +
+                                (int64_t)(t - jj * p.bs) * C::ROWB;
+            const uint32_t n = (uint32_t)(e - t) * C::ROWB;
+            const uint32_t so = (uint32_t)(t - t0) * C::ROWB;
+            bulk_g2s(dst_k + so, p.k_pool + off, n, bar);
+            bulk_g2s(dst_v + so, p.v_pool + off, n, bar);
         }
     };
 
-    // this lane's slice of the query, in fp32
-    float qf[C::VEC];
+    // this lane's slice of the query, in fp32 pairs
+    float2 q2[C::VEC / 2];
     {
         const uint4 qv = *reinterpret_cast<const uint4 *>(
             reinterpret_cast<const char *>(p.q) + (bh * D + c * C::VEC) * C::S);
-        Elem<T>::unpack(qv, qf);
+        Elem<T>::unpack2x(qv, q2);
     }
 
     if (lane == 0)
         for (int k = 0; k < min(kSimtStages, my_tiles); ++k) issue(k);
 
     float m_run = -INFINITY;  // running max of log2-scaled scores
-    float l_run = 0.f;        // running sum of 2^(s - m_run), this lane's rows
-    float acc[C::VEC];
+    float l_run = 0.f;        // running sum of 2^(s - m_run) over this lane's row group
+    float2 acc2[C::VEC / 2];
 #pragma unroll
-    for (int e = 0; e < C::VEC; ++e) acc[e] = 0.f;
+    for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = make_float2(0.f, 0.f);
+    // P of this warp's current tile, laid out [row group][value] so that a
+    // lane reads the 8 weights of its rows with two 16-byte loads
     float *pw = pbuf + warp * C::TILE;
 
     int k = 0;
@@ -240,14 +260,13 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
         float v[C::NVALS];
 #pragma unroll
         for (int j = 0; j < C::NVALS; ++j) {
-            const int row = j * C::RPW + r;
-            const uint4 kv = *reinterpret_cast<const uint4 *>(ks + row * C::ROWB + c * 16);
-            float kf[C::VEC];
-            Elem<T>::unpack(kv, kf);
-            float s = 0.f;
+            const uint4 kv = *reinterpret_cast<const uint4 *>(ks + (j * C::RPW + r) * C::ROWB + c * 16);
+            float2 k2[C::VEC / 2];
+            Elem<T>::unpack2x(kv, k2);
+            float2 a = __fmul2_rn(q2[0], k2[0]);
 #pragma unroll
-            for (int e = 0; e < C::VEC; ++e) s = fmaf(qf[e], kf[e], s);
-            v[j] = s;
+            for (int e = 1; e < C::VEC / 2; ++e) a = __ffma2_rn(q2[e], k2[e], a);
+            v[j] = a.x + a.y;
         }
         Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
 
@@ -259,31 +278,54 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
             sc[kk] = row < nrows ? v[kk] * p.scale_log2 : -INFINITY;
             tmax = fmaxf(tmax, sc[kk]);
         }
-        tmax = warp_max(tmax);
+        tmax = warp_max_f32(tmax);
         const float m_new = fmaxf(m_run, tmax);
-        const float corr = exp2f(m_run - m_new);
+        const float corr = ex2_approx(m_run - m_new);
 #pragma unroll
-        for (int kk = 0; kk < C::NFIN; ++kk) {
-            const int row = row_of_value<C>(c, kk) * C::RPW + r;
-            pw[row] = exp2f(sc[kk] - m_new);
-        }
+        for (int kk = 0; kk < C::NFIN; ++kk)
+            pw[r * C::NVALS + row_of_value<C>(c, kk)] = ex2_approx(sc[kk] - m_new);
         __syncwarp();
-        l_run *= corr;
+        float pj[C::NVALS];
 #pragma unroll
-        for (int e = 0; e < C::VEC; ++e) acc[e] *= corr;
+        for (int j = 0; j < C::NVALS; j += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(pw + r * C::NVALS + j);
+            pj[j] = f.x;
+            pj[j + 1] = f.y;
+            pj[j + 2] = f.z;
+            pj[j + 3] = f.w;
+        }
+        const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
-        for (int j = 0; j < C::NVALS; ++j) {
-            const int row = j * C::RPW + r;
-            if (row < nrows) {
-                const float pj = pw[row];
-                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + row * C::ROWB + c * 16);
-                float vf[C::VEC];
-                Elem<T>::unpack(vv, vf);
+        for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __fmul2_rn(acc2[e], corr2);
+        float psum = 0.f;
+        if (nrows == C::TILE) {
 #pragma unroll
-                for (int e = 0; e < C::VEC; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
-                l_run += pj;
+            for (int j = 0; j < C::NVALS; ++j) {
+                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
+                float2 v2[C::VEC / 2];
+                Elem<T>::unpack2x(vv, v2);
+                const float2 p2 = make_float2(pj[j], pj[j]);
+#pragma unroll
+                for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
+                psum += pj[j];
+            }
+        } else {
+            // rows past the valid length were never fetched: skip them
+            // (their weight is 0, but the buffer holds stale data)
+#pragma unroll
+            for (int j = 0; j < C::NVALS; ++j) {
+                if (j * C::RPW + r < nrows) {
+                    const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
+                    float2 v2[C::VEC / 2];
+                    Elem<T>::unpack2x(vv, v2);
+                    const float2 p2 = make_float2(pj[j], pj[j]);
+#pragma unroll
+                    for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
+                    psum += pj[j];
+                }
             }
         }
+        l_run = fmaf(l_run, corr, psum);
         m_run = m_new;
         fence_proxy_async_smem();
         __syncwarp();
@@ -304,11 +346,17 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
     for (int o = C::LPT; o < 32; o <<= 1) {
         l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
 #pragma unroll
-        for (int e = 0; e < C::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+        for (int e = 0; e < C::VEC / 2; ++e) {
+            acc2[e].x += __shfl_xor_sync(0xffffffffu, acc2[e].x, o);
+            acc2[e].y += __shfl_xor_sync(0xffffffffu, acc2[e].y, o);
+        }
     }
     if (lane < C::LPT) {
 #pragma unroll
-        for (int e = 0; e < C::VEC; ++e) red_acc[warp * D + lane * C::VEC + e] = acc[e];
+        for (int e = 0; e < C::VEC / 2; ++e) {
+            red_acc[warp * D + lane * C::VEC + 2 * e] = acc2[e].x;
+            red_acc[warp * D + lane * C::VEC + 2 * e + 1] = acc2[e].y;
+        }
     }
     if (lane == 0) {
         red_m[warp] = m_run;
@@ -324,7 +372,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, 2) decode_simt_kernel(DecodeP
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kSimtWarps; ++w) {
-        wsc[w] = exp2f(red_m[w] - M);   // warps without tiles: 2^-inf = 0
+        wsc[w] = ex2_approx(red_m[w] - M);   // warps without tiles: 2^-inf = 0
         lsum = fmaf(red_l[w], wsc[w], lsum);
     }
     if (!SPLIT) {
@@ -387,7 +435,9 @@ __global__ void __launch_bounds__(128) reduce_kernel(ReduceParams p) {
 // ---------------------------------------------------------------------------
 
 template <typename T, int D, bool SPLIT>
-static cudaError_t launch_simt_t(const DecodeParams &p, cudaStream_t stream) {
+static cudaError_t launch_simt_t(const DecodeParams &params, cudaStream_t stream) {
+    DecodeParams p = params;
+    p.table_cap = min(p.table_cap, kSimtTableCap);
     const size_t smem = SimtSmem<T, D>::bytes(p.table_cap);
     auto kern = decode_simt_kernel<T, D, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -423,16 +473,6 @@ bool simt_supported(int dtype, int head_dim) {
     if (dtype == PA_F16 || dtype == PA_BF16)
         return head_dim == 32 || head_dim == 64 || head_dim == 128 || head_dim == 256;
     return false;
-}
-
-size_t simt_smem_bytes(int dtype, int head_dim, int table_cap) {
-    // the fixed part depends on (dtype, D) only through the P and reduction
-    // buffers; evaluate it for the matching instantiation
-    const int s = dtype == PA_F32 ? 4 : 2;
-    const size_t tile = (size_t)kTileBytes / ((size_t)head_dim * s);
-    return (size_t)kSimtWarps * kSimtStages * 2 * kTileBytes + (size_t)kSimtWarps * kSimtStages * 8 +
-           (size_t)kSimtWarps * tile * 4 + (size_t)kSimtWarps * (head_dim + 2) * 4 + 16 +
-           (size_t)table_cap * 4;
 }
 
 cudaError_t launch_decode_simt(int dtype, const DecodeParams &p, bool split, cudaStream_t stream) {

@@ -103,6 +103,24 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 
 // ---------------------------------------------------------------------------
+// fast math on the hardware units
+// ---------------------------------------------------------------------------
+
+// 2^x on the multi-function unit (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Maximum of x over the 32 lanes of the warp, in one instruction.
+__device__ __forceinline__ float warp_max_f32(float x) {
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
 // tensor-core fragments (mma.sync m16n8k16, fp32 accumulate)
 // ---------------------------------------------------------------------------
 
@@ -154,6 +172,11 @@ template <typename T> struct Elem;
 
 template <> struct Elem<float> {
     static constexpr int kDtype = PA_F32;
+    // 16 bytes -> 2 float2
+    static __device__ __forceinline__ void unpack2x(const uint4 &v, float2 *f) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
     // 16 bytes -> 4 floats
     static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
         f[0] = __uint_as_float(v.x);
@@ -167,6 +190,12 @@ template <> struct Elem<float> {
 
 template <> struct Elem<__half> {
     static constexpr int kDtype = PA_F16;
+    // 16 bytes -> 4 float2
+    static __device__ __forceinline__ void unpack2x(const uint4 &v, float2 *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+    }
     static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -192,6 +221,13 @@ template <> struct Elem<__half> {
 
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kDtype = PA_BF16;
+    // 16 bytes -> 4 float2 (bf16 is the top half of an fp32: exact)
+    static __device__ __forceinline__ void unpack2x(const uint4 &v, float2 *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
     static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

@@ -27,6 +27,7 @@ struct DecodeParams {
     int64_t block_stride_bytes;
     int32_t rows_per_block;    // block_stride / head_dim (tensor-map row pitch per block)
     int32_t B, H, Hkv, D, MB, bs;
+    int32_t bs_shift;          // log2(bs) when bs is a power of two, else -1
     int32_t partition_tokens;  // 0: whole sequence (final mode)
     int32_t num_partitions;    // P (1 in final mode)
     int32_t table_cap;         // block_table entries staged in shared memory
@@ -68,7 +69,6 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_decode_simt(int dtype, const DecodeParams &p, bool split,
                                cudaStream_t stream);
 bool simt_supported(int dtype, int head_dim);
-size_t simt_smem_bytes(int dtype, int head_dim, int table_cap);
 
 // Tensor-core GQA decode: grid = B*Hkv*ceil(g/16)*P CTAs.
 cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
