@@ -7,10 +7,6 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
-namespace pa {
-size_t gqa_tc_smem_bytes(int head_dim, int table_cap);
-}
-
 namespace {
 
 constexpr int32_t kVersion = 10000;    // 1.0.0

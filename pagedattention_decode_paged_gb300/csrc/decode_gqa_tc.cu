@@ -3,25 +3,26 @@
 // With grouped-query attention the g query heads that share one kv head all
 // read the same K and V rows, so per tile of 16 tokens the work is two small
 // dense contractions:
-//     S[h][t] = sum_d Q[h][d] K[t][d]     (heads x tokens, reduced over D)
-//     O[h][d] += sum_t P[h][t] V[t][d]    (heads x D, reduced over tokens)
-// One CTA owns one (sequence, kv head[, head group of 16][, partition]) and
-// reads each K/V row from HBM once for all g heads.  The per-block
-// decomposition and the valid-length rule are those of the SIMT kernel
-// ("KV Cache paging in LLM inference", intelliparadigm.com, s2.2; "A strange
-// KV Cache bug", dpshk.com/news/5937191, s2.4).
+//     S^T[t][h] = sum_d K[t][d] Q[h][d]      (tokens x heads, reduced over D)
+//     O^T[d][h] += sum_t V[t][d] P^T[t][h]   (D x heads, reduced over tokens)
+// One CTA owns one (sequence, kv head[, group of 16 query heads][, partition])
+// and reads each K/V row from HBM once for all heads of the group.  The
+// per-block decomposition and the valid-length rule are those of the SIMT
+// kernel ("KV Cache paging in LLM inference", intelliparadigm.com, s2.2; "A
+// strange KV Cache bug", dpshk.com/news/5937191, s2.4).
 //
-// Mapping onto mma.sync.m16n8k16 (bf16/f16 in, fp32 accumulate): the 16
-// MMA rows are query heads (g of them live, the rest zero), so the score
-// accumulator of one MMA is already laid out as the A operand of the P.V
-// MMA and P never leaves registers.  K fragments come from ldmatrix, V
-// fragments from ldmatrix.trans.
+// Mapping onto mma.sync.m16n8k16 (bf16/f16 in, fp32 accumulate): tokens are
+// the 16 MMA rows and query heads the 8 MMA columns, so a group of 8 heads
+// fills the MMA exactly.  K fragments come from ldmatrix; the score
+// accumulator, turned into 16-bit P^T, is transposed in registers with
+// movmatrix into the B operand of the P.V MMA; V^T fragments come from
+// ldmatrix.trans.  Online softmax runs per head column in the log2 domain.
 //
 // Data movement: tiles are fetched by TMA 2-D tensor copies from a tensor
 // map that views a pool as a [rows][head_dim] matrix (row = one token of one
 // kv head of one block), in boxes of 64 elements x box_rows rows with 128-byte
 // swizzling, so ldmatrix reads eight rows without bank conflicts.  Each warp
-// owns a ring of kTcStages tiles, as in the SIMT kernel.
+// owns a ring of tiles and takes every fourth tile of the sequence.
 #include <math.h>
 
 #include <type_traits>
@@ -32,15 +33,16 @@
 namespace pa {
 
 constexpr int kTcWarps = 4;
-constexpr int kTcTile = 16;  // tokens per tile (one MMA K step for P.V)
+constexpr int kTcTile = 16;        // tokens per tile (one MMA M tile)
+constexpr int kTcTableCap = 1024;  // table entries staged per CTA (rest read from global)
 
 template <int D>
 struct TcCfg {
     static constexpr int HALVES = D / 64;                // 128-byte column slabs
     static constexpr int TILE_BYTES = kTcTile * D * 2;   // K (or V) bytes per tile
-    static constexpr int STAGES = D == 64 ? 4 : 3;
-    static constexpr int KSTEPS = D / 16;                // MMA K steps of Q.K^T
-    static constexpr int NT_O = D / 8;                   // MMA N tiles of P.V
+    static constexpr int STAGES = D == 64 ? 4 : 2;       // tiles in flight per warp
+    static constexpr int KSTEPS = D / 16;                // MMA K steps of K.Q^T
+    static constexpr int MT = D / 16;                    // MMA M tiles of V^T.P^T
     static constexpr size_t kStageBytes = (size_t)kTcWarps * STAGES * 2 * TILE_BYTES;
     static constexpr size_t kRedBytes = (size_t)kTcWarps * 16 * (D + 2) * 4;
     static_assert(kRedBytes <= kStageBytes, "merge area reuses the stage buffers");
@@ -57,8 +59,9 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(half * (kTcTile * 128) + row * 128 + ((cj ^ (row & 7)) << 4));
 }
 
-template <typename T, int D, bool SPLIT>
-__global__ void __launch_bounds__(kTcWarps * 32, 2)
+// NT = head tiles of 8 (1 for groups up to 8 heads, 2 up to 16)
+template <typename T, int D, int NT, bool SPLIT>
+__global__ void __launch_bounds__(kTcWarps * 32, 3)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, DecodeParams p, int box_rows) {
     using C = TcCfg<D>;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     const int hk = unit % p.Hkv;
     const int part = unit / p.Hkv;
     const int h0 = hk * g + hg * 16;       // first query head of this CTA
-    const int nh = min(16, g - hg * 16);   // live MMA rows
+    const int nh = min(16, g - hg * 16);   // live MMA columns
     T *out = reinterpret_cast<T *>(p.out);
 
     const int32_t len = p.seq_lens[b];
@@ -123,6 +126,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kTcWarps + 1 : 0;
     const int subs = kTcTile / box_rows;   // boxes per tile per slab
 
+    auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow[j]; };
+    auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
+
+    // lane 0 of the warp fetches local tile k into ring slot k % STAGES
     auto issue = [&](int k) {
         const int t0 = t_begin + (warp + k * kTcWarps) * kTcTile;
         const int slot = k % C::STAGES;
@@ -134,10 +141,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
             if (t >= t_end) break;
-            const int j = t / p.bs;
-            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) ok = false;
-            else bytes += (uint32_t)(box_rows * 128 * C::HALVES * 2);
+            const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
+            if (good(lookup(j))) bytes += (uint32_t)(box_rows * 128 * C::HALVES * 2);
+            else ok = false;
         }
         if (!ok) {
             flags[0] = 1;
@@ -147,9 +153,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
             if (t >= t_end) break;
-            const int j = t / p.bs;
-            const int32_t blk = (j - j0 < ncache) ? tbl[j - j0] : trow[j];
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) continue;
+            const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
+            const int32_t blk = lookup(j);
+            if (!good(blk)) continue;
             const int32_t y = blk * p.rows_per_block + hk * p.bs + (t - j * p.bs);
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf) {
@@ -159,39 +165,50 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
             }
         }
     };
-
-    // Q as MMA A fragments: rows = heads h0+gid and h0+gid+8, zero past nh
-    uint32_t qa[C::KSTEPS][4];
+    // Q^T as MMA B fragments: column gid of head tile nt is head
+    // h0 + nt*8 + gid (zero past nh); k rows are head_dim
+    uint32_t qb[C::KSTEPS][NT][2];
     {
-        const char *qb = reinterpret_cast<const char *>(p.q);
-        const int64_t r0 = ((int64_t)b * p.H + h0 + gid) * D;
-        const int64_t r1 = r0 + 8 * D;
-        const bool live0 = gid < nh, live1 = gid + 8 < nh;
+        const char *qp = reinterpret_cast<const char *>(p.q);
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            const int c0 = kk * 16 + 2 * tig;
-            qa[kk][0] = live0 ? *reinterpret_cast<const uint32_t *>(qb + (r0 + c0) * 2) : 0u;
-            qa[kk][1] = live1 ? *reinterpret_cast<const uint32_t *>(qb + (r1 + c0) * 2) : 0u;
-            qa[kk][2] = live0 ? *reinterpret_cast<const uint32_t *>(qb + (r0 + c0 + 8) * 2) : 0u;
-            qa[kk][3] = live1 ? *reinterpret_cast<const uint32_t *>(qb + (r1 + c0 + 8) * 2) : 0u;
+        for (int nt = 0; nt < NT; ++nt) {
+            const bool live = nt * 8 + gid < nh;
+            const int64_t row = ((int64_t)b * p.H + h0 + nt * 8 + gid) * D;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                const int c0 = kk * 16 + 2 * tig;
+                qb[kk][nt][0] = live ? *reinterpret_cast<const uint32_t *>(qp + (row + c0) * 2) : 0u;
+                qb[kk][nt][1] = live ? *reinterpret_cast<const uint32_t *>(qp + (row + c0 + 8) * 2) : 0u;
+            }
         }
     }
 
     if (lane == 0)
         for (int k = 0; k < min(C::STAGES, my_tiles); ++k) issue(k);
 
-    float o_acc[C::NT_O][4];
+    // O^T accumulators: M tile mt, head tile nt; regs 0/1 = d row gid, 2/3 =
+    // d row gid+8; even/odd = head column 2*tig / 2*tig+1
+    float o_acc[C::MT][NT][4];
 #pragma unroll
-    for (int n = 0; n < C::NT_O; ++n)
+    for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o_acc[n][e] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max, rows gid and gid+8
-    float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_acc[mt][nt][e] = 0.f;
+    float m_run[NT][2], l_run[NT][2];   // per head column 2*tig + j of head tile nt
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            m_run[nt][j] = -INFINITY;
+            l_run[nt][j] = 0.f;
+        }
 
-    // ldmatrix lane roles
+    // ldmatrix lane roles (x4: lanes 8i..8i+7 address the rows of matrix i)
     const int mi = lane >> 3, ri = lane & 7;
-    const int k_tok = (mi >> 1) * 8 + ri, k_chunk = mi & 1;  // K: x4 = {t0-7,t8-15} x {d lo, d hi}
-    const int v_tok = (mi & 1) * 8 + ri, v_chunk = mi >> 1;  // V: x4 = {t0-7,t8-15} x {d, d+8}
+    const int a_tok = (mi & 1) * 8 + ri, a_chunk = mi >> 1;  // K: {t0-7,t8-15} x {d lo, d hi}
+    const int v_tok = (mi >> 1) * 8 + ri, v_chunk = mi & 1;  // V^T: {d lo, d hi} x {t0-7,t8-15}
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
     int k = 0;
     bool aborted = false;
@@ -220,85 +237,85 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         }
         const uint32_t ks_u = smem_u32(ks), vs_u = smem_u32(vs);
 
-        // S = Q K^T for tokens 0-7 (s[0]) and 8-15 (s[1])
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // S^T = K Q^T: rows = tokens 0-15 of the tile, columns = heads
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(ks_u + swz(k_tok, 2 * kk + k_chunk), b0, b1, b2, b3);
-            MmaOp<T>::run(s[0], qa[kk], b0, b1);
-            MmaOp<T>::run(s[1], qa[kk], b2, b3);
+            uint32_t a[4];
+            ldsm_x4(ks_u + swz(a_tok, 2 * kk + a_chunk), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(s[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
         }
 
-        // online softmax per head row, in the log2 domain
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // online softmax down each head column (log2 domain); this lane holds
+        // tokens gid (regs 0/1) and gid+8 (regs 2/3)
+        const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+        uint32_t bhi[NT][2], blo[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+            float pv[4];
+            float corr[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = nt * 8 + 2 * tig + (e & 1);
-                s[nt][e] = tok < nvalid ? s[nt][e] * p.scale_log2 : -INFINITY;
-                if (e < 2) mx0 = fmaxf(mx0, s[nt][e]);
-                else mx1 = fmaxf(mx1, s[nt][e]);
+            for (int j = 0; j < 2; ++j) {
+                const float x0 = v0 ? s[nt][j] * p.scale_log2 : -INFINITY;
+                const float x1 = v1 ? s[nt][j + 2] * p.scale_log2 : -INFINITY;
+                float mx = fmaxf(x0, x1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m_run[nt][j], mx);
+                corr[j] = ex2_approx(m_run[nt][j] - mn);
+                m_run[nt][j] = mn;
+                pv[j] = ex2_approx(x0 - mn);
+                pv[j + 2] = ex2_approx(x1 - mn);
             }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        // P as the A operand of the P.V MMA.  bf16 keeps only 8 mantissa
-        // bits, which on very short sequences moves the output by more than
-        // the accuracy target, so for bf16 P is carried as hi + lo (both
-        // bf16, about 16 bits together) and multiplied twice.
-        constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-        uint32_t phi[4], plo[4] = {0u, 0u, 0u, 0u};
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const float p00 = exp2f(s[nt][0] - mn0), p01 = exp2f(s[nt][1] - mn0);
-            const float p10 = exp2f(s[nt][2] - mn1), p11 = exp2f(s[nt][3] - mn1);
-            const uint32_t lo = Elem<T>::pack2(p00, p01);  // row gid, tokens nt*8 + 2tig..
-            const uint32_t hi = Elem<T>::pack2(p10, p11);  // row gid+8
-            phi[2 * nt] = lo;
-            phi[2 * nt + 1] = hi;
-            float a, bb, c, dd;
-            Elem<T>::unpack2(lo, a, bb);
-            Elem<T>::unpack2(hi, c, dd);
+            // 16-bit P^T fragments (row = token, columns = 2 heads), then the
+            // in-register transpose into the B operand (row = head)
+            const uint32_t h0w = Elem<T>::pack2(pv[0], pv[1]);
+            const uint32_t h1w = Elem<T>::pack2(pv[2], pv[3]);
+            bhi[nt][0] = movmatrix_trans(h0w);
+            bhi[nt][1] = movmatrix_trans(h1w);
+            float r0, r1, r2, r3;
+            Elem<T>::unpack2(h0w, r0, r1);
+            Elem<T>::unpack2(h1w, r2, r3);
             if constexpr (kSplitP) {
-                plo[2 * nt] = Elem<T>::pack2(p00 - a, p01 - bb);
-                plo[2 * nt + 1] = Elem<T>::pack2(p10 - c, p11 - dd);
-                ps0 += p00 + p01;
-                ps1 += p10 + p11;
+                // bf16 keeps 8 mantissa bits: carry the rounding error as a
+                // second bf16 term so P is good to about 16 bits
+                blo[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0] - r0, pv[1] - r1));
+                blo[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2] - r2, pv[3] - r3));
+                l_run[nt][0] = fmaf(l_run[nt][0], corr[0], pv[0] + pv[2]);
+                l_run[nt][1] = fmaf(l_run[nt][1], corr[1], pv[1] + pv[3]);
             } else {
-                ps0 += a + bb;    // normalise with exactly the weights the MMA uses
-                ps1 += c + dd;
+                blo[nt][0] = blo[nt][1] = 0u;
+                // normalise with exactly the weights the MMA uses
+                l_run[nt][0] = fmaf(l_run[nt][0], corr[0], r0 + r2);
+                l_run[nt][1] = fmaf(l_run[nt][1], corr[1], r1 + r3);
+            }
+            const float2 c2 = make_float2(corr[0], corr[1]);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                float2 lo = __fmul2_rn(make_float2(o_acc[mt][nt][0], o_acc[mt][nt][1]), c2);
+                float2 hi = __fmul2_rn(make_float2(o_acc[mt][nt][2], o_acc[mt][nt][3]), c2);
+                o_acc[mt][nt][0] = lo.x;
+                o_acc[mt][nt][1] = lo.y;
+                o_acc[mt][nt][2] = hi.x;
+                o_acc[mt][nt][3] = hi.y;
             }
         }
-        l0 = l0 * c0 + ps0;
-        l1 = l1 * c1 + ps1;
+
+        // O^T += V^T P^T, one 16-row slab of head_dim per ldmatrix
 #pragma unroll
-        for (int n = 0; n < C::NT_O; ++n) {
-            o_acc[n][0] *= c0;
-            o_acc[n][1] *= c0;
-            o_acc[n][2] *= c1;
-            o_acc[n][3] *= c1;
-        }
-        // O += P V, two 8-wide column tiles per ldmatrix
-        const uint32_t pf_hi[4] = {phi[0], phi[1], phi[2], phi[3]};
-        const uint32_t pf_lo[4] = {plo[0], plo[1], plo[2], plo[3]};
+        for (int mt = 0; mt < C::MT; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(vs_u + swz(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int n = 0; n < C::NT_O; n += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(vs_u + swz(v_tok, n + v_chunk), b0, b1, b2, b3);
-            MmaOp<T>::run(o_acc[n], pf_hi, b0, b1);
-            MmaOp<T>::run(o_acc[n + 1], pf_hi, b2, b3);
-            if constexpr (kSplitP) {
-                MmaOp<T>::run(o_acc[n], pf_lo, b0, b1);
-                MmaOp<T>::run(o_acc[n + 1], pf_lo, b2, b3);
+            for (int nt = 0; nt < NT; ++nt) {
+                MmaOp<T>::run(o_acc[mt][nt], a, bhi[nt][0], bhi[nt][1]);
+                if constexpr (kSplitP) MmaOp<T>::run(o_acc[mt][nt], a, blo[nt][0], blo[nt][1]);
             }
         }
         fence_proxy_async_smem();
@@ -314,31 +331,39 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
             mbar_wait(smem_u32(&bars[warp * C::STAGES + kk % C::STAGES]), (kk / C::STAGES) & 1);
     }
 
-    // complete the row sums across the 4 lanes of a row group
+    // complete each head column's sum over the 8 lanes that share it
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], 4);
+            l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], 8);
+            l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], 16);
+        }
 
     // merge the warps through shared memory (reusing the stage buffers)
     __syncthreads();
-    float *red_o = reinterpret_cast<float *>(stages);            // [W][16][D]
+    float *red_o = reinterpret_cast<float *>(stages);            // [W][16 heads][D]
     float *red_m = red_o + kTcWarps * 16 * D;                     // [W][16]
     float *red_l = red_m + kTcWarps * 16;                         // [W][16]
 #pragma unroll
-    for (int n = 0; n < C::NT_O; ++n) {
-        const int d = n * 8 + 2 * tig;
-        red_o[(warp * 16 + gid) * D + d] = o_acc[n][0];
-        red_o[(warp * 16 + gid) * D + d + 1] = o_acc[n][1];
-        red_o[(warp * 16 + gid + 8) * D + d] = o_acc[n][2];
-        red_o[(warp * 16 + gid + 8) * D + d + 1] = o_acc[n][3];
-    }
-    if (tig == 0) {
-        red_m[warp * 16 + gid] = m0;
-        red_m[warp * 16 + gid + 8] = m1;
-        red_l[warp * 16 + gid] = l0;
-        red_l[warp * 16 + gid + 8] = l1;
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hh = nt * 8 + 2 * tig + (e & 1);
+                const int d = mt * 16 + gid + (e >> 1) * 8;
+                red_o[(warp * 16 + hh) * D + d] = o_acc[mt][nt][e];
+            }
+    if (gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                red_m[warp * 16 + nt * 8 + 2 * tig + j] = m_run[nt][j];
+                red_l[warp * 16 + nt * 8 + 2 * tig + j] = l_run[nt][j];
+            }
     }
     __syncthreads();
 
@@ -351,7 +376,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         float a = 0.f, lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kTcWarps; ++w) {
-            const float sc = exp2f(red_m[w * 16 + row] - M);
+            const float sc = ex2_approx(red_m[w * 16 + row] - M);
             a = fmaf(red_o[(w * 16 + row) * D + d], sc, a);
             lsum = fmaf(red_l[w * 16 + row], sc, lsum);
         }
@@ -359,21 +384,23 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         if (!SPLIT) {
             out[bhr * D + d] = Elem<T>::from_float(bad ? 0.f : a / lsum);
         } else {
-            const int64_t slot = bhr * p.num_partitions + part;
-            p.ws_acc[slot * D + d] = a;
+            const int64_t ws = bhr * p.num_partitions + part;
+            p.ws_acc[ws * D + d] = a;
             if (d == 0) {
-                p.ws_m[slot] = M;
-                p.ws_l[slot] = bad ? -1.f : lsum;
+                p.ws_m[ws] = M;
+                p.ws_l[ws] = bad ? -1.f : lsum;
             }
         }
     }
 }
 
-template <typename T, int D, bool SPLIT>
-static cudaError_t launch_tc_t(const DecodeParams &p, const CUtensorMap &kmap,
+template <typename T, int D, int NT, bool SPLIT>
+static cudaError_t launch_tc_t(const DecodeParams &params, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
+    DecodeParams p = params;
+    p.table_cap = min(p.table_cap, kTcTableCap);
     const size_t smem = TcCfg<D>::bytes(p.table_cap);
-    auto kern = decode_gqa_tc_kernel<T, D, SPLIT>;
+    auto kern = decode_gqa_tc_kernel<T, D, NT, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;
@@ -383,22 +410,27 @@ static cudaError_t launch_tc_t(const DecodeParams &p, const CUtensorMap &kmap,
     return cudaGetLastError();
 }
 
+template <typename T, int D, bool SPLIT>
+static cudaError_t launch_tc_nt(const DecodeParams &p, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
+    // every CTA serves at most 16 heads; groups of up to 8 need one head tile
+    const int g = p.H / p.Hkv;
+    if (g <= 8) return launch_tc_t<T, D, 1, SPLIT>(p, kmap, vmap, box_rows, stream);
+    return launch_tc_t<T, D, 2, SPLIT>(p, kmap, vmap, box_rows, stream);
+}
+
 template <typename T, bool SPLIT>
 static cudaError_t launch_tc_d(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
     switch (p.D) {
-        case 64: return launch_tc_t<T, 64, SPLIT>(p, kmap, vmap, box_rows, stream);
-        case 128: return launch_tc_t<T, 128, SPLIT>(p, kmap, vmap, box_rows, stream);
+        case 64: return launch_tc_nt<T, 64, SPLIT>(p, kmap, vmap, box_rows, stream);
+        case 128: return launch_tc_nt<T, 128, SPLIT>(p, kmap, vmap, box_rows, stream);
     }
     return cudaErrorInvalidValue;
 }
 
 bool gqa_tc_supported(int dtype, int head_dim) {
     return (dtype == PA_F16 || dtype == PA_BF16) && (head_dim == 64 || head_dim == 128);
-}
-
-size_t gqa_tc_smem_bytes(int head_dim, int table_cap) {
-    return head_dim == 64 ? TcCfg<64>::bytes(table_cap) : TcCfg<128>::bytes(table_cap);
 }
 
 cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,

@@ -140,6 +140,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "memory");
 }
 
+// Transpose an 8x8 matrix of 16-bit elements held as a warp fragment (lane i
+// holds row i/4, columns 2(i%4) and 2(i%4)+1) into the same fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 template <typename T> struct MmaOp;
 
 template <> struct MmaOp<__nv_bfloat16> {
