@@ -185,7 +185,7 @@ def describe(w, index) -> dict:
             "num_kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs, "num_blocks": w.NB,
             "seq_len_min": min(lens) + 1, "seq_len_max": max(lens) + 1,
             "seq_len_mean": round(sum(lens) / len(lens) + 1, 1),
-            "split_kv_partition": SPLIT_PTOK.get(index)}
+            "split_kv_partition": None}
 
 
 # ---------------------------------------------------------------------------
@@ -215,7 +215,7 @@ def run_gpu(args) -> None:
                           block_stride=w.block_stride, dtype=w.dtype)
     path = pa.paged_attention_decode_path(shape)
     kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
-    ptok = SPLIT_PTOK.get(args.workload)
+    ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
     positions = w.lens.clone()
     lens_after = (w.lens + 1).clone()
     out = torch.empty_like(w.q)
@@ -330,6 +330,7 @@ def run_gpu(args) -> None:
 
     if rank == 0:
         cfg = describe(w, args.workload)
+        cfg["split_kv_partition"] = ptok
         cfg["l2"] = ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2; no flush"
                      % (dbytes / 1e6)) if dbytes > 2 * 129e6 else "L2 flushed: no (small workload)"
         cfg["parallelism"] = f"replicas x{world}"
@@ -442,6 +443,8 @@ def main() -> None:
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--split-tokens", type=int, default=None,
+                    help="split-KV partition size (0: single-pass decode); default per workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

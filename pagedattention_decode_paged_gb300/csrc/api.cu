@@ -133,9 +133,50 @@ pa::DecodeParams base_params(const pa_shape *s, const void *q, const void *k_poo
     return p;
 }
 
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+// CTAs per work unit for the single-pass decode.  When the launch has fewer
+// units than the GPU has SMs, most SMs would sit idle (or stream one long
+// unit each at a single CTA's pace), so each unit is spread over a cluster of
+// up to 8 CTAs, as far as every CTA still gets at least 16 tiles of the
+// longest possible sequence.  With more units than SMs, plain one-CTA units
+// measured faster (cluster placement and the per-CTA merge cost more than the
+// better wave fill earns).
+int choose_cluster(int64_t units, int64_t max_tiles) {
+#ifdef PA_CLUSTER_OVERRIDE
+    (void)units;
+    (void)max_tiles;
+    return PA_CLUSTER_OVERRIDE;
+#else
+    if (units >= sm_count()) return 1;
+    const int64_t c = max_tiles / 16;
+    return (int)(c < 1 ? 1 : (c > 8 ? 8 : c));
+#endif
+}
+
 // Launch the decode kernel family chosen for `s` (final or split mode).
 pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cudaStream_t stream) {
     cudaError_t e;
+    p.cluster = 1;
+    if (!split) {
+        const bool tc = tc_eligible(s);
+        const int g = s->num_heads / s->num_kv_heads;
+        const int64_t units = tc ? (int64_t)s->batch * s->num_kv_heads * ((g + 15) / 16)
+                                 : (int64_t)s->batch * s->num_heads;
+        const int tile = tc ? 16 : 4096 / (s->head_dim * elem_size(s->dtype));
+        const int64_t max_tiles = ((int64_t)s->max_blocks_per_seq * s->block_size + tile - 1) / tile;
+        p.cluster = choose_cluster(units, max_tiles);
+    }
     if (tc_eligible(s)) {
         CUtensorMap kmap, vmap;
         if (!encode_pool_map(&kmap, s, p.k_pool) || !encode_pool_map(&vmap, s, p.v_pool))

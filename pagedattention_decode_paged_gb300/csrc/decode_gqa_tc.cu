@@ -45,7 +45,8 @@ struct TcCfg {
     static constexpr int MT = D / 16;                    // MMA M tiles of V^T.P^T
     static constexpr size_t kStageBytes = (size_t)kTcWarps * STAGES * 2 * TILE_BYTES;
     static constexpr size_t kRedBytes = (size_t)kTcWarps * 16 * (D + 2) * 4;
-    static_assert(kRedBytes <= kStageBytes, "merge area reuses the stage buffers");
+    static constexpr size_t kXchgBytes = (size_t)16 * (D + 3) * 4;  // CTA result for the cluster leader
+    static_assert(kRedBytes + kXchgBytes <= kStageBytes, "merge areas reuse the stage buffers");
     static constexpr size_t kBars = (size_t)kTcWarps * STAGES * 8;
     static constexpr size_t kFixed = 1024 /*alignment slack*/ + kStageBytes + kBars + 16;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 4; }
@@ -78,9 +79,17 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     const int gid = lane >> 2;  // MMA row group
     const int tig = lane & 3;   // thread in group
 
+    // A unit may be spread over the CTAs of a thread-block cluster (final
+    // mode only); the leader merges their states through distributed shared
+    // memory.
+    const int csize = SPLIT ? 1 : (int)cluster_size();
+    const int crank = SPLIT ? 0 : (int)cluster_rank();
+    const int vwarp = crank * kTcWarps + warp;
+    const int nvw = csize * kTcWarps;
+
     const int g = p.H / p.Hkv;
     const int ngroups = (g + 15) / 16;
-    int unit = blockIdx.x;
+    int unit = blockIdx.x / csize;
     const int b = unit % p.B;
     unit /= p.B;
     const int hg = unit % ngroups;
@@ -123,7 +132,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     __syncthreads();
 
     const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
-    const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kTcWarps + 1 : 0;
+    const int my_tiles = vwarp < ntiles ? (ntiles - 1 - vwarp) / nvw + 1 : 0;
     const int subs = kTcTile / box_rows;   // boxes per tile per slab
 
     auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow[j]; };
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
 
     // lane 0 of the warp fetches local tile k into ring slot k % STAGES
     auto issue = [&](int k) {
-        const int t0 = t_begin + (warp + k * kTcWarps) * kTcTile;
+        const int t0 = t_begin + (vwarp + k * nvw) * kTcTile;
         const int slot = k % C::STAGES;
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * C::STAGES + slot) * 2) * C::TILE_BYTES);
         const uint32_t dst_v = dst_k + C::TILE_BYTES;
@@ -221,7 +230,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         }
         unsigned char *ks = stages + (size_t)((warp * C::STAGES + slot) * 2) * C::TILE_BYTES;
         unsigned char *vs = ks + C::TILE_BYTES;
-        const int t0 = t_begin + (warp + k * kTcWarps) * kTcTile;
+        const int t0 = t_begin + (vwarp + k * nvw) * kTcTile;
         const int nvalid = min(kTcTile, t_end - t0);
         if (nvalid < kTcTile) {
             // rows past the valid length hold padding (possibly never written
@@ -368,6 +377,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     __syncthreads();
 
     const bool bad = flags[0] != 0;
+    // cluster exchange area: [16 heads][D] merged acc, then M, l per head, bad
+    float *xacc = red_l + kTcWarps * 16;
+    float *xm = xacc + 16 * D;
+    float *xl = xm + 16;
+    float *xbad = xl + 16;
     for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
         const int row = i / D, d = i % D;
         float M = -INFINITY;
@@ -376,12 +390,18 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         float a = 0.f, lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kTcWarps; ++w) {
-            const float sc = ex2_approx(red_m[w * 16 + row] - M);
+            const float sc = merge_weight(red_m[w * 16 + row], M);
             a = fmaf(red_o[(w * 16 + row) * D + d], sc, a);
             lsum = fmaf(red_l[w * 16 + row], sc, lsum);
         }
         const int64_t bhr = (int64_t)b * p.H + h0 + row;
-        if (!SPLIT) {
+        if (!SPLIT && csize > 1) {
+            xacc[row * D + d] = a;
+            if (d == 0) {
+                xm[row] = M;
+                xl[row] = lsum;
+            }
+        } else if (!SPLIT) {
             out[bhr * D + d] = Elem<T>::from_float(bad ? 0.f : a / lsum);
         } else {
             const int64_t ws = bhr * p.num_partitions + part;
@@ -391,6 +411,28 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
                 p.ws_l[ws] = bad ? -1.f : lsum;
             }
         }
+    }
+    if (!SPLIT && csize > 1) {
+        if (threadIdx.x == 0) xbad[0] = bad ? 1.f : 0.f;
+        cluster_sync();
+        if (crank == 0) {
+            bool badc = false;
+            for (int r = 0; r < csize; ++r) badc |= dsmem_ld_f32(dsmem_addr(xbad, r)) != 0.f;
+            for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
+                const int row = i / D, d = i % D;
+                float Mc = -INFINITY;
+                for (int r = 0; r < csize; ++r) Mc = fmaxf(Mc, dsmem_ld_f32(dsmem_addr(&xm[row], r)));
+                float a = 0.f, lc = 0.f;
+                for (int r = 0; r < csize; ++r) {
+                    const float sc = merge_weight(dsmem_ld_f32(dsmem_addr(&xm[row], r)), Mc);
+                    a = fmaf(dsmem_ld_f32(dsmem_addr(&xacc[row * D + d], r)), sc, a);
+                    lc = fmaf(dsmem_ld_f32(dsmem_addr(&xl[row], r)), sc, lc);
+                }
+                out[((int64_t)b * p.H + h0 + row) * D + d] = Elem<T>::from_float(badc ? 0.f : a / lc);
+            }
+        }
+        // keep every CTA's shared memory alive until the leader has read it
+        cluster_sync();
     }
 }
 
@@ -404,10 +446,10 @@ static cudaError_t launch_tc_t(const DecodeParams &params, const CUtensorMap &km
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;
-    const int64_t grid = (int64_t)p.B * p.Hkv * ((g + 15) / 16) * p.num_partitions;
+    const int cluster = SPLIT ? 1 : max(1, p.cluster);
+    const int64_t grid = (int64_t)p.B * p.Hkv * ((g + 15) / 16) * p.num_partitions * cluster;
     if (grid == 0) return cudaSuccess;
-    kern<<<(unsigned)grid, kTcWarps * 32, smem, stream>>>(kmap, vmap, p, box_rows);
-    return cudaGetLastError();
+    return launch_clustered(kern, grid, kTcWarps * 32, smem, cluster, stream, kmap, vmap, p, box_rows);
 }
 
 template <typename T, int D, bool SPLIT>

@@ -101,7 +101,8 @@ struct SimtSmem {
     static constexpr size_t kP = (size_t)kSimtWarps * C::TILE * 4;
     static constexpr size_t kRed = (size_t)kSimtWarps * (D + 2) * 4;
     static constexpr size_t kFlags = 16;
-    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags;
+    static constexpr size_t kXchg = (size_t)(D + 4) * 4;   // CTA result read by the cluster leader
+    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags + kXchg;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 4; }
 };
 
@@ -117,14 +118,24 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     float *red_l = red_m + kSimtWarps;
     float *red_acc = red_l + kSimtWarps;
     int *flags = reinterpret_cast<int *>(smem + L::kStages + L::kBars + L::kP + L::kRed);
+    float *xchg = reinterpret_cast<float *>(smem + L::kStages + L::kBars + L::kP + L::kRed + L::kFlags);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kFixed);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // A unit may be spread over the CTAs of a thread-block cluster (final
+    // mode only): its tiles go round-robin to the csize*kSimtWarps warps of
+    // the cluster, and the leader merges the CTAs' softmax states through
+    // distributed shared memory.
+    const int csize = SPLIT ? 1 : (int)cluster_size();
+    const int crank = SPLIT ? 0 : (int)cluster_rank();
+    const int vwarp = crank * kSimtWarps + warp;    // warp index within the cluster
+    const int nvw = csize * kSimtWarps;             // warps sharing the unit
+
     // unit = (b fastest, then h, then partition): CTAs that read the same
     // shared prefix blocks for different sequences run side by side.
-    int unit = blockIdx.x;
+    int unit = blockIdx.x / csize;
     const int b = unit % p.B;
     unit /= p.B;
     const int h = unit % p.H;
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     __syncthreads();
 
     const int ntiles = (t_end - t_begin + C::TILE - 1) / C::TILE;
-    const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kSimtWarps + 1 : 0;
+    const int my_tiles = vwarp < ntiles ? (ntiles - 1 - vwarp) / nvw + 1 : 0;
     const int r = lane / C::LPT;   // row group
     const int c = lane % C::LPT;   // 16-byte column
     const int64_t head_off = (int64_t)hk * p.bs * C::ROWB;
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
 
     // lane 0 of the warp fetches local tile k into ring slot k % kSimtStages
     auto issue = [&](int k) {
-        const int t0 = t_begin + (warp + k * kSimtWarps) * C::TILE;
+        const int t0 = t_begin + (vwarp + k * nvw) * C::TILE;
         const int t1 = min(t0 + C::TILE, t_end);
         const int slot = k % kSimtStages;
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes);
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
         }
         const unsigned char *ks = stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes;
         const unsigned char *vs = ks + kTileBytes;
-        const int t0 = t_begin + (warp + k * kSimtWarps) * C::TILE;
+        const int t0 = t_begin + (vwarp + k * nvw) * C::TILE;
         const int nrows = min(C::TILE, t_end - t0);
 
         // scores: partial dot products of 8 rows, then the butterfly
@@ -372,10 +383,46 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kSimtWarps; ++w) {
-        wsc[w] = ex2_approx(red_m[w] - M);   // warps without tiles: 2^-inf = 0
+        wsc[w] = merge_weight(red_m[w], M);   // warps without tiles weigh 0
         lsum = fmaf(red_l[w], wsc[w], lsum);
     }
-    if (!SPLIT) {
+    if (!SPLIT && csize > 1) {
+        // publish this CTA's state, then the leader merges the cluster
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSimtWarps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
+            xchg[d] = a;
+        }
+        if (threadIdx.x == 0) {
+            xchg[D] = M;
+            xchg[D + 1] = lsum;
+            xchg[D + 2] = bad ? 1.f : 0.f;
+        }
+        cluster_sync();
+        if (crank == 0) {
+            float Mc = -INFINITY;
+            bool badc = false;
+            for (int r = 0; r < csize; ++r) {
+                Mc = fmaxf(Mc, dsmem_ld_f32(dsmem_addr(&xchg[D], r)));
+                badc |= dsmem_ld_f32(dsmem_addr(&xchg[D + 2], r)) != 0.f;
+            }
+            float lc = 0.f;
+            for (int r = 0; r < csize; ++r)
+                lc = fmaf(dsmem_ld_f32(dsmem_addr(&xchg[D + 1], r)),
+                          merge_weight(dsmem_ld_f32(dsmem_addr(&xchg[D], r)), Mc), lc);
+            const float inv = 1.f / lc;
+            for (int d = threadIdx.x; d < D; d += blockDim.x) {
+                float a = 0.f;
+                for (int r = 0; r < csize; ++r)
+                    a = fmaf(dsmem_ld_f32(dsmem_addr(&xchg[d], r)),
+                             merge_weight(dsmem_ld_f32(dsmem_addr(&xchg[D], r)), Mc), a);
+                out[bh * D + d] = Elem<T>::from_float(badc ? 0.f : a * inv);
+            }
+        }
+        // keep every CTA's shared memory alive until the leader has read it
+        cluster_sync();
+    } else if (!SPLIT) {
         const float inv = 1.f / lsum;
         for (int d = threadIdx.x; d < D; d += blockDim.x) {
             float a = 0.f;
@@ -442,10 +489,10 @@ static cudaError_t launch_simt_t(const DecodeParams &params, cudaStream_t stream
     auto kern = decode_simt_kernel<T, D, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)p.B * p.H * p.num_partitions;
+    const int cluster = SPLIT ? 1 : max(1, p.cluster);
+    const int64_t grid = (int64_t)p.B * p.H * p.num_partitions * cluster;
     if (grid == 0) return cudaSuccess;
-    kern<<<(unsigned)grid, kSimtWarps * 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_clustered(kern, grid, kSimtWarps * 32, smem, cluster, stream, p);
 }
 
 template <typename T, bool SPLIT>

@@ -103,6 +103,48 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters and distributed shared memory
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes before
+// the barrier with reads after it across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
 // fast math on the hardware units
 // ---------------------------------------------------------------------------
 
@@ -111,6 +153,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Weight 2^(m - M) of a softmax state with running max m when merged into a
+// state with max M >= m; an empty state (m = -inf) weighs exactly 0 even
+// when M is -inf too.
+__device__ __forceinline__ float merge_weight(float m, float M) {
+    return m == -INFINITY ? 0.f : ex2_approx(m - M);
 }
 
 // Maximum of x over the 32 lanes of the warp, in one instruction.

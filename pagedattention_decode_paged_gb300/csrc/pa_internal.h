@@ -31,6 +31,7 @@ struct DecodeParams {
     int32_t partition_tokens;  // 0: whole sequence (final mode)
     int32_t num_partitions;    // P (1 in final mode)
     int32_t table_cap;         // block_table entries staged in shared memory
+    int32_t cluster;           // CTAs per unit in final mode (thread-block cluster), 1 = none
     float scale_log2;          // scale * log2(e)
 };
 
@@ -59,6 +60,30 @@ struct ReduceParams {
     int32_t partition_tokens;
     int32_t num_partitions;
 };
+
+// Launch `kern` on grid x block threads, as thread-block clusters of
+// `cluster` CTAs along x when cluster > 1 (grid must be a multiple of it).
+template <typename Kern, typename... Args>
+inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
+                                    cudaStream_t stream, Args... args) {
+    if (cluster <= 1) {
+        kern<<<(unsigned)grid, block, smem, stream>>>(args...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Launchers (return the launch's cudaError_t).  `split` selects the partial
 // (workspace) mode.

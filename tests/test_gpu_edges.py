@@ -179,3 +179,29 @@ def test_huge_scores_stay_finite():
                                seed=12, poison=True)
     w.q *= 100.0
     hz.run_step_and_check(w)
+
+
+# Few sequences with long contexts: the single-pass decode spreads each
+# (sequence, head) unit over a thread-block cluster and merges the CTAs'
+# partial softmax states through distributed shared memory.
+CLUSTER_LENS = [0, 1500, 37, 700, 1]
+
+
+@pytest.mark.parametrize("H,Hkv,dtype", [(4, 4, F16), (2, 2, F32), (16, 2, BF16), (8, 1, F16)])
+def test_cluster_split_single_pass(H, Hkv, dtype):
+    w = workloads.make_generic(B=len(CLUSTER_LENS), H=H, Hkv=Hkv, D=128 if dtype != F32 else 64,
+                               bs=16, dtype=dtype, lens=CLUSTER_LENS, seed=21 + H)
+    hz.run_step_and_check(w)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (16, 2)])
+def test_cluster_split_bad_entries_and_lengths(H, Hkv):
+    lens = [900, 900, 900, 900]
+    w = workloads.make_generic(B=4, H=H, Hkv=Hkv, D=128, bs=16, dtype=BF16, lens=lens, seed=31)
+    w.block_table[1, 40] = -1            # hole deep inside the valid range
+    w.block_table[2, 0] = w.NB + 3       # first block past the pool
+    out, err = _decode_only(w, [900, 900, 900, w.MB * w.bs + 5])
+    assert err & pa.DEVERR_BAD_BLOCK and err & pa.DEVERR_BAD_LEN
+    assert not out[1].any() and not out[2].any() and not out[3].any()
+    ref, _ = hz.oracle_decode(w, w.pool, torch.tensor(lens, dtype=torch.int32))
+    hz.assert_close(out[0:1], ref[0:1], BF16)
