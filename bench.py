@@ -1,9 +1,10 @@
 """Benchmark of one decode step of paged attention on GB300.
 
-A step is one pass of the hot path over one batch: paged_kv_append of the
-step's K/V row for every (sequence, kv head), then paged_attention_decode
-over the L + 1 valid tokens (split-KV partial + reduce where the workload
-uses it).  The default workload is the Llama-7B-like layer: 64 sequences,
+A step is one pass of the hot path over one batch: the append of the step's
+K/V row for every (sequence, kv head) and decode attention over the L + 1
+valid tokens, issued as one paged_attention_decode_append launch (or, with
+--unfused and for split-KV workloads, paged_kv_append followed by
+paged_attention_decode / the partial + reduce pair).  The default workload is the Llama-7B-like layer: 64 sequences,
 32 heads (MHA), head_dim 128, fp16, block_size 16, lengths uniform in
 450..520, 4096-block pool with shuffled ids.
 
@@ -88,7 +89,8 @@ def append_bytes(w) -> int:
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+                "clocks.mem")
 
 
 class ClockSampler:
@@ -120,7 +122,7 @@ class ClockSampler:
     def summary(self) -> dict | None:
         if self.proc is None:
             return None
-        sm, mx, reasons = [], None, set()
+        sm, mx, mem, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in getattr(self, "out", "").splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -129,6 +131,8 @@ class ClockSampler:
             try:
                 sm.append(float(f[1]))
                 mx = float(f[2])
+                if len(f) > 9:
+                    mem.append(float(f[9]))
             except ValueError:
                 continue
             for name, val in zip(names, f[5:9]):
@@ -137,7 +141,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "mem_mhz": statistics.median(mem) if mem else None, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -152,7 +156,7 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_traffic(kernel: str, workload: str) -> int | None:
+def kernel_traffic(kernel: str, workload: str, fused: bool = False) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if still current.
 
     The summary records the sha256 of the kernel's source file; when the
@@ -162,6 +166,8 @@ def kernel_traffic(kernel: str, workload: str) -> int | None:
     src = ROOT / "pagedattention_decode_paged_gb300" / "csrc" / KERNEL_SOURCES[kernel]
     digest = hashlib.sha256(src.read_bytes()).hexdigest()
     for f in sorted(PROFILE_DIR.glob(f"{kernel}*{workload}*.md")):
+        if ("fused" in f.name) != fused:
+            continue
         text = f.read_text()
         m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
@@ -208,7 +214,7 @@ def run_gpu(args) -> None:
 
     # each rank holds its own replica of the workload (weak scaling)
     w = workloads.make_workload(args.workload, block_size=args.block_size, device=dev,
-                                seed=1000 + args.workload + 7 * rank)
+                                seed=1000 + args.workload + 7 * rank, batch=args.batch)
     kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
     shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
                           block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
@@ -223,6 +229,8 @@ def run_gpu(args) -> None:
     ws = (pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
           if ptok else None)
     stream = torch.cuda.current_stream()
+
+    fused = not ptok and not args.unfused
 
     def append():
         pa.paged_kv_append(w.k_new, w.v_new, w.k_flat(), w.v_flat(), w.block_table, positions,
@@ -240,16 +248,29 @@ def run_gpu(args) -> None:
                                       lens_after, w.scale, num_kv_heads=w.Hkv, err_word=err,
                                       **kw)
 
-    launches_per_step = 1 + (2 if ptok else 1)
+    def step():
+        if fused:
+            pa.paged_attention_decode_append(out, w.q, w.k_new, w.v_new, w.k_flat(), w.v_flat(),
+                                             w.block_table, positions, w.scale,
+                                             num_kv_heads=w.Hkv, err_word=err, **kw)
+        else:
+            append()
+            decode()
+
+    launches_per_step = 1 if fused else 1 + (2 if ptok else 1)
     for _ in range(args.warmup):
-        append()
-        decode()
+        step()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # kernel durations are sampled live on every EVERY-th step of the timed
+    # region (events bracket those launches on the launching stream); the
+    # other steps run back to back, so that events do not sit between kernels
+    EVERY = 16
+    sampled = list(range(0, K, EVERY))
+    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if dist:
@@ -258,18 +279,26 @@ def run_gpu(args) -> None:
     with ClockSampler(local_gpu_index(local_rank)) as clk:
         t0.record(stream)
         for i in range(K):
-            ev[i][0].record(stream)
-            append()
-            ev[i][1].record(stream)
-            decode()
-            ev[i][2].record(stream)
+            e = ev.get(i)
+            if e is None:
+                step()
+                continue
+            e[0].record(stream)
+            if fused:
+                e[1].record(stream)
+                step()
+            else:
+                append()
+                e[1].record(stream)
+                decode()
+            e[2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
-    append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
+    append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
     if dist:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -292,8 +321,7 @@ def run_gpu(args) -> None:
         w.block_table.copy_(host["block_table"], non_blocking=True)
         positions.copy_(host["positions"], non_blocking=True)
         lens_after.copy_(host["lens_after"], non_blocking=True)
-        append()
-        decode()
+        step()
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -318,8 +346,10 @@ def run_gpu(args) -> None:
 
     dbytes = decode_bytes(w, lens_after)
     step_bytes = dbytes + append_bytes(w)
+    # the fused kernel also writes the appended rows into the pool
+    kbytes = dbytes + (2 * w.B * w.Hkv * w.D * w.q.element_size() if fused else 0)
     peaks = measured_peaks()
-    achieved = dbytes / (decode_ms * 1e-3) / 1e9
+    achieved = kbytes / (decode_ms * 1e-3) / 1e9
     ms_step = total_ms / K
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     e2e_value = world * step_bytes / (e2e_ms / Ke * 1e-3) / 1e9
@@ -343,13 +373,14 @@ def run_gpu(args) -> None:
             "tokens_per_s": round(world * w.B / (ms_step * 1e-3), 1),
             "us_per_layer_step": round(ms_step * 1e3, 3),
             "decode_us": round(decode_ms * 1e3, 3), "append_us": round(append_ms * 1e3, 3),
-            "decode_bytes": dbytes, "logical_kv_bytes": logical_kv_bytes(w, lens_after),
-            "decode_path": kernel,
+            "decode_bytes": dbytes, "kernel_bytes": kbytes,
+            "logical_kv_bytes": logical_kv_bytes(w, lens_after),
+            "decode_path": kernel, "fused_append": fused,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": kernel_traffic(kernel, f"w{args.workload}"),
-                         "kernel": kernel},
+                         "traffic": kernel_traffic(kernel, f"w{args.workload}", fused),
+                         "kernel": kernel, "timed_launches": len(sampled)},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": Ke,
                     "ms_per_step": round(e2e_ms / Ke, 6)},
@@ -405,7 +436,8 @@ def run_reference(args) -> None:
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    w = workloads.make_workload(args.workload, block_size=args.block_size, device="cpu")
+    w = workloads.make_workload(args.workload, block_size=args.block_size, device="cpu",
+                                batch=args.batch)
     lens_after = w.lens + 1
     for i in range(args.warmup):
         _oracle_sample(w, lens_after, [i % w.B])
@@ -442,7 +474,11 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (workloads 2-4)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time paged_kv_append and paged_attention_decode as two launches")
     ap.add_argument("--split-tokens", type=int, default=None,
                     help="split-KV partition size (0: single-pass decode); default per workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -178,6 +178,31 @@ pa_status paged_attention_decode(const pa_shape *shape, void *out, const void *q
                                  const int32_t *block_table, const int32_t *seq_lens,
                                  float scale, int32_t *err_word, pa_stream_t stream);
 
+/*
+ * paged_attention_decode_append -- paged_kv_append followed by
+ * paged_attention_decode with seq_lens = positions + 1, in one launch.
+ *
+ * For every sequence b, k_new[b][h][:] and v_new[b][h][:] are written to slot
+ * positions[b] % block_size of block block_table[b][positions[b] / block_size]
+ * exactly as paged_kv_append writes them, and out[b][:][:] is the attention
+ * of q over the positions[b] + 1 tokens that then hold the sequence ([BM]
+ * s4.4 and [BUG] s4.1 for the append, [PG] s2.2 for the attention).  The
+ * appended token is taken from k_new/v_new directly, so the output does not
+ * depend on when the pool write lands.  Results equal the two separate calls
+ * (same kernels, same arithmetic).  positions[b] outside
+ * [0, max_blocks_per_seq*block_size) gives PA_DEVERR_BAD_POS and zeros; a
+ * target entry outside [0, num_blocks) gives PA_DEVERR_BAD_BLOCK and zeros.
+ * positions is not modified.
+ *
+ * k_new, v_new: device [B][Hkv][D]; positions: device int32 [B]; the rest as
+ * paged_attention_decode.
+ */
+pa_status paged_attention_decode_append(const pa_shape *shape, void *out, const void *q,
+                                        const void *k_new, const void *v_new, void *k_pool,
+                                        void *v_pool, const int32_t *block_table,
+                                        const int32_t *positions, float scale,
+                                        int32_t *err_word, pa_stream_t stream);
+
 /* Which kernel family paged_attention_decode and _partial use for `shape`. */
 typedef enum pa_path {
     PA_PATH_INVALID = 0,     /* shape rejected                                  */

@@ -7,6 +7,7 @@ library has not been built, importing works but every call raises -- there is
 no CPU fallback.
 
 Names follow the C ABI: paged_kv_append, paged_attention_decode,
+paged_attention_decode_append (both in one launch),
 paged_attention_partial_workspace, paged_attention_decode_partial,
 paged_attention_decode_reduce, paged_attention_decode_path.
 """
@@ -27,6 +28,7 @@ PA_PATH_INVALID, PA_PATH_SIMT, PA_PATH_TENSOR_GQA = 0, 1, 2
 DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attention_decode",
+            "paged_attention_decode_append", "paged_attention_decode_split_static",
             "paged_attention_decode_path", "paged_attention_partial_workspace",
             "paged_attention_decode_partial", "paged_attention_decode_reduce")
 
@@ -69,6 +71,9 @@ def load() -> ctypes.CDLL:
             lib.paged_kv_append.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.paged_attention_decode.restype = ctypes.c_int
             lib.paged_attention_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
+            lib.paged_attention_decode_append.restype = ctypes.c_int
+            lib.paged_attention_decode_append.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32,
+                                                          vp, vp]
             lib.paged_attention_decode_path.restype = ctypes.c_int
             lib.paged_attention_decode_path.argtypes = [sp]
             lib.paged_attention_partial_workspace.restype = sz
@@ -152,6 +157,19 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_table, seq_lens, scale,
                                          _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
                                          float(scale), _ptr(err_word), _stream(stream)),
            "paged_attention_decode")
+
+
+def paged_attention_decode_append(out, q, k_new, v_new, k_pool, v_pool, block_table, positions,
+                                  scale, *, num_kv_heads, block_size, num_blocks, block_stride,
+                                  err_word=None, stream=None) -> None:
+    """Append k_new/v_new at positions[b], then attend over positions[b] + 1 tokens."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    _check(load().paged_attention_decode_append(ctypes.byref(shape), _ptr(out), _ptr(q),
+                                                _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                                _ptr(v_pool), _ptr(block_table), _ptr(positions),
+                                                float(scale), _ptr(err_word), _stream(stream)),
+           "paged_attention_decode_append")
 
 
 def paged_attention_decode_path(shape: Shape) -> int:

@@ -133,7 +133,7 @@ pa::DecodeParams base_params(const pa_shape *s, const void *q, const void *k_poo
     return p;
 }
 
-int sm_count() {
+[[maybe_unused]] int sm_count() {
     static int counts[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
@@ -270,6 +270,29 @@ pa_status paged_attention_decode(const pa_shape *shape, void *out, const void *q
     p.partition_tokens = 0;
     p.num_partitions = 1;
     p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
+    return launch_decode(shape, p, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status paged_attention_decode_append(const pa_shape *shape, void *out, const void *q,
+                                        const void *k_new, const void *v_new, void *k_pool,
+                                        void *v_pool, const int32_t *block_table,
+                                        const int32_t *positions, float scale,
+                                        int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, positions);
+    if (st != PA_OK || shape->batch == 0) return st;
+    if (out == nullptr || k_new == nullptr || v_new == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_MISALIGNED;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, positions, scale, err_word);
+    p.out = out;
+    p.partition_tokens = 0;
+    p.num_partitions = 1;
+    p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
+    p.positions = positions;
+    p.k_new = static_cast<const char *>(k_new);
+    p.v_new = static_cast<const char *>(v_new);
+    p.k_pool_w = static_cast<char *>(k_pool);
+    p.v_pool_w = static_cast<char *>(v_pool);
     return launch_decode(shape, p, false, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -12,6 +12,8 @@
 namespace pa {
 
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+    grid_dependency_wait();
+    allow_dependents();
     const int vecs = p.row_bytes / 16;                    // 16-byte vectors per row
     const int64_t total = (int64_t)p.B * p.Hkv * 2 * vecs;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -48,8 +50,7 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream) {
     if (total == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
-    append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_clustered(append_kernel, blocks, threads, 0, 1, stream, p);
 }
 
 }  // namespace pa

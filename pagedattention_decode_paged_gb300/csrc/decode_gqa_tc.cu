@@ -65,6 +65,8 @@ template <typename T, int D, int NT, bool SPLIT>
 __global__ void __launch_bounds__(kTcWarps * 32, 3)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, DecodeParams p, int box_rows) {
+    grid_dependency_wait();
+    allow_dependents();
     using C = TcCfg<D>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // 128-byte swizzled boxes need 1024-byte aligned destinations
@@ -100,9 +102,19 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     const int nh = min(16, g - hg * 16);   // live MMA columns
     T *out = reinterpret_cast<T *>(p.out);
 
-    const int32_t len = p.seq_lens[b];
-    if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
-        if (threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+    // Stage the first table entries before the length is known, so that the
+    // two dependent global loads at CTA start overlap (entries past the
+    // sequence are staged but never used).
+    const int j0 = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
+    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
+    const int nspec = min(min(p.MB - j0, p.table_cap), 64);
+    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[j0 + j];
+
+    // fused append: the sequence is its pre-step length plus the new token
+    const bool fused = !SPLIT && p.positions != nullptr;
+    const int32_t len = fused ? p.positions[b] + 1 : p.seq_lens[b];
+    if (len < (fused ? 1 : 0) || (int64_t)len > (int64_t)p.MB * p.bs) {
+        if (threadIdx.x == 0) report(p.err_word, fused ? PA_DEVERR_BAD_POS : PA_DEVERR_BAD_LEN);
         if (!SPLIT)
             for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
                 out[((int64_t)b * p.H + h0) * D + i] = Elem<T>::from_float(0.f);
@@ -117,11 +129,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         return;
     }
 
-    const int j0 = t_begin / p.bs;
     const int nblk = (t_end - 1) / p.bs + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
-    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
-    for (int j = threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
+    for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
     if (threadIdx.x == 0) {
         flags[0] = 0;
         prefetch_tensormap(&kmap);
@@ -138,6 +148,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow[j]; };
     auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
 
+    // fused append: rows before the new token come from the pool, the new
+    // token's row from k_new/v_new (never read back from the pool here)
+    const int t_pool = fused ? t_end - 1 : t_end;
+    constexpr int kChunks = D / 8;   // 16-byte chunks per row
+
     // lane 0 of the warp fetches local tile k into ring slot k % STAGES
     auto issue = [&](int k) {
         const int t0 = t_begin + (vwarp + k * nvw) * kTcTile;
@@ -149,7 +164,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         bool ok = true;
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
-            if (t >= t_end) break;
+            if (t >= t_pool) break;
             const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
             if (good(lookup(j))) bytes += (uint32_t)(box_rows * 128 * C::HALVES * 2);
             else ok = false;
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         mbar_arrive_expect_tx(bar, bytes);
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
-            if (t >= t_end) break;
+            if (t >= t_pool) break;
             const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
             const int32_t blk = lookup(j);
             if (!good(blk)) continue;
@@ -194,6 +209,33 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
 
     if (lane == 0)
         for (int k = 0; k < min(C::STAGES, my_tiles); ++k) issue(k);
+
+    // fused append (after the first copies are in flight)
+    uint4 new_k = make_uint4(0, 0, 0, 0), new_v = make_uint4(0, 0, 0, 0);
+    if (fused) {
+        const int64_t src = ((int64_t)b * p.Hkv + hk) * (D * 2) + lane * 16;
+        if (lane < kChunks && vwarp == (ntiles - 1) % nvw) {
+            new_k = *reinterpret_cast<const uint4 *>(p.k_new + src);
+            new_v = *reinterpret_cast<const uint4 *>(p.v_new + src);
+        }
+        if (warp == 0) {
+            // the append's target slot must name a pool block; one CTA per
+            // (sequence, kv head) writes the row there
+            const int pos = t_end - 1;
+            const int jn = p.bs_shift >= 0 ? (pos >> p.bs_shift) : pos / p.bs;
+            const int32_t nb = lookup(jn);
+            if (!good(nb) && lane == 0) {
+                flags[0] = 1;
+                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+            }
+            if (good(nb) && crank == 0 && hg == 0 && lane < kChunks) {
+                const int64_t dst = (int64_t)nb * p.block_stride_bytes +
+                                    ((int64_t)hk * p.bs + (pos - jn * p.bs)) * (D * 2) + lane * 16;
+                *reinterpret_cast<uint4 *>(p.k_pool_w + dst) = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                *reinterpret_cast<uint4 *>(p.v_pool_w + dst) = *reinterpret_cast<const uint4 *>(p.v_new + src);
+            }
+        }
+    }
 
     // O^T accumulators: M tile mt, head tile nt; regs 0/1 = d row gid, 2/3 =
     // d row gid+8; even/odd = head column 2*tig / 2*tig+1
@@ -241,6 +283,14 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
                 const int row = nvalid + i / (C::HALVES * 8);
                 const int ch = i % (C::HALVES * 8);
                 *reinterpret_cast<uint4 *>(vs + swz(row, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+        if (fused && t0 + nvalid == t_end) {
+            // the appended token is the last valid row of the last tile
+            if (lane < kChunks) {
+                *reinterpret_cast<uint4 *>(ks + swz(nvalid - 1, lane)) = new_k;
+                *reinterpret_cast<uint4 *>(vs + swz(nvalid - 1, lane)) = new_v;
             }
             __syncwarp();
         }

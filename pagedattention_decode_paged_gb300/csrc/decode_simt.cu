@@ -108,6 +108,8 @@ struct SimtSmem {
 
 template <typename T, int D, bool SPLIT>
 __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_kernel(DecodeParams p) {
+    grid_dependency_wait();
+    allow_dependents();
     using C = SimtCfg<T, D>;
     using L = SimtSmem<T, D>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -144,9 +146,19 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     const int64_t bh = (int64_t)b * p.H + h;
     T *out = reinterpret_cast<T *>(p.out);
 
-    const int32_t len = p.seq_lens[b];
-    if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
-        if (threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+    // Stage the first table entries before the length is known, so that the
+    // two dependent global loads at CTA start overlap (entries past the
+    // sequence are staged but never used).
+    const int j0 = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
+    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
+    const int nspec = min(min(p.MB - j0, p.table_cap), 64);
+    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[j0 + j];
+
+    // fused append: the sequence is its pre-step length plus the new token
+    const bool fused = !SPLIT && p.positions != nullptr;
+    const int32_t len = fused ? p.positions[b] + 1 : p.seq_lens[b];
+    if (len < (fused ? 1 : 0) || (int64_t)len > (int64_t)p.MB * p.bs) {
+        if (threadIdx.x == 0) report(p.err_word, fused ? PA_DEVERR_BAD_POS : PA_DEVERR_BAD_LEN);
         if (!SPLIT)
             for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
         return;
@@ -162,11 +174,9 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     }
 
     // stage the needed part of the block_table row in shared memory
-    const int j0 = t_begin / p.bs;
     const int nblk = (t_end - 1) / p.bs + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
-    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
-    for (int j = threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
+    for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
     if (threadIdx.x == 0) flags[0] = 0;
     if (threadIdx.x < kSimtWarps * kSimtStages) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
     mbar_init_fence();
@@ -180,6 +190,10 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
 
     auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow[j]; };
     auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
+    // fused append: rows before the new token come from the pool, the new
+    // token's row from k_new/v_new (never read back from the pool here)
+    const int t_pool = fused ? t_end - 1 : t_end;
+
     auto bad_block = [&]() {
         flags[0] = 1;
         report(p.err_word, PA_DEVERR_BAD_BLOCK);
@@ -188,11 +202,16 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     // lane 0 of the warp fetches local tile k into ring slot k % kSimtStages
     auto issue = [&](int k) {
         const int t0 = t_begin + (vwarp + k * nvw) * C::TILE;
-        const int t1 = min(t0 + C::TILE, t_end);
+        const int t1 = min(t0 + C::TILE, t_pool);
         const int slot = k % kSimtStages;
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * kSimtStages + slot) * 2) * kTileBytes);
         const uint32_t dst_v = dst_k + kTileBytes;
         const uint32_t bar = smem_u32(&bars[warp * kSimtStages + slot]);
+        if (t1 <= t0) {
+            // a tile holding only the appended token: nothing to fetch
+            mbar_arrive_expect_tx(bar, 0);
+            return;
+        }
         const int j = p.bs_shift >= 0 ? (t0 >> p.bs_shift) : t0 / p.bs;
         const int in_blk = t0 - j * p.bs;
         if (in_blk + (t1 - t0) <= p.bs) {
@@ -244,6 +263,35 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     if (lane == 0)
         for (int k = 0; k < min(kSimtStages, my_tiles); ++k) issue(k);
 
+    // fused append (after the first copies are in flight)
+    uint4 new_k = make_uint4(0, 0, 0, 0), new_v = make_uint4(0, 0, 0, 0);
+    if (fused) {
+        const int64_t src = ((int64_t)b * p.Hkv + hk) * C::ROWB + lane * 16;
+        const int last_owner = (ntiles - 1) % nvw;
+        if (lane < C::LPT && vwarp == last_owner) {
+            new_k = *reinterpret_cast<const uint4 *>(p.k_new + src);
+            new_v = *reinterpret_cast<const uint4 *>(p.v_new + src);
+        }
+        if (warp == 0) {
+            // the append's target slot must name a pool block; one CTA per
+            // (sequence, kv head) writes the row there
+            const int pos = t_end - 1;
+            const int jn = p.bs_shift >= 0 ? (pos >> p.bs_shift) : pos / p.bs;
+            const int32_t nb = (jn - j0 < ncache) ? tbl[jn - j0] : trow[jn];
+            const bool ok = nb >= 0 && (int64_t)nb < p.num_blocks;
+            if (!ok && lane == 0) {
+                flags[0] = 1;
+                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+            }
+            if (ok && crank == 0 && h % (p.H / p.Hkv) == 0 && lane < C::LPT) {
+                const int64_t dst = (int64_t)nb * p.block_stride_bytes + head_off +
+                                    (int64_t)(pos - jn * p.bs) * C::ROWB + lane * 16;
+                *reinterpret_cast<uint4 *>(p.k_pool_w + dst) = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                *reinterpret_cast<uint4 *>(p.v_pool_w + dst) = *reinterpret_cast<const uint4 *>(p.v_new + src);
+            }
+        }
+    }
+
     float m_run = -INFINITY;  // running max of log2-scaled scores
     float l_run = 0.f;        // running sum of 2^(s - m_run) over this lane's row group
     float2 acc2[C::VEC / 2];
@@ -266,6 +314,14 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
         const unsigned char *vs = ks + kTileBytes;
         const int t0 = t_begin + (vwarp + k * nvw) * C::TILE;
         const int nrows = min(C::TILE, t_end - t0);
+        if (fused && t0 + nrows == t_end) {
+            // the appended token is the last row of the last tile
+            if (lane < C::LPT) {
+                *reinterpret_cast<uint4 *>(const_cast<unsigned char *>(ks) + (nrows - 1) * C::ROWB + lane * 16) = new_k;
+                *reinterpret_cast<uint4 *>(const_cast<unsigned char *>(vs) + (nrows - 1) * C::ROWB + lane * 16) = new_v;
+            }
+            __syncwarp();
+        }
 
         // scores: partial dot products of 8 rows, then the butterfly
         float v[C::NVALS];
@@ -451,6 +507,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
 
 template <typename T>
 __global__ void __launch_bounds__(128) reduce_kernel(ReduceParams p) {
+    grid_dependency_wait();
+    allow_dependents();
     const int64_t bh = blockIdx.x;
     const int b = (int)(bh / p.H);
     T *out = reinterpret_cast<T *>(p.out);
@@ -539,12 +597,11 @@ cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream)
     const int64_t grid = (int64_t)p.B * p.H;
     if (grid == 0) return cudaSuccess;
     switch (dtype) {
-        case PA_F32: reduce_kernel<float><<<(unsigned)grid, 128, 0, stream>>>(p); break;
-        case PA_F16: reduce_kernel<__half><<<(unsigned)grid, 128, 0, stream>>>(p); break;
-        case PA_BF16: reduce_kernel<__nv_bfloat16><<<(unsigned)grid, 128, 0, stream>>>(p); break;
-        default: return cudaErrorInvalidValue;
+        case PA_F32: return launch_clustered(reduce_kernel<float>, grid, 128, 0, 1, stream, p);
+        case PA_F16: return launch_clustered(reduce_kernel<__half>, grid, 128, 0, 1, stream, p);
+        case PA_BF16: return launch_clustered(reduce_kernel<__nv_bfloat16>, grid, 128, 0, 1, stream, p);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -103,6 +103,24 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Every kernel of the library is launched so that it may be scheduled while
+// the previous kernel in the stream is still running.  It calls
+// grid_dependency_wait() before its first global-memory access, which waits
+// for the previous grid to complete and its writes to become visible, and
+// allow_dependents() once all of its own CTAs may be resident, so that the
+// next kernel's CTAs can take SM slots as this one's tail drains.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // thread-block clusters and distributed shared memory
 // ---------------------------------------------------------------------------
 

@@ -32,6 +32,15 @@ struct DecodeParams {
     int32_t num_partitions;    // P (1 in final mode)
     int32_t table_cap;         // block_table entries staged in shared memory
     int32_t cluster;           // CTAs per unit in final mode (thread-block cluster), 1 = none
+    // Fused append (final mode only): when positions is not null, the step's
+    // new rows k_new/v_new [B][Hkv][D] are written to slot positions[b] of
+    // the pools and attention runs over positions[b] + 1 tokens, the last of
+    // them taken straight from k_new/v_new.  seq_lens is then unused.
+    const int32_t *positions;
+    const char *k_new;
+    const char *v_new;
+    char *k_pool_w;
+    char *v_pool_w;
     float scale_log2;          // scale * log2(e)
 };
 
@@ -63,25 +72,36 @@ struct ReduceParams {
 
 // Launch `kern` on grid x block threads, as thread-block clusters of
 // `cluster` CTAs along x when cluster > 1 (grid must be a multiple of it).
+// Launches allow programmatic dependent launch: the kernel may be scheduled
+// before the previous kernel of the stream has finished, and waits for it
+// (griddepcontrol.wait) before touching global memory.
+#ifndef PA_PDL
+#define PA_PDL 1
+#endif
 template <typename Kern, typename... Args>
 inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
                                     cudaStream_t stream, Args... args) {
-    if (cluster <= 1) {
-        kern<<<(unsigned)grid, block, smem, stream>>>(args...);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(block, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (PA_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 

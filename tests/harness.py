@@ -97,3 +97,26 @@ def run_step_and_check(w, *, split_ptok=None):
     ref, e = oracle_decode(w, ref_pool, w.lens + 1)
     assert not e.any()
     return assert_close(out, ref, w.dtype, w.name)
+
+
+def gpu_fused(g, positions, err, out=None):
+    out = torch.empty_like(g.q) if out is None else out
+    pa.paged_attention_decode_append(out, g.q, g.k_new, g.v_new, g.k_flat(), g.v_flat(),
+                                     g.block_table, positions, g.scale, num_kv_heads=g.Hkv,
+                                     err_word=err, **kw(g))
+    return out
+
+
+def run_fused_step_and_check(w):
+    """paged_attention_decode_append on the GPU vs the oracle's append then decode."""
+    g = w.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_fused(g, g.lens, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+    ref_pool, e = oracle_append(w)
+    assert not e.any()
+    assert torch.equal(int_view(g.pool.cpu()), int_view(ref_pool)), "append not bit-exact"
+    ref, e = oracle_decode(w, ref_pool, w.lens + 1)
+    assert not e.any()
+    return out, assert_close(out, ref, w.dtype, w.name)

@@ -205,3 +205,35 @@ def test_cluster_split_bad_entries_and_lengths(H, Hkv):
     assert not out[1].any() and not out[2].any() and not out[3].any()
     ref, _ = hz.oracle_decode(w, w.pool, torch.tensor(lens, dtype=torch.int32))
     hz.assert_close(out[0:1], ref[0:1], BF16)
+
+
+
+@pytest.mark.parametrize("H,Hkv,dtype,D,bs", [(3, 3, F32, 64, 16), (4, 4, F16, 128, 8),
+                                              (16, 2, BF16, 128, 16), (8, 2, BF16, 64, 32),
+                                              (8, 2, F32, 64, 4), (4, 4, BF16, 256, 3)])
+@pytest.mark.parametrize("lens", [LENS, CLUSTER_LENS])
+def test_fused_append_decode_shapes(H, Hkv, dtype, D, bs, lens):
+    w = workloads.make_generic(B=len(lens), H=H, Hkv=Hkv, D=D, bs=bs, dtype=dtype, lens=lens,
+                               seed=H + D + bs)
+    hz.run_fused_step_and_check(w)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (16, 2)])
+def test_fused_append_decode_errors(H, Hkv):
+    lens = [40, 40, 40, 47]
+    w = workloads.make_generic(B=4, H=H, Hkv=Hkv, D=128, bs=16, dtype=BF16, lens=lens, seed=41)
+    g = w.to("cuda")
+    before = g.pool.clone()
+    pos = torch.tensor([40, w.MB * w.bs, -1, 47], dtype=torch.int32, device="cuda")
+    g.block_table[3, 2] = w.NB + 1          # target of sequence 3's append (47 // 16 = 2)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = hz.gpu_fused(g, pos, err)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & pa.DEVERR_BAD_POS and e & pa.DEVERR_BAD_BLOCK
+    assert not out[1].any() and not out[2].any() and not out[3].any()
+    changed = (hz.int_view(g.pool) != hz.int_view(before)).reshape(w.NB, -1).any(1)
+    assert set(torch.nonzero(changed).flatten().tolist()) == {int(w.block_table[0, 2])}
+    ref_pool, _ = hz.oracle_append(w)
+    ref, _ = hz.oracle_decode(w, ref_pool, w.lens + 1)
+    hz.assert_close(out[0:1], ref[0:1], BF16)

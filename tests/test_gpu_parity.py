@@ -173,3 +173,27 @@ def test_multi_step_decode_matches_oracle_every_step(index, kwargs):
         ref, _ = hz.oracle_decode(w, ref_pool, lens + 1)
         hz.assert_close(out, ref, w.dtype, f"step {step}")
     assert torch.equal(hz.int_view(g.pool.cpu()), hz.int_view(ref_pool))
+
+
+# ---------------------------------------------------------------------------
+# the fused step: paged_attention_decode_append
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("index,bs", [(1, None), (2, None), (3, 8), (3, 64), (4, 16), (4, 256), (5, None)])
+def test_fused_append_decode_full_size(index, bs):
+    w = workloads.make_workload(index, block_size=bs, poison=True)
+    hz.run_fused_step_and_check(w)
+
+
+@pytest.mark.parametrize("index", [2, 4, 5])
+def test_fused_equals_separate_calls_bitwise(index):
+    w = workloads.make_workload(index, poison=True, **({"max_len": 4000} if index == 5 else {}))
+    a, b = w.to("cuda"), w.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fused = hz.gpu_fused(a, a.lens, err)
+    hz.gpu_append(b, b.lens, err)
+    separate = hz.gpu_decode(b, b.lens + 1, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(fused, separate)
+    assert torch.equal(hz.int_view(a.pool), hz.int_view(b.pool))

@@ -129,6 +129,19 @@ def test_append_rejects_bad_arguments(lib):
     assert f(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == pa.PA_ERR_INVALID_ARG
 
 
+def test_fused_append_decode_rejects_bad_arguments(lib):
+    f = lib.paged_attention_decode_append
+    s = base_shape()
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(None, *ok, 0.1, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), None, *ok[1:], 0.1, None, None) == pa.PA_ERR_INVALID_ARG      # out
+    assert f(ctypes.byref(s), FAKE, FAKE, None, *ok[3:], 0.1, None, None) == pa.PA_ERR_INVALID_ARG  # k_new
+    assert f(ctypes.byref(s), *ok[:7], None, 0.1, None, None) == pa.PA_ERR_INVALID_ARG     # positions
+    assert f(ctypes.byref(s), FAKE, FAKE, FAKE + 4, *ok[3:], 0.1, None, None) == pa.PA_ERR_MISALIGNED
+    assert f(ctypes.byref(s), *ok, float("inf"), None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(base_shape(batch=0)), *ok, 0.1, None, None) == pa.PA_OK
+
+
 def test_split_rejects_bad_arguments(lib):
     s = base_shape()
     need = pa.paged_attention_partial_workspace(s, 32)
