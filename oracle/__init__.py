@@ -77,6 +77,12 @@ def _lib():
                                                   vp, vp, vp, vp, i32]
             lib.pao_merge_partials.restype = None
             lib.pao_merge_partials.argtypes = [i32, i32, vp, vp, vp, vp]
+            lib.pao_kv_append_tokens.restype = i32
+            lib.pao_kv_append_tokens.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i32,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.pao_attention_decode_window.restype = i32
+            lib.pao_attention_decode_window.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i32,
+                                                        vp, vp, vp, vp, vp, dbl, i64, vp, vp, i32]
             lib.pao_kv_append.restype = i32
             lib.pao_kv_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, i32,
                                           vp, vp, vp, vp, vp, vp, vp]
@@ -234,3 +240,38 @@ def kv_append(k_new, v_new, k_pool, v_pool, block_table, positions, *, block_siz
                          _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
                          bt.ctypes.data, pos.ctypes.data, err.ctypes.data)
     return err
+
+
+def kv_append_tokens(k_new, v_new, k_pool, v_pool, block_table, positions, counts, *,
+                     block_size: int, block_stride: int, num_blocks: int):
+    """Prefill write of counts[b] tokens per sequence from a padded batch
+    k_new/v_new [B][T][Hkv][D], in place ([BUG] s2.3-2.4, s4.1)."""
+    B, T, Hkv, D = (int(s) for s in k_new.shape)
+    bt = _i32(block_table)
+    pos = _i32(positions)
+    cnt = _i32(counts)
+    MB = bt.shape[1]
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_kv_append_tokens(B, T, Hkv, D, block_size, MB, num_blocks, block_stride,
+                                _dtype_code(k_new), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                _ptr(v_pool), bt.ctypes.data, pos.ctypes.data, cnt.ctypes.data,
+                                err.ctypes.data)
+    return err
+
+
+def attention_decode_window(q, k_pool, v_pool, block_table, seq_lens, scale: float, window: int,
+                            *, num_kv_heads: int, block_size: int, block_stride: int,
+                            num_blocks: int, threads: int = 0):
+    """Decode attention over the last `window` valid tokens ([BUG] s5.3)."""
+    B, H, D = (int(s) for s in q.shape)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    MB = bt.shape[1]
+    out = np.empty((B, H, D), dtype=np.float64)
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_attention_decode_window(B, H, num_kv_heads, D, block_size, MB, num_blocks,
+                                       block_stride, _dtype_code(q), _ptr(q), _ptr(k_pool),
+                                       _ptr(v_pool), bt.ctypes.data, sl.ctypes.data,
+                                       float(scale), int(window), out.ctypes.data,
+                                       err.ctypes.data, int(threads))
+    return out, err

@@ -405,3 +405,109 @@ int pao_kv_append(int B, int Hkv, int D, int bs, int MB, int64_t NB,
     }
     return any;
 }
+
+/* ------------------------------------------------------------------------ */
+/* multi-token append: the prompt (prefill) write                            */
+/* ------------------------------------------------------------------------ */
+
+/* For every sequence b, tokens t < counts[b] of k_new/v_new [B][T][Hkv][D]
+ * (a padded batch: rows t >= counts[b] are padding and are never written,
+ * the valid-length rule of [BUG] s2.3-2.4) go to positions positions[b] + t,
+ * each through the table exactly as the one-token append places it.
+ * counts[b] outside [0, T] flags PAO_SEQ_BAD_LEN and skips the sequence;
+ * positions[b] < 0 or positions[b] + counts[b] past the table row flags
+ * PAO_SEQ_BAD_POS and skips it; a token whose target entry names no pool
+ * block is skipped and flags PAO_SEQ_BAD_BLOCK (the other tokens are
+ * written).  Returns the OR of all status bits. */
+int pao_kv_append_tokens(int B, int T, int Hkv, int D, int bs, int MB, int64_t NB,
+                         int64_t block_stride, int dtype, const void *k_new,
+                         const void *v_new, void *k_pool, void *v_pool,
+                         const int32_t *block_table, const int32_t *positions,
+                         const int32_t *counts, int32_t *seq_err)
+{
+    int s = pao_dtype_bytes(dtype);
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        seq_err[b] = 0;
+        int64_t n = counts[b];
+        int64_t start = positions[b];
+        if (n < 0 || n > T) {
+            seq_err[b] = PAO_SEQ_BAD_LEN;
+        } else if (start < 0 || start + n > (int64_t)MB * bs) {
+            seq_err[b] = PAO_SEQ_BAD_POS;
+        } else {
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t pos = start + t;
+                int64_t blk = block_table[(int64_t)b * MB + pos / bs];
+                if (blk < 0 || blk >= NB) {
+                    seq_err[b] |= PAO_SEQ_BAD_BLOCK;
+                    continue;
+                }
+                for (int hk = 0; hk < Hkv; ++hk) {
+                    int64_t dst = blk * block_stride + (int64_t)hk * bs * D + (pos % bs) * D;
+                    int64_t src = (((int64_t)b * T + t) * Hkv + hk) * D;
+                    memcpy((char *)k_pool + dst * s, (const char *)k_new + src * s, (size_t)D * s);
+                    memcpy((char *)v_pool + dst * s, (const char *)v_new + src * s, (size_t)D * s);
+                }
+            }
+        }
+        any |= seq_err[b];
+    }
+    return any;
+}
+
+/* ------------------------------------------------------------------------ */
+/* sliding-window decode ([BUG] s5.3: keep only the most recent tokens)      */
+/* ------------------------------------------------------------------------ */
+
+/* As pao_attention_decode, but each query attends only to the last `window`
+ * valid tokens [max(0, L - window), L) of its sequence.  window must be
+ * positive; a window of at least L gives the full attention. */
+int pao_attention_decode_window(int B, int H, int Hkv, int D, int bs, int MB, int64_t NB,
+                                int64_t block_stride, int dtype, const void *q,
+                                const void *k_pool, const void *v_pool,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                double scale, int64_t window, double *out,
+                                int32_t *seq_err, int nthreads)
+{
+    int group = H / Hkv;
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        seq_err[b] = validate_sequence(seq_lens[b], bs, MB, NB,
+                                       block_table + (int64_t)b * MB);
+        any |= seq_err[b];
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+        int b = (int)(u / Hkv);
+        int hk = (int)(u % Hkv);
+        int64_t len = seq_lens[b];
+        if (seq_err[b]) {
+            for (int h = hk * group; h < (hk + 1) * group; ++h)
+                for (int d = 0; d < D; ++d)
+                    out[((int64_t)b * H + h) * D + d] = 0.0;
+            continue;
+        }
+        int64_t first = len > window ? len - window : 0;
+        size_t n = (size_t)(len > 0 ? len : 1) * D;
+        double *Kc = (double *)malloc(n * sizeof(double));
+        double *Vc = (double *)malloc(n * sizeof(double));
+        double *qd = (double *)malloc((size_t)D * sizeof(double));
+        pao_gather(D, bs, Hkv, block_stride, dtype, k_pool, v_pool,
+                   block_table + (int64_t)b * MB, hk, len, Kc, Vc);
+        for (int h = hk * group; h < (hk + 1) * group; ++h) {
+            for (int d = 0; d < D; ++d)
+                qd[d] = pao_element(q, ((int64_t)b * H + h) * D + d, dtype);
+            pao_attention_contiguous(len - first, D, qd, Kc + first * D, Vc + first * D,
+                                     scale, out + ((int64_t)b * H + h) * D);
+        }
+        free(Kc);
+        free(Vc);
+        free(qd);
+    }
+    return any;
+}

@@ -501,6 +501,107 @@ def test_validation_flags_bad_tables_and_lengths():
 
 
 # ---------------------------------------------------------------------------
+# multi-token append (prefill write) and sliding-window decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_multi_token_append_equals_token_by_token(dtype):
+    """A padded batch written at once equals its valid tokens written one by
+    one; padding rows (t >= counts[b]) never reach the pool ("A strange KV
+    Cache bug", s2.3-2.4)."""
+    tdt = workloads.DTYPES[dtype]
+    B, T, Hkv, D, bs = 4, 9, 2, 8, 4
+    g = torch.Generator().manual_seed(17)
+    counts = torch.tensor([9, 0, 5, 3], dtype=torch.int32)
+    starts = torch.tensor([0, 7, 6, 13], dtype=torch.int32)
+    kn = torch.randn(B, T, Hkv, D, generator=g).to(tdt)
+    vn = torch.randn(B, T, Hkv, D, generator=g).to(tdt)
+    for b in range(B):
+        kn[b, counts[b]:] = float("nan")
+        vn[b, counts[b]:] = float("nan")
+    MB = 5
+    NB = B * MB + 2
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    table = perm[:B * MB].view(B, MB).contiguous()
+    stride = 2 * Hkv * bs * D
+    pool_a = torch.zeros(NB, 2, Hkv, bs, D, dtype=tdt)
+    pool_b = pool_a.clone()
+    fa, fb = pool_a.view(-1), pool_b.view(-1)
+    kw = dict(block_size=bs, block_stride=stride, num_blocks=NB)
+    err = oracle.kv_append_tokens(kn, vn, fa, fa[Hkv * bs * D:], table, starts, counts, **kw)
+    assert not err.any()
+    for b in range(B):
+        for t in range(int(counts[b])):
+            one = torch.zeros(B, dtype=torch.int32)
+            mask = torch.zeros(B, dtype=torch.bool)
+            mask[b] = True
+            # append only sequence b's token t: other rows get a position past the table
+            pos = torch.where(mask, starts + t, torch.full((B,), MB * bs, dtype=torch.int32))
+            e = oracle.kv_append(kn[:, t].contiguous(), vn[:, t].contiguous(), fb,
+                                 fb[Hkv * bs * D:], table, pos, **kw)
+            assert e[b] == 0
+    assert torch.equal(pool_a.view(torch.int16 if dtype != "f32" else torch.int32),
+                       pool_b.view(torch.int16 if dtype != "f32" else torch.int32))
+    assert not pool_a.float().isnan().any()
+
+
+def test_multi_token_append_flags():
+    B, T, Hkv, D, bs, MB = 4, 4, 1, 4, 4, 2
+    pool = torch.zeros(10, 2, Hkv, bs, D)
+    flat = pool.view(-1)
+    table = torch.tensor([[0, 1], [2, 3], [4, -1], [6, 7]], dtype=torch.int32)
+    kn = torch.ones(B, T, Hkv, D)
+    err = oracle.kv_append_tokens(kn, kn, flat, flat[Hkv * bs * D:], table,
+                                  torch.tensor([0, 6, 2, 0], dtype=torch.int32),
+                                  torch.tensor([5, 3, 4, 2], dtype=torch.int32),
+                                  block_size=bs, block_stride=2 * Hkv * bs * D, num_blocks=10)
+    assert err[0] == oracle.SEQ_BAD_LEN        # 5 tokens in a batch of 4
+    assert err[1] == oracle.SEQ_BAD_POS        # 6 + 3 > 2 blocks * 4 slots
+    assert err[2] == oracle.SEQ_BAD_BLOCK      # tokens 4, 5 land in the unallocated block
+    assert err[3] == 0
+    assert pool[4, :, :, 2:].all() and not pool[2:4].any()
+
+
+def test_window_decode_pins():
+    rng = np.random.default_rng(51)
+    B, H, Hkv, D, bs = 3, 4, 2, 16, 4
+    lens = np.array([1, 23, 40], dtype=np.int32)
+    K = rng.standard_normal((B, Hkv, 40, D)).astype(np.float32)
+    V = rng.standard_normal((B, Hkv, 40, D)).astype(np.float32)
+    q = rng.standard_normal((B, H, D)).astype(np.float32)
+    NB = B * 10 + 3
+    kp, vp, table, stride = scatter_to_pool(K, V, bs, NB, rng)
+    kw = dict(num_kv_heads=Hkv, block_size=bs, block_stride=stride, num_blocks=NB)
+    full, _ = oracle.attention_decode(q, kp, vp, table, lens, 0.3, **kw)
+    for W in (40, 1000):
+        o, e = oracle.attention_decode_window(q, kp, vp, table, lens, 0.3, W, **kw)
+        assert not e.any() and np.array_equal(o, full)
+    o, _ = oracle.attention_decode_window(q, kp, vp, table, lens, 0.3, 1, **kw)
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(o[b, h], V[b, h // 2, lens[b] - 1].astype(np.float64))
+    for W in (3, 7, 16):
+        o, _ = oracle.attention_decode_window(q, kp, vp, table, lens, 0.3, W, **kw)
+        ref = np.zeros_like(o)
+        for b in range(B):
+            L = int(lens[b])
+            lo = max(0, L - W)
+            for h in range(H):
+                ref[b, h] = oracle.attention_contiguous(q[b, h].astype(np.float64),
+                                                        K[b, h // 2, lo:L], V[b, h // 2, lo:L], 0.3)
+        assert np.array_equal(o, ref), W
+        sd = sdpa_reference(q.astype(np.float64),
+                            np.stack([np.pad(K[b, :, max(0, lens[b] - W):lens[b]],
+                                             ((0, 0), (0, 40 - min(W, lens[b])), (0, 0)))
+                                      for b in range(B)]).astype(np.float64),
+                            np.stack([np.pad(V[b, :, max(0, lens[b] - W):lens[b]],
+                                             ((0, 0), (0, 40 - min(W, lens[b])), (0, 0)))
+                                      for b in range(B)]).astype(np.float64),
+                            np.minimum(lens, W), 0.3)
+        np.testing.assert_allclose(o, sd, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # the battery catches plausible mistakes planted in a copy of the oracle
 # ---------------------------------------------------------------------------
 
@@ -514,6 +615,10 @@ MUTANTS = {
     "query head uses kv head": ("qd[d] = pao_element(q, ((int64_t)b * H + h) * D + d, dtype);",
                                 "qd[d] = pao_element(q, ((int64_t)b * H + hk) * D + d, dtype);"),
     "f16 exponent bias": ("expo - 25", "expo - 24"),
+    "window one token too long": ("int64_t first = len > window ? len - window : 0;",
+                                  "int64_t first = len > window ? len - window - 1 : 0;"),
+    "prefill writes padding": ("for (int64_t t = 0; t < n; ++t) {\n                int64_t pos = start + t;",
+                               "for (int64_t t = 0; t < T && start + t < (int64_t)MB * bs; ++t) {\n                int64_t pos = start + t;"),
     "one padding slot read": ("int64_t len = seq_lens[b];\n        if (seq_err[b]) {",
                               "int64_t len = seq_lens[b] + (seq_lens[b] % bs != 0);\n        if (seq_err[b]) {"),
 }
@@ -528,7 +633,9 @@ def _battery(lib) -> bool:
                  lambda: test_decode_matches_sdpa_float64(8, 1, 16),
                  lambda: test_decode_16bit_inputs_match_sdpa("f16"),
                  test_single_token_returns_v0_exactly,
-                 test_constant_values_give_that_constant]
+                 test_constant_values_give_that_constant,
+                 test_window_decode_pins,
+                 lambda: test_multi_token_append_equals_token_by_token("f32")]
         for t in tests:
             try:
                 t()
@@ -544,7 +651,8 @@ def _load_like_real(path):
     lib = ctypes.CDLL(str(path))
     for fn in ("pao_blocks_needed", "pao_kv_bytes", "pao_convert", "pao_gather",
                "pao_attention_contiguous", "pao_attention_decode", "pao_attention_partial",
-               "pao_merge_partials", "pao_kv_append"):
+               "pao_merge_partials", "pao_kv_append", "pao_kv_append_tokens",
+               "pao_attention_decode_window"):
         getattr(lib, fn).restype = getattr(real, fn).restype
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
     return lib
