@@ -203,6 +203,41 @@ pa_status paged_attention_decode_append(const pa_shape *shape, void *out, const 
                                         const int32_t *positions, float scale,
                                         int32_t *err_word, pa_stream_t stream);
 
+/*
+ * paged_kv_append_tokens -- the prompt (prefill) write of several tokens per
+ * sequence.
+ *
+ * k_new, v_new are a padded batch [B][max_tokens][Hkv][D]: rows t <
+ * counts[b] of sequence b are written to positions positions[b] + t, each
+ * through block_table as paged_kv_append places a single token, and rows t >=
+ * counts[b] are padding that never enters the cache -- the valid length, not
+ * the padded length, defines the cache contents ([BUG] s2.3-2.4, s4.1).
+ * counts[b] outside [0, max_tokens] gives PA_DEVERR_BAD_LEN and
+ * positions[b] < 0 or positions[b] + counts[b] past the table row gives
+ * PA_DEVERR_BAD_POS, both skipping the sequence; a token whose target entry
+ * is outside [0, num_blocks) is skipped with PA_DEVERR_BAD_BLOCK.  The copy
+ * is bit-exact.  positions and counts are device int32 [B].
+ */
+pa_status paged_kv_append_tokens(const pa_shape *shape, const void *k_new, const void *v_new,
+                                 int32_t max_tokens, void *k_pool, void *v_pool,
+                                 const int32_t *block_table, const int32_t *positions,
+                                 const int32_t *counts, int32_t *err_word, pa_stream_t stream);
+
+/*
+ * paged_attention_decode_window -- decode over a sliding window.
+ *
+ * As paged_attention_decode, but each query attends only to the last
+ * `window` valid tokens [max(0, L - window), L) of its sequence, the
+ * sliding-window cache policy of [BUG] s5.3; blocks wholly before the window
+ * are not read.  window must be positive; window >= L gives the full
+ * attention.
+ */
+pa_status paged_attention_decode_window(const pa_shape *shape, void *out, const void *q,
+                                        const void *k_pool, const void *v_pool,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        float scale, int32_t window, int32_t *err_word,
+                                        pa_stream_t stream);
+
 /* Which kernel family paged_attention_decode and _partial use for `shape`. */
 typedef enum pa_path {
     PA_PATH_INVALID = 0,     /* shape rejected                                  */

@@ -7,7 +7,8 @@ library has not been built, importing works but every call raises -- there is
 no CPU fallback.
 
 Names follow the C ABI: paged_kv_append, paged_attention_decode,
-paged_attention_decode_append (both in one launch),
+paged_attention_decode_append (both in one launch), paged_kv_append_tokens
+(prefill write), paged_attention_decode_window (sliding window),
 paged_attention_partial_workspace, paged_attention_decode_partial,
 paged_attention_decode_reduce, paged_attention_decode_path.
 """
@@ -29,6 +30,7 @@ DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attention_decode",
             "paged_attention_decode_append", "paged_attention_decode_split_static",
+            "paged_kv_append_tokens", "paged_attention_decode_window",
             "paged_attention_decode_path", "paged_attention_partial_workspace",
             "paged_attention_decode_partial", "paged_attention_decode_reduce")
 
@@ -74,6 +76,11 @@ def load() -> ctypes.CDLL:
             lib.paged_attention_decode_append.restype = ctypes.c_int
             lib.paged_attention_decode_append.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, f32,
                                                           vp, vp]
+            lib.paged_kv_append_tokens.restype = ctypes.c_int
+            lib.paged_kv_append_tokens.argtypes = [sp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+            lib.paged_attention_decode_window.restype = ctypes.c_int
+            lib.paged_attention_decode_window.argtypes = [sp, vp, vp, vp, vp, vp, vp, f32, i32, vp,
+                                                          vp]
             lib.paged_attention_decode_path.restype = ctypes.c_int
             lib.paged_attention_decode_path.argtypes = [sp]
             lib.paged_attention_partial_workspace.restype = sz
@@ -170,6 +177,34 @@ def paged_attention_decode_append(out, q, k_new, v_new, k_pool, v_pool, block_ta
                                                 _ptr(v_pool), _ptr(block_table), _ptr(positions),
                                                 float(scale), _ptr(err_word), _stream(stream)),
            "paged_attention_decode_append")
+
+
+def paged_kv_append_tokens(k_new, v_new, k_pool, v_pool, block_table, positions, counts, *,
+                           block_size, num_blocks, block_stride, err_word=None,
+                           stream=None) -> None:
+    """Prefill write: counts[b] rows of the padded batch k_new/v_new [B][T][Hkv][D]
+    go to positions[b] + t."""
+    B, T, Hkv, D = k_new.shape
+    shape = make_shape(batch=B, num_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=block_size,
+                       max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
+                       block_stride=block_stride, dtype=k_new.dtype)
+    _check(load().paged_kv_append_tokens(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), int(T),
+                                         _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                         _ptr(positions), _ptr(counts), _ptr(err_word),
+                                         _stream(stream)), "paged_kv_append_tokens")
+
+
+def paged_attention_decode_window(out, q, k_pool, v_pool, block_table, seq_lens, scale, window,
+                                  *, num_kv_heads, block_size, num_blocks, block_stride,
+                                  err_word=None, stream=None) -> None:
+    """Decode attention over the last `window` valid tokens of each sequence."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    _check(load().paged_attention_decode_window(ctypes.byref(shape), _ptr(out), _ptr(q),
+                                                _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                                _ptr(seq_lens), float(scale), int(window),
+                                                _ptr(err_word), _stream(stream)),
+           "paged_attention_decode_window")
 
 
 def paged_attention_decode_path(shape: Shape) -> int:

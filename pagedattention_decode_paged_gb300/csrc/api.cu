@@ -174,7 +174,9 @@ pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cuda
         const int64_t units = tc ? (int64_t)s->batch * s->num_kv_heads * ((g + 15) / 16)
                                  : (int64_t)s->batch * s->num_heads;
         const int tile = tc ? 16 : 4096 / (s->head_dim * elem_size(s->dtype));
-        const int64_t max_tiles = ((int64_t)s->max_blocks_per_seq * s->block_size + tile - 1) / tile;
+        int64_t max_len = (int64_t)s->max_blocks_per_seq * s->block_size;
+        if (p.window > 0 && p.window < max_len) max_len = p.window;
+        const int64_t max_tiles = (max_len + tile - 1) / tile;
         p.cluster = choose_cluster(units, max_tiles);
     }
     if (tc_eligible(s)) {
@@ -294,6 +296,62 @@ pa_status paged_attention_decode_append(const pa_shape *shape, void *out, const 
     p.k_pool_w = static_cast<char *>(k_pool);
     p.v_pool_w = static_cast<char *>(v_pool);
     return launch_decode(shape, p, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status paged_attention_decode_window(const pa_shape *shape, void *out, const void *q,
+                                        const void *k_pool, const void *v_pool,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        float scale, int32_t window, int32_t *err_word,
+                                        pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK) return st;
+    if (window <= 0) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    if (out == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out)) return PA_ERR_MISALIGNED;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.out = out;
+    p.partition_tokens = 0;
+    p.num_partitions = 1;
+    p.window = window;
+    p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
+    return launch_decode(shape, p, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status paged_kv_append_tokens(const pa_shape *shape, const void *k_new, const void *v_new,
+                                 int32_t max_tokens, void *k_pool, void *v_pool,
+                                 const int32_t *block_table, const int32_t *positions,
+                                 const int32_t *counts, int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (max_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0 || max_tokens == 0) return PA_OK;
+    if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        block_table == nullptr || positions == nullptr || counts == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_MISALIGNED;
+    pa::AppendParams p{};
+    p.k_new = static_cast<const char *>(k_new);
+    p.v_new = static_cast<const char *>(v_new);
+    p.k_pool = static_cast<char *>(k_pool);
+    p.v_pool = static_cast<char *>(v_pool);
+    p.block_table = block_table;
+    p.positions = positions;
+    p.counts = counts;
+    p.T = max_tokens;
+    p.err_word = err_word;
+    p.num_blocks = shape->num_blocks;
+    p.block_stride_bytes = shape->block_stride * elem_size(shape->dtype);
+    p.B = shape->batch;
+    p.Hkv = shape->num_kv_heads;
+    p.MB = shape->max_blocks_per_seq;
+    p.bs = shape->block_size;
+    p.row_bytes = shape->head_dim * elem_size(shape->dtype);
+    const cudaError_t e = pa::launch_append_tokens(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return PA_ERR_INVALID_ARG;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 size_t paged_attention_partial_workspace(const pa_shape *shape, int32_t partition_tokens) {

@@ -105,10 +105,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
     // Stage the first table entries before the length is known, so that the
     // two dependent global loads at CTA start overlap (entries past the
     // sequence are staged but never used).
-    const int j0 = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
+    // (not with a sliding window, whose first block depends on the length)
+    const int jspec = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
     const int32_t *trow = p.block_table + (int64_t)b * p.MB;
-    const int nspec = min(min(p.MB - j0, p.table_cap), 64);
-    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[j0 + j];
+    const int nspec = p.window > 0 ? 0 : min(min(p.MB - jspec, p.table_cap), 64);
+    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[jspec + j];
 
     // fused append: the sequence is its pre-step length plus the new token
     const bool fused = !SPLIT && p.positions != nullptr;
@@ -120,7 +121,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
                 out[((int64_t)b * p.H + h0) * D + i] = Elem<T>::from_float(0.f);
         return;
     }
-    const int t_begin = SPLIT ? part * p.partition_tokens : 0;
+    // sliding window: tokens before t_win are not attended; tiles start on
+    // the 16-row TMA grid at or below it and mask the rows before it
+    const int t_win = (!SPLIT && p.window > 0) ? max(0, len - p.window) : 0;
+    const int t_begin = SPLIT ? part * p.partition_tokens : (t_win & ~(kTcTile - 1));
     const int t_end = SPLIT ? min(len, t_begin + p.partition_tokens) : len;
     if (t_end <= t_begin) {
         if (!SPLIT)
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         return;
     }
 
+    const int j0 = t_begin / p.bs;
     const int nblk = (t_end - 1) / p.bs + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
     for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
@@ -274,6 +279,15 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         unsigned char *vs = ks + C::TILE_BYTES;
         const int t0 = t_begin + (vwarp + k * nvw) * kTcTile;
         const int nvalid = min(kTcTile, t_end - t0);
+        const int lo = max(0, t_win - t0);   // rows before the window (first tile only)
+        if (lo > 0) {
+            // attended weight is 0 there; keep V finite under 0 * V
+            const int nchunks = lo * C::HALVES * 8;
+            for (int i = lane; i < nchunks; i += 32)
+                *reinterpret_cast<uint4 *>(vs + swz(i / (C::HALVES * 8), i % (C::HALVES * 8))) =
+                    make_uint4(0, 0, 0, 0);
+            __syncwarp();
+        }
         if (nvalid < kTcTile) {
             // rows past the valid length hold padding (possibly never written
             // or poisoned): P is zero there, and V must be finite so that
@@ -312,7 +326,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
 
         // online softmax down each head column (log2 domain); this lane holds
         // tokens gid (regs 0/1) and gid+8 (regs 2/3)
-        const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+        const bool v0 = gid >= lo && gid < nvalid, v1 = gid + 8 >= lo && gid + 8 < nvalid;
         uint32_t bhi[NT][2], blo[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {

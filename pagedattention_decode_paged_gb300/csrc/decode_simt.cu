@@ -149,10 +149,11 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     // Stage the first table entries before the length is known, so that the
     // two dependent global loads at CTA start overlap (entries past the
     // sequence are staged but never used).
-    const int j0 = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
+    // (not with a sliding window, whose first block depends on the length)
+    const int jspec = SPLIT ? (part * p.partition_tokens) / p.bs : 0;
     const int32_t *trow = p.block_table + (int64_t)b * p.MB;
-    const int nspec = min(min(p.MB - j0, p.table_cap), 64);
-    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[j0 + j];
+    const int nspec = p.window > 0 ? 0 : min(min(p.MB - jspec, p.table_cap), 64);
+    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[jspec + j];
 
     // fused append: the sequence is its pre-step length plus the new token
     const bool fused = !SPLIT && p.positions != nullptr;
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
             for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
         return;
     }
-    const int t_begin = SPLIT ? part * p.partition_tokens : 0;
+    // sliding window: only the last `window` tokens are attended (and read)
+    const int t_begin = SPLIT ? part * p.partition_tokens : (p.window > 0 ? max(0, len - p.window) : 0);
     const int t_end = SPLIT ? min(len, t_begin + p.partition_tokens) : len;
     if (t_end <= t_begin) {
         // nothing to attend to: final mode writes zeros, split mode leaves
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     }
 
     // stage the needed part of the block_table row in shared memory
+    const int j0 = t_begin / p.bs;
     const int nblk = (t_end - 1) / p.bs + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
     for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];

@@ -41,6 +41,7 @@ struct DecodeParams {
     const char *v_new;
     char *k_pool_w;
     char *v_pool_w;
+    int32_t window;            // > 0: attend to the last `window` tokens only (final mode)
     float scale_log2;          // scale * log2(e)
 };
 
@@ -56,6 +57,11 @@ struct AppendParams {
     int64_t block_stride_bytes;
     int32_t B, Hkv, MB, bs;
     int32_t row_bytes;         // head_dim * element size
+    // multi-token write (prefill): k_new/v_new are [B][T][Hkv][D] and
+    // counts[b] <= T rows of sequence b are written from positions[b] on;
+    // counts == nullptr means one token per sequence ([B][Hkv][D], T = 1)
+    const int32_t *counts;
+    int32_t T;
 };
 
 struct ReduceParams {
@@ -108,6 +114,7 @@ inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t s
 // Launchers (return the launch's cudaError_t).  `split` selects the partial
 // (workspace) mode.
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_append_tokens(const AppendParams &p, cudaStream_t stream);
 
 // SIMT decode: grid = B*H*P CTAs.  Returns cudaErrorInvalidValue if the
 // (dtype, D) pair has no instantiation.
