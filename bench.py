@@ -46,31 +46,48 @@ UNIT = "GB/s"
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 SPLIT_PTOK = {5: 1024}          # workloads timed through the split-KV pair
 PROFILE_DIR = ROOT / "profiles"
-KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu"}
+KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
+                  "append_tokens": "append.cu"}
 
 
 # ---------------------------------------------------------------------------
 # algorithmic byte counts
 # ---------------------------------------------------------------------------
 
-def decode_bytes(w, lens_after) -> int:
+def decode_bytes(w, lens_after, window: int = 0) -> int:
     """Valid K/V rows + needed table entries + seq_lens + Q + O of one decode.
 
     Blocks shared by several table rows are counted once (they need to cross
-    HBM once).
+    HBM once).  With a sliding window only the last `window` rows count.
     """
     s = w.q.element_size()
     lens = [int(x) for x in lens_after]
     tab = w.block_table.cpu()
     row_bytes = w.Hkv * w.D * s            # one token, all kv heads, K or V
-    seen = {}
+    rows = {}                              # (block, slot) rows read, shared ones once
+    tables = 0
     for b, L in enumerate(lens):
-        for j in range(-(-L // w.bs)):
+        lo = max(0, L - window) if window > 0 else 0
+        j0, j1 = lo // w.bs, -(-L // w.bs)
+        tables += j1 - j0
+        for j in range(j0, j1):
             blk = int(tab[b, j])
-            seen[blk] = max(seen.get(blk, 0), min(w.bs, L - j * w.bs))
-    kv = 2 * row_bytes * sum(seen.values())
-    table = 4 * sum(-(-L // w.bs) for L in lens)
-    return kv + table + 4 * w.B + 2 * w.B * w.H * w.D * s
+            a, e = max(lo, j * w.bs) - j * w.bs, min(L, (j + 1) * w.bs) - j * w.bs
+            cur = rows.get(blk)
+            rows[blk] = (a, e) if cur is None else (min(cur[0], a), max(cur[1], e))
+    kv = 2 * row_bytes * sum(e - a for a, e in rows.values())
+    return kv + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
+
+
+def prefill_bytes(w) -> int:
+    """Prompt write of every sequence's L tokens: read the padded batch's
+    valid rows, write them into the pool, plus positions, counts and the
+    table entries the write needs."""
+    s = w.q.element_size()
+    lens = [int(x) for x in w.lens]
+    rows = sum(lens)
+    tables = sum(-(-L // w.bs) for L in lens)
+    return 2 * 2 * rows * w.Hkv * w.D * s + 8 * w.B + 4 * tables
 
 
 def logical_kv_bytes(w, lens_after) -> int:
@@ -221,6 +238,8 @@ def run_gpu(args) -> None:
                           block_stride=w.block_stride, dtype=w.dtype)
     path = pa.paged_attention_decode_path(shape)
     kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
+    if args.prefill:
+        kernel = "append_tokens"
     ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
     positions = w.lens.clone()
     lens_after = (w.lens + 1).clone()
@@ -232,32 +251,72 @@ def run_gpu(args) -> None:
 
     fused = not ptok and not args.unfused
 
+    window = args.window or 0
+    if window:
+        fused = False
+    prefill = None
+    if args.prefill:
+        # the padded batch of whole prompts, lengths = the workload's lengths
+        T = int(w.lens.max())
+        gen = torch.Generator(device=dev).manual_seed(99)
+        prefill = {
+            "k": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
+            "v": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
+            "start": torch.zeros(w.B, dtype=torch.int32, device=dev),
+        }
+        fused = False
+    kflat, vflat = w.k_flat(), w.v_flat()
+
+    def make_calls(prepared: bool):
+        """The step's C-ABI calls.  Prepared calls marshal their arguments
+        once (a serving loop reuses its buffers every step) and are bound to
+        the bench stream; graph capture needs calls on the capture stream."""
+        o = dict(err_word=err, prepare=prepared,
+                 stream=stream.cuda_stream if prepared else None)
+
+        def bind(fn, *a, **k):
+            c = fn(*a, **k, **o)
+            return c if prepared else (lambda: fn(*a, **k, **dict(o, prepare=False)))
+
+        calls = []
+        if prefill is not None:
+            calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
+                              w.block_table, prefill["start"], w.lens, **kw))
+            return calls, []
+        if fused:
+            calls.append(bind(pa.paged_attention_decode_append, out, w.q, w.k_new, w.v_new, kflat,
+                              vflat, w.block_table, positions, w.scale, num_kv_heads=w.Hkv, **kw))
+            return calls, []
+        app = [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table, positions,
+                    **kw)]
+        if window:
+            calls.append(bind(pa.paged_attention_decode_window, out, w.q, kflat, vflat,
+                              w.block_table, lens_after, w.scale, window, num_kv_heads=w.Hkv, **kw))
+        elif ptok:
+            calls.append(bind(pa.paged_attention_decode_partial, w.q, kflat, vflat, w.block_table,
+                              lens_after, w.scale, ptok, ws, num_kv_heads=w.Hkv, **kw))
+            calls.append(bind(pa.paged_attention_decode_reduce, out, ws, lens_after, ptok,
+                              num_kv_heads=w.Hkv, max_blocks_per_seq=w.MB, **kw))
+        else:
+            calls.append(bind(pa.paged_attention_decode, out, w.q, kflat, vflat, w.block_table,
+                              lens_after, w.scale, num_kv_heads=w.Hkv, **kw))
+        return calls, app
+
+    main_calls, app_calls = make_calls(prepared=True)
+
     def append():
-        pa.paged_kv_append(w.k_new, w.v_new, w.k_flat(), w.v_flat(), w.block_table, positions,
-                           err_word=err, **kw)
+        for c in app_calls:
+            c()
 
     def decode():
-        if ptok:
-            pa.paged_attention_decode_partial(w.q, w.k_flat(), w.v_flat(), w.block_table,
-                                              lens_after, w.scale, ptok, ws, num_kv_heads=w.Hkv,
-                                              err_word=err, **kw)
-            pa.paged_attention_decode_reduce(out, ws, lens_after, ptok, num_kv_heads=w.Hkv,
-                                             max_blocks_per_seq=w.MB, err_word=err, **kw)
-        else:
-            pa.paged_attention_decode(out, w.q, w.k_flat(), w.v_flat(), w.block_table,
-                                      lens_after, w.scale, num_kv_heads=w.Hkv, err_word=err,
-                                      **kw)
+        for c in main_calls:
+            c()
 
     def step():
-        if fused:
-            pa.paged_attention_decode_append(out, w.q, w.k_new, w.v_new, w.k_flat(), w.v_flat(),
-                                             w.block_table, positions, w.scale,
-                                             num_kv_heads=w.Hkv, err_word=err, **kw)
-        else:
-            append()
-            decode()
+        append()
+        decode()
 
-    launches_per_step = 1 if fused else 1 + (2 if ptok else 1)
+    launches_per_step = len(main_calls) + len(app_calls)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -265,11 +324,30 @@ def run_gpu(args) -> None:
         raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
 
     K = args.steps
+    graph = None
+    if args.graph:
+        # capture args.graph steps into one CUDA graph; the timed region
+        # replays it K / args.graph times (K is rounded up to a multiple)
+        K = -(-K // args.graph) * args.graph
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g_main, g_app = make_calls(prepared=False)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.graph):
+                for c in g_app + g_main:
+                    c()
+        graph.replay()
+        torch.cuda.synchronize()
     # kernel durations are sampled live on every EVERY-th step of the timed
     # region (events bracket those launches on the launching stream); the
     # other steps run back to back, so that events do not sit between kernels
     EVERY = 16
-    sampled = list(range(0, K, EVERY))
+    sampled = [] if graph is not None else list(range(0, K, EVERY))
     ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -278,27 +356,29 @@ def run_gpu(args) -> None:
     torch.cuda.synchronize()
     with ClockSampler(local_gpu_index(local_rank)) as clk:
         t0.record(stream)
-        for i in range(K):
+        for i in range(K // args.graph if graph is not None else 0):
+            graph.replay()
+        for i in range(0 if graph is not None else K):
             e = ev.get(i)
             if e is None:
                 step()
                 continue
             e[0].record(stream)
-            if fused:
-                e[1].record(stream)
-                step()
-            else:
-                append()
-                e[1].record(stream)
-                decode()
+            append()
+            e[1].record(stream)
+            decode()
             e[2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
-    append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
+    if graph is not None:
+        # no events inside the graph: the step time bounds the kernel time
+        decode_ms = append_ms = total_ms / K
+    else:
+        decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
+        append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
     if dist:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -344,10 +424,13 @@ def run_gpu(args) -> None:
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during timing")
 
-    dbytes = decode_bytes(w, lens_after)
-    step_bytes = dbytes + append_bytes(w)
-    # the fused kernel also writes the appended rows into the pool
-    kbytes = dbytes + (2 * w.B * w.Hkv * w.D * w.q.element_size() if fused else 0)
+    if prefill is not None:
+        dbytes = step_bytes = kbytes = prefill_bytes(w)
+    else:
+        dbytes = decode_bytes(w, lens_after, window)
+        step_bytes = dbytes + append_bytes(w)
+        # the fused kernel also writes the appended rows into the pool
+        kbytes = dbytes + (2 * w.B * w.Hkv * w.D * w.q.element_size() if fused else 0)
     peaks = measured_peaks()
     achieved = kbytes / (decode_ms * 1e-3) / 1e9
     ms_step = total_ms / K
@@ -375,12 +458,14 @@ def run_gpu(args) -> None:
             "decode_us": round(decode_ms * 1e3, 3), "append_us": round(append_ms * 1e3, 3),
             "decode_bytes": dbytes, "kernel_bytes": kbytes,
             "logical_kv_bytes": logical_kv_bytes(w, lens_after),
-            "decode_path": kernel, "fused_append": fused,
+            "decode_path": kernel, "fused_append": fused, "cuda_graph_steps": args.graph or None,
+            "window": window or None, "op": "prefill write" if prefill is not None else "decode step",
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": kernel_traffic(kernel, f"w{args.workload}", fused),
-                         "kernel": kernel, "timed_launches": len(sampled)},
+                         "kernel": kernel, "timed_launches": len(sampled),
+                         "kernel_timing": "graph step" if graph is not None else "events"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": Ke,
                     "ms_per_step": round(e2e_ms / Ke, 6)},
@@ -477,6 +562,12 @@ def main() -> None:
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (workloads 2-4)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window decode over the last W tokens (append + window decode)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the prompt write of every sequence's full length instead")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="capture this many steps into one CUDA graph and replay it")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_append and paged_attention_decode as two launches")
     ap.add_argument("--split-tokens", type=int, default=None,

@@ -135,6 +135,33 @@ def _check(status: int, what: str) -> None:
         raise PagedAttnError(status, what)
 
 
+class Prepared:
+    """A C-ABI call with its arguments marshalled once.
+
+    Calling it re-issues the same call (same buffers, shape, scale and
+    stream), costing a few microseconds of host time instead of the full
+    marshalling; the tensors it was built from must stay alive and keep their
+    storage.  Every wrapper below returns one when given prepare=True.
+    """
+
+    __slots__ = ("_fn", "_args", "_what", "_keep")
+
+    def __init__(self, fn, args, what, keep):
+        self._fn, self._args, self._what, self._keep = fn, args, what, keep
+
+    def __call__(self) -> None:
+        status = self._fn(*self._args)
+        if status != PA_OK:
+            raise PagedAttnError(status, self._what)
+
+
+def _issue(fn, args, what, prepare, keep=()):
+    if prepare:
+        return Prepared(fn, args, what, keep)
+    _check(fn(*args), what)
+    return None
+
+
 def decode_shape(q, block_table, *, num_kv_heads, block_size, num_blocks, block_stride) -> Shape:
     B, H, D = q.shape
     return make_shape(batch=B, num_heads=H, num_kv_heads=num_kv_heads, head_dim=D,
@@ -143,68 +170,74 @@ def decode_shape(q, block_table, *, num_kv_heads, block_size, num_blocks, block_
 
 
 def paged_kv_append(k_new, v_new, k_pool, v_pool, block_table, positions, *, block_size,
-                    num_blocks, block_stride, err_word=None, stream=None) -> None:
+                    num_blocks, block_stride, err_word=None, stream=None, prepare=False):
     """Write k_new/v_new [B][Hkv][D] at positions[b] through block_table."""
     B, Hkv, D = k_new.shape
     shape = make_shape(batch=B, num_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=block_size,
                        max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
                        block_stride=block_stride, dtype=k_new.dtype)
-    _check(load().paged_kv_append(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
-                                  _ptr(v_pool), _ptr(block_table), _ptr(positions),
-                                  _ptr(err_word), _stream(stream)), "paged_kv_append")
+    args = (
+            ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+            _ptr(block_table), _ptr(positions), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_kv_append, args, "paged_kv_append", prepare,
+                  (shape,))
 
 
 def paged_attention_decode(out, q, k_pool, v_pool, block_table, seq_lens, scale, *, num_kv_heads,
                            block_size, num_blocks, block_stride, err_word=None,
-                           stream=None) -> None:
+                           stream=None, prepare=False):
     """out[B][H][D] = attention of q over the valid tokens of each sequence."""
     shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
                          num_blocks=num_blocks, block_stride=block_stride)
-    _check(load().paged_attention_decode(ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool),
-                                         _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
-                                         float(scale), _ptr(err_word), _stream(stream)),
-           "paged_attention_decode")
+    args = (
+            ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+            _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_attention_decode, args, "paged_attention_decode", prepare,
+                  (shape,))
 
 
 def paged_attention_decode_append(out, q, k_new, v_new, k_pool, v_pool, block_table, positions,
                                   scale, *, num_kv_heads, block_size, num_blocks, block_stride,
-                                  err_word=None, stream=None) -> None:
+                                  err_word=None, stream=None, prepare=False):
     """Append k_new/v_new at positions[b], then attend over positions[b] + 1 tokens."""
     shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
                          num_blocks=num_blocks, block_stride=block_stride)
-    _check(load().paged_attention_decode_append(ctypes.byref(shape), _ptr(out), _ptr(q),
-                                                _ptr(k_new), _ptr(v_new), _ptr(k_pool),
-                                                _ptr(v_pool), _ptr(block_table), _ptr(positions),
-                                                float(scale), _ptr(err_word), _stream(stream)),
-           "paged_attention_decode_append")
+    args = (
+            ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+            _ptr(v_pool), _ptr(block_table), _ptr(positions), float(scale), _ptr(err_word),
+            _stream(stream))
+    return _issue(load().paged_attention_decode_append, args, "paged_attention_decode_append", prepare,
+                  (shape,))
 
 
 def paged_kv_append_tokens(k_new, v_new, k_pool, v_pool, block_table, positions, counts, *,
                            block_size, num_blocks, block_stride, err_word=None,
-                           stream=None) -> None:
+                           stream=None, prepare=False):
     """Prefill write: counts[b] rows of the padded batch k_new/v_new [B][T][Hkv][D]
     go to positions[b] + t."""
     B, T, Hkv, D = k_new.shape
     shape = make_shape(batch=B, num_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=block_size,
                        max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
                        block_stride=block_stride, dtype=k_new.dtype)
-    _check(load().paged_kv_append_tokens(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), int(T),
-                                         _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-                                         _ptr(positions), _ptr(counts), _ptr(err_word),
-                                         _stream(stream)), "paged_kv_append_tokens")
+    args = (
+            ctypes.byref(shape), _ptr(k_new), _ptr(v_new), int(T), _ptr(k_pool), _ptr(v_pool),
+            _ptr(block_table), _ptr(positions), _ptr(counts), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_kv_append_tokens, args, "paged_kv_append_tokens", prepare,
+                  (shape,))
 
 
 def paged_attention_decode_window(out, q, k_pool, v_pool, block_table, seq_lens, scale, window,
                                   *, num_kv_heads, block_size, num_blocks, block_stride,
-                                  err_word=None, stream=None) -> None:
+                                  err_word=None, stream=None, prepare=False):
     """Decode attention over the last `window` valid tokens of each sequence."""
     shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
                          num_blocks=num_blocks, block_stride=block_stride)
-    _check(load().paged_attention_decode_window(ctypes.byref(shape), _ptr(out), _ptr(q),
-                                                _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-                                                _ptr(seq_lens), float(scale), int(window),
-                                                _ptr(err_word), _stream(stream)),
-           "paged_attention_decode_window")
+    args = (
+            ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+            _ptr(block_table), _ptr(seq_lens), float(scale), int(window), _ptr(err_word),
+            _stream(stream))
+    return _issue(load().paged_attention_decode_window, args, "paged_attention_decode_window", prepare,
+                  (shape,))
 
 
 def paged_attention_decode_path(shape: Shape) -> int:
@@ -217,30 +250,31 @@ def paged_attention_partial_workspace(shape: Shape, partition_tokens: int) -> in
 
 def paged_attention_decode_partial(q, k_pool, v_pool, block_table, seq_lens, scale,
                                    partition_tokens, workspace, *, num_kv_heads, block_size,
-                                   num_blocks, block_stride, err_word=None, stream=None) -> None:
+                                   num_blocks, block_stride, err_word=None, stream=None, prepare=False):
     shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
                          num_blocks=num_blocks, block_stride=block_stride)
     nbytes = workspace.numel() * workspace.element_size()
-    _check(load().paged_attention_decode_partial(ctypes.byref(shape), _ptr(q), _ptr(k_pool),
-                                                 _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
-                                                 float(scale), int(partition_tokens),
-                                                 _ptr(workspace), nbytes, _ptr(err_word),
-                                                 _stream(stream)),
-           "paged_attention_decode_partial")
+    args = (
+            ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+            _ptr(seq_lens), float(scale), int(partition_tokens), _ptr(workspace), nbytes,
+            _ptr(err_word), _stream(stream))
+    return _issue(load().paged_attention_decode_partial, args, "paged_attention_decode_partial", prepare,
+                  (shape,))
 
 
 def paged_attention_decode_reduce(out, workspace, seq_lens, partition_tokens, *, num_kv_heads,
                                   block_size, num_blocks, block_stride, max_blocks_per_seq,
-                                  err_word=None, stream=None) -> None:
+                                  err_word=None, stream=None, prepare=False):
     B, H, D = out.shape
     shape = make_shape(batch=B, num_heads=H, num_kv_heads=num_kv_heads, head_dim=D,
                        block_size=block_size, max_blocks_per_seq=max_blocks_per_seq,
                        num_blocks=num_blocks, block_stride=block_stride, dtype=out.dtype)
     nbytes = workspace.numel() * workspace.element_size()
-    _check(load().paged_attention_decode_reduce(ctypes.byref(shape), _ptr(out), _ptr(workspace),
-                                                nbytes, _ptr(seq_lens), int(partition_tokens),
-                                                _ptr(err_word), _stream(stream)),
-           "paged_attention_decode_reduce")
+    args = (
+            ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, _ptr(seq_lens),
+            int(partition_tokens), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_attention_decode_reduce, args, "paged_attention_decode_reduce", prepare,
+                  (shape,))
 
 
 def workspace_for(q, block_table, partition_tokens, *, num_kv_heads, block_size, num_blocks,

@@ -164,6 +164,42 @@ int choose_cluster(int64_t units, int64_t max_tiles) {
 #endif
 }
 
+// Encoded tensor maps, keyed by everything the encoding depends on; a
+// repeated call on the same pool (every decode step) skips the driver call.
+struct MapKey {
+    const void *pool;
+    int64_t rows;
+    int32_t head_dim, box_rows, dtype, device;
+    bool operator==(const MapKey &o) const {
+        return pool == o.pool && rows == o.rows && head_dim == o.head_dim &&
+               box_rows == o.box_rows && dtype == o.dtype && device == o.device;
+    }
+};
+
+bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
+    constexpr int kSlots = 16;
+    static std::mutex mu;
+    static MapKey keys[kSlots];
+    static CUtensorMap maps[kSlots];
+    static int used = 0, next = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const int64_t rows = (s->num_blocks - 1) * (s->block_stride / s->head_dim) +
+                         (int64_t)s->num_kv_heads * s->block_size;
+    const MapKey key{pool, rows, s->head_dim, box_rows_for(s), s->dtype, dev};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == key) {
+            *map = maps[i];
+            return true;
+        }
+    if (!encode_pool_map(map, s, pool)) return false;
+    const int slot = used < kSlots ? used++ : (next++ % kSlots);
+    keys[slot] = key;
+    maps[slot] = *map;
+    return true;
+}
+
 // Launch the decode kernel family chosen for `s` (final or split mode).
 pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cudaStream_t stream) {
     cudaError_t e;
@@ -181,7 +217,7 @@ pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cuda
     }
     if (tc_eligible(s)) {
         CUtensorMap kmap, vmap;
-        if (!encode_pool_map(&kmap, s, p.k_pool) || !encode_pool_map(&vmap, s, p.v_pool))
+        if (!cached_pool_map(&kmap, s, p.k_pool) || !cached_pool_map(&vmap, s, p.v_pool))
             return PA_ERR_CUDA;
         e = pa::launch_decode_gqa_tc(s->dtype, p, kmap, vmap, box_rows_for(s), split, stream);
     } else {

@@ -84,6 +84,25 @@ struct ReduceParams {
 #ifndef PA_PDL
 #define PA_PDL 1
 #endif
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, size) -- the attribute call costs
+// microseconds of host time, more than a small launch itself.  `configured`
+// is the caller's per-kernel record (largest limit set so far, per device):
+// kernels of one signature share a function-pointer type, so the record
+// cannot live in this template.
+template <typename Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, int (&configured)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && configured[dev] >= (int)bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64 && configured[dev] < (int)bytes)
+        configured[dev] = (int)bytes;
+    return e;
+}
+
 template <typename Kern, typename... Args>
 inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
                                     cudaStream_t stream, Args... args) {
