@@ -47,6 +47,8 @@ DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"
 SPLIT_PTOK = {5: 1024}          # workloads timed through the split-KV pair
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
+                  "decode_simt_balanced": "decode_balanced_simt.cu",
+                  "decode_tc_balanced": "decode_balanced_tc.cu",
                   "append_tokens": "append.cu"}
 
 
@@ -252,8 +254,15 @@ def run_gpu(args) -> None:
     fused = not ptok and not args.unfused
 
     window = args.window or 0
-    if window:
+    balanced = args.balanced
+    if window and not balanced:
         fused = False
+    bws = None
+    if balanced:
+        ptok = None
+        fused = not args.unfused
+        kernel = kernel.replace("decode_gqa_tc", "decode_tc") + "_balanced"
+        bws = pa.balanced_workspace_for(w.q, w.block_table, num_kv_heads=w.Hkv, **kw)
     prefill = None
     if args.prefill:
         # the padded batch of whole prompts, lengths = the workload's lengths
@@ -283,6 +292,17 @@ def run_gpu(args) -> None:
             calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
                               w.block_table, prefill["start"], w.lens, **kw))
             return calls, []
+        if balanced:
+            if fused:
+                calls.append(bind(pa.paged_attention_decode_balanced, out, w.q, kflat, vflat,
+                                  w.block_table, w.scale, bws, positions=positions, k_new=w.k_new,
+                                  v_new=w.v_new, window=window, num_kv_heads=w.Hkv, **kw))
+                return calls, []
+            calls.append(bind(pa.paged_attention_decode_balanced, out, w.q, kflat, vflat,
+                              w.block_table, w.scale, bws, seq_lens=lens_after, window=window,
+                              num_kv_heads=w.Hkv, **kw))
+            return calls, [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table,
+                                positions, **kw)]
         if fused:
             calls.append(bind(pa.paged_attention_decode_append, out, w.q, w.k_new, w.v_new, kflat,
                               vflat, w.block_table, positions, w.scale, num_kv_heads=w.Hkv, **kw))
@@ -459,7 +479,8 @@ def run_gpu(args) -> None:
             "decode_bytes": dbytes, "kernel_bytes": kbytes,
             "logical_kv_bytes": logical_kv_bytes(w, lens_after),
             "decode_path": kernel, "fused_append": fused, "cuda_graph_steps": args.graph or None,
-            "window": window or None, "op": "prefill write" if prefill is not None else "decode step",
+            "window": window or None, "schedule": "balanced" if balanced else "one CTA per unit",
+            "op": "prefill write" if prefill is not None else "decode step",
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -568,6 +589,8 @@ def main() -> None:
                     help="time the prompt write of every sequence's full length instead")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many steps into one CUDA graph and replay it")
+    ap.add_argument("--balanced", action="store_true",
+                    help="time paged_attention_decode_balanced (persistent load-balanced grid)")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_append and paged_attention_decode as two launches")
     ap.add_argument("--split-tokens", type=int, default=None,

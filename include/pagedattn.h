@@ -12,6 +12,8 @@
  *   paged_attention_decode_partial  the same over fixed token partitions,
  *   paged_attention_decode_reduce   then a log-sum-exp merge (split-KV, for
  *                                   long contexts or few sequences)
+ *   paged_attention_decode_balanced the same step on a persistent grid with
+ *                                   equal work per warp (mixed lengths)
  *
  * Sources (web pages on paged KV caches), cited by title and section:
  *   "KV Cache and BlockManager" (dpshk.com/news/5906718)            [BM]
@@ -289,6 +291,55 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
                                         const void *workspace, size_t workspace_bytes,
                                         const int32_t *seq_lens, int32_t partition_tokens,
                                         int32_t *err_word, pa_stream_t stream);
+
+/*
+ * paged_attention_decode_balanced -- one decode step under a load-balanced,
+ * persistent schedule.
+ *
+ * Computes exactly what the single-pass entry points compute, selected by
+ * the arguments:
+ *   seq_lens != NULL, positions == NULL   paged_attention_decode (window 0)
+ *                                         or paged_attention_decode_window
+ *   positions != NULL, seq_lens == NULL   paged_attention_decode_append
+ *                                         (k_new, v_new required), over the
+ *                                         last `window` tokens when window > 0
+ * with the same device checks, zeros and PA_DEVERR_* bits.  k_pool and
+ * v_pool are written only in the append mode.
+ *
+ * The attention is the per-block decomposition of [PG] s2.2; what differs is
+ * the schedule, which the sources leave to the implementation: the grid is
+ * sized to the GPU (a few CTAs per SM), and the tiles of all
+ * (sequence, head) items, laid end to end, are cut into one equal slice per
+ * warp, so a batch mixing short and long sequences ([BUG] s2 serves such
+ * batches) keeps every SM streaming until the end.  An item cut between
+ * warps is finished by the last of them to arrive, which merges their
+ * partial softmax states (the log-sum-exp merge of the split-KV pair).
+ * Results differ from paged_attention_decode only by fp32 rounding order,
+ * and are reproducible run to run for the same inputs and device.
+ *
+ * Workspace: device memory of at least paged_attention_balanced_workspace()
+ * bytes, 16-byte aligned, owned by the caller.  It must be ZERO-FILLED
+ * before its first use (e.g. cudaMemsetAsync); every call leaves the
+ * counters in it at zero again, so no call after the first needs a fill --
+ * unless a call was aborted before completing (a device error that killed
+ * the context), after which the workspace must be zero-filled again.  Calls
+ * that may overlap on the GPU need separate workspaces.  The size depends on
+ * the shape and on the GPU the call runs on (SM count); query it with the
+ * target device current.  Returns 0 for a shape this entry point rejects.
+ *
+ * Rejected shapes (PA_ERR_UNSUPPORTED): the schedule keeps two int32 per
+ * sequence in shared memory and counts tiles in int32, which bounds batch
+ * and batch*heads*max_blocks_per_seq*block_size/16.
+ */
+size_t paged_attention_balanced_workspace(const pa_shape *shape);
+
+pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, const void *q,
+                                          void *k_pool, void *v_pool,
+                                          const int32_t *block_table, const int32_t *seq_lens,
+                                          const int32_t *positions, const void *k_new,
+                                          const void *v_new, float scale, int32_t window,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *err_word, pa_stream_t stream);
 
 /*
  * paged_attention_decode_split_static -- the split-KV pair without any

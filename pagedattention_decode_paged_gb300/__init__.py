@@ -10,7 +10,9 @@ Names follow the C ABI: paged_kv_append, paged_attention_decode,
 paged_attention_decode_append (both in one launch), paged_kv_append_tokens
 (prefill write), paged_attention_decode_window (sliding window),
 paged_attention_partial_workspace, paged_attention_decode_partial,
-paged_attention_decode_reduce, paged_attention_decode_path.
+paged_attention_decode_reduce, paged_attention_decode_path,
+paged_attention_balanced_workspace, paged_attention_decode_balanced
+(persistent load-balanced schedule).
 """
 from __future__ import annotations
 
@@ -32,7 +34,8 @@ EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attentio
             "paged_attention_decode_append", "paged_attention_decode_split_static",
             "paged_kv_append_tokens", "paged_attention_decode_window",
             "paged_attention_decode_path", "paged_attention_partial_workspace",
-            "paged_attention_decode_partial", "paged_attention_decode_reduce")
+            "paged_attention_decode_partial", "paged_attention_decode_reduce",
+            "paged_attention_balanced_workspace", "paged_attention_decode_balanced")
 
 
 class PagedAttnError(RuntimeError):
@@ -90,6 +93,11 @@ def load() -> ctypes.CDLL:
                                                            vp, vp]
             lib.paged_attention_decode_reduce.restype = ctypes.c_int
             lib.paged_attention_decode_reduce.argtypes = [sp, vp, vp, sz, vp, i32, vp, vp]
+            lib.paged_attention_balanced_workspace.restype = sz
+            lib.paged_attention_balanced_workspace.argtypes = [sp]
+            lib.paged_attention_decode_balanced.restype = ctypes.c_int
+            lib.paged_attention_decode_balanced.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                            f32, i32, vp, sz, vp, vp]
             _lib = lib
     return _lib
 
@@ -286,3 +294,38 @@ def workspace_for(q, block_table, partition_tokens, *, num_kv_heads, block_size,
     if n == 0:
         raise PagedAttnError(PA_ERR_INVALID_ARG, "paged_attention_partial_workspace")
     return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
+
+
+def paged_attention_balanced_workspace(shape: Shape) -> int:
+    return int(load().paged_attention_balanced_workspace(ctypes.byref(shape)))
+
+
+def balanced_workspace_for(q, block_table, *, num_kv_heads, block_size, num_blocks,
+                           block_stride) -> torch.Tensor:
+    """Allocate (through torch) a zero-filled workspace for
+    paged_attention_decode_balanced on q's device."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    with torch.cuda.device(q.device):
+        n = paged_attention_balanced_workspace(shape)
+    if n == 0:
+        raise PagedAttnError(PA_ERR_UNSUPPORTED, "paged_attention_balanced_workspace")
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
+
+
+def paged_attention_decode_balanced(out, q, k_pool, v_pool, block_table, scale, workspace, *,
+                                    seq_lens=None, positions=None, k_new=None, v_new=None,
+                                    window=0, num_kv_heads, block_size, num_blocks, block_stride,
+                                    err_word=None, stream=None, prepare=False):
+    """One decode step on the load-balanced persistent grid: plain decode
+    (seq_lens) or fused append + decode (positions, k_new, v_new), over the
+    last `window` tokens when window > 0."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    nbytes = workspace.numel() * workspace.element_size()
+    args = (
+            ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+            _ptr(seq_lens), _ptr(positions), _ptr(k_new), _ptr(v_new), float(scale), int(window),
+            _ptr(workspace), nbytes, _ptr(err_word), _stream(stream))
+    return _issue(load().paged_attention_decode_balanced, args, "paged_attention_decode_balanced",
+                  prepare, (shape,))

@@ -21,7 +21,8 @@ INCLUDE = ROOT / "include"
 LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "libpagedattn.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "decode_gqa_tc.cu"]
+SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "decode_gqa_tc.cu", "decode_balanced_simt.cu",
+           "decode_balanced_tc.cu"]
 
 
 def _nvcc() -> str:

@@ -240,6 +240,45 @@ pa_status check_decode_args(const pa_shape *s, const void *q, const void *k_pool
     return PA_OK;
 }
 
+// The load-balanced schedule for `s` on the current device (window > 0
+// bounds the tiles per item).  PA_ERR_UNSUPPORTED when the schedule's
+// shared-memory tables or int32 tile indices cannot hold the shape.
+pa_status balanced_plan(const pa_shape *s, int32_t window, pa::BalancedPlan *plan, bool *tc_out) {
+    const bool tc = tc_eligible(s);
+    const int g = s->num_heads / s->num_kv_heads;
+    const int64_t items_per_seq = tc ? (int64_t)s->num_kv_heads * ((g + 15) / 16) : s->num_heads;
+    const int tile = tc ? 16 : 4096 / (s->head_dim * elem_size(s->dtype));
+    int64_t max_len = (int64_t)s->max_blocks_per_seq * s->block_size;
+    if (window > 0 && window + 15 < max_len) max_len = window + 15;
+    const int64_t max_tiles = (max_len + tile - 1) / tile;
+    const int64_t total = (int64_t)s->batch * items_per_seq * max_tiles;
+    if (total >= (int64_t)INT32_MAX / 2) return PA_ERR_UNSUPPORTED;
+    const cudaError_t e =
+        tc ? pa::plan_balanced_tc(s->dtype, s->head_dim, g, s->batch, total, plan)
+           : pa::plan_balanced_simt(s->dtype, s->head_dim, s->batch, total, plan);
+    if (e == cudaErrorInvalidValue) {
+        (void)cudaGetLastError();   // a too-large shared-memory request is not sticky; drop it
+        return PA_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (plan->grid <= 0) return PA_ERR_UNSUPPORTED;
+    plan->items = (int64_t)s->batch * items_per_seq;
+    *tc_out = tc;
+    return PA_OK;
+}
+
+// Workspace of the balanced schedule: records, then one counter per item.
+struct BalWs {
+    size_t off_counters, total;
+};
+BalWs balanced_ws(const pa::BalancedPlan &plan) {
+    BalWs w;
+    const size_t rec = (size_t)2 * plan.grid * pa::kBalWarps * plan.rec_floats * 4;
+    w.off_counters = (rec + 15) & ~(size_t)15;
+    w.total = w.off_counters + (size_t)plan.items * 4;
+    return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -460,6 +499,69 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
     return pa::launch_reduce(shape->dtype, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
+}
+
+size_t paged_attention_balanced_workspace(const pa_shape *shape) {
+    if (check_shape(shape) != PA_OK || shape->batch == 0 ||
+        !pa::simt_supported(shape->dtype, shape->head_dim))
+        return 0;
+    pa::BalancedPlan plan;
+    bool tc = false;
+    if (balanced_plan(shape, 0, &plan, &tc) != PA_OK) return 0;
+    return balanced_ws(plan).total;
+}
+
+pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, const void *q,
+                                          void *k_pool, void *v_pool,
+                                          const int32_t *block_table, const int32_t *seq_lens,
+                                          const int32_t *positions, const void *k_new,
+                                          const void *v_new, float scale, int32_t window,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *err_word, pa_stream_t stream) {
+    const bool fused = positions != nullptr;
+    if (fused == (seq_lens != nullptr)) return PA_ERR_INVALID_ARG;   // exactly one of the two
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, fused ? positions : seq_lens);
+    if (st != PA_OK) return st;
+    if (window < 0 || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    if (out == nullptr || workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (fused && (k_new == nullptr || v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(workspace)) return PA_ERR_MISALIGNED;
+    if (fused && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_MISALIGNED;
+    pa::BalancedPlan plan;
+    bool tc = false;
+    st = balanced_plan(shape, window, &plan, &tc);
+    if (st != PA_OK) return st;
+    const BalWs w = balanced_ws(plan);
+    if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.out = out;
+    p.partition_tokens = 0;
+    p.num_partitions = 1;
+    p.window = window;
+    if (fused) {
+        p.positions = positions;
+        p.k_new = static_cast<const char *>(k_new);
+        p.v_new = static_cast<const char *>(v_new);
+        p.k_pool_w = static_cast<char *>(k_pool);
+        p.v_pool_w = static_cast<char *>(v_pool);
+    }
+    char *ws = static_cast<char *>(workspace);
+    p.records = reinterpret_cast<float *>(ws);
+    p.counters = reinterpret_cast<int32_t *>(ws + w.off_counters);
+    p.rec_floats = plan.rec_floats;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (tc) {
+        CUtensorMap kmap, vmap;
+        if (!cached_pool_map(&kmap, shape, k_pool) || !cached_pool_map(&vmap, shape, v_pool))
+            return PA_ERR_CUDA;
+        e = pa::launch_balanced_tc(shape->dtype, p, kmap, vmap, box_rows_for(shape), plan, s);
+    } else {
+        e = pa::launch_balanced_simt(shape->dtype, p, plan, s);
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // extern "C"

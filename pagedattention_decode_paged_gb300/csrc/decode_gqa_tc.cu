@@ -29,18 +29,22 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "tc_tile.cuh"
 
 namespace pa {
 
 constexpr int kTcWarps = 4;
-constexpr int kTcTile = 16;        // tokens per tile (one MMA M tile)
 constexpr int kTcTableCap = 1024;  // table entries staged per CTA (rest read from global)
+#ifndef PA_TC_STAGES
+#define PA_TC_STAGES 2                 // tiles in flight per warp at head_dim >= 128
+#endif
+constexpr int kTcMinBlocks = PA_TC_STAGES <= 2 ? 3 : 2;
 
 template <int D>
 struct TcCfg {
     static constexpr int HALVES = D / 64;                // 128-byte column slabs
     static constexpr int TILE_BYTES = kTcTile * D * 2;   // K (or V) bytes per tile
-    static constexpr int STAGES = D == 64 ? 4 : 2;       // tiles in flight per warp
+    static constexpr int STAGES = D == 64 ? 4 : PA_TC_STAGES;  // tiles in flight per warp
     static constexpr int KSTEPS = D / 16;                // MMA K steps of K.Q^T
     static constexpr int MT = D / 16;                    // MMA M tiles of V^T.P^T
     static constexpr size_t kStageBytes = (size_t)kTcWarps * STAGES * 2 * TILE_BYTES;
@@ -52,17 +56,9 @@ struct TcCfg {
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 4; }
 };
 
-// byte offset of 16-byte chunk `chunk` (0..D/8) of row `row` (0..15) inside
-// a swizzled [HALVES][16][128 B] tile
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    const int half = chunk >> 3;
-    const int cj = chunk & 7;
-    return (uint32_t)(half * (kTcTile * 128) + row * 128 + ((cj ^ (row & 7)) << 4));
-}
-
 // NT = head tiles of 8 (1 for groups up to 8 heads, 2 up to 16)
 template <typename T, int D, int NT, bool SPLIT>
-__global__ void __launch_bounds__(kTcWarps * 32, 3)
+__global__ void __launch_bounds__(kTcWarps * 32, kTcMinBlocks)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, DecodeParams p, int box_rows) {
     grid_dependency_wait();
@@ -260,11 +256,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
             l_run[nt][j] = 0.f;
         }
 
-    // ldmatrix lane roles (x4: lanes 8i..8i+7 address the rows of matrix i)
-    const int mi = lane >> 3, ri = lane & 7;
-    const int a_tok = (mi & 1) * 8 + ri, a_chunk = mi >> 1;  // K: {t0-7,t8-15} x {d lo, d hi}
-    const int v_tok = (mi >> 1) * 8 + ri, v_chunk = mi & 1;  // V^T: {d lo, d hi} x {t0-7,t8-15}
-    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
     int k = 0;
     bool aborted = false;
@@ -282,22 +273,14 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
         const int lo = max(0, t_win - t0);   // rows before the window (first tile only)
         if (lo > 0) {
             // attended weight is 0 there; keep V finite under 0 * V
-            const int nchunks = lo * C::HALVES * 8;
-            for (int i = lane; i < nchunks; i += 32)
-                *reinterpret_cast<uint4 *>(vs + swz(i / (C::HALVES * 8), i % (C::HALVES * 8))) =
-                    make_uint4(0, 0, 0, 0);
+            tc_zero_v_rows<D>(vs, 0, lo, lane);
             __syncwarp();
         }
         if (nvalid < kTcTile) {
             // rows past the valid length hold padding (possibly never written
             // or poisoned): P is zero there, and V must be finite so that
             // 0 * V stays 0 inside the MMA
-            const int nchunks = (kTcTile - nvalid) * C::HALVES * 8;
-            for (int i = lane; i < nchunks; i += 32) {
-                const int row = nvalid + i / (C::HALVES * 8);
-                const int ch = i % (C::HALVES * 8);
-                *reinterpret_cast<uint4 *>(vs + swz(row, ch)) = make_uint4(0, 0, 0, 0);
-            }
+            tc_zero_v_rows<D>(vs, nvalid, kTcTile, lane);
             __syncwarp();
         }
         if (fused && t0 + nvalid == t_end) {
@@ -308,89 +291,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 3)
             }
             __syncwarp();
         }
-        const uint32_t ks_u = smem_u32(ks), vs_u = smem_u32(vs);
-
-        // S^T = K Q^T: rows = tokens 0-15 of the tile, columns = heads
-        float s[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            uint32_t a[4];
-            ldsm_x4(ks_u + swz(a_tok, 2 * kk + a_chunk), a[0], a[1], a[2], a[3]);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(s[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
-        }
-
-        // online softmax down each head column (log2 domain); this lane holds
-        // tokens gid (regs 0/1) and gid+8 (regs 2/3)
-        const bool v0 = gid >= lo && gid < nvalid, v1 = gid + 8 >= lo && gid + 8 < nvalid;
-        uint32_t bhi[NT][2], blo[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float pv[4];
-            float corr[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float x0 = v0 ? s[nt][j] * p.scale_log2 : -INFINITY;
-                const float x1 = v1 ? s[nt][j + 2] * p.scale_log2 : -INFINITY;
-                float mx = fmaxf(x0, x1);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m_run[nt][j], mx);
-                corr[j] = ex2_approx(m_run[nt][j] - mn);
-                m_run[nt][j] = mn;
-                pv[j] = ex2_approx(x0 - mn);
-                pv[j + 2] = ex2_approx(x1 - mn);
-            }
-            // 16-bit P^T fragments (row = token, columns = 2 heads), then the
-            // in-register transpose into the B operand (row = head)
-            const uint32_t h0w = Elem<T>::pack2(pv[0], pv[1]);
-            const uint32_t h1w = Elem<T>::pack2(pv[2], pv[3]);
-            bhi[nt][0] = movmatrix_trans(h0w);
-            bhi[nt][1] = movmatrix_trans(h1w);
-            float r0, r1, r2, r3;
-            Elem<T>::unpack2(h0w, r0, r1);
-            Elem<T>::unpack2(h1w, r2, r3);
-            if constexpr (kSplitP) {
-                // bf16 keeps 8 mantissa bits: carry the rounding error as a
-                // second bf16 term so P is good to about 16 bits
-                blo[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0] - r0, pv[1] - r1));
-                blo[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2] - r2, pv[3] - r3));
-                l_run[nt][0] = fmaf(l_run[nt][0], corr[0], pv[0] + pv[2]);
-                l_run[nt][1] = fmaf(l_run[nt][1], corr[1], pv[1] + pv[3]);
-            } else {
-                blo[nt][0] = blo[nt][1] = 0u;
-                // normalise with exactly the weights the MMA uses
-                l_run[nt][0] = fmaf(l_run[nt][0], corr[0], r0 + r2);
-                l_run[nt][1] = fmaf(l_run[nt][1], corr[1], r1 + r3);
-            }
-            const float2 c2 = make_float2(corr[0], corr[1]);
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                float2 lo = __fmul2_rn(make_float2(o_acc[mt][nt][0], o_acc[mt][nt][1]), c2);
-                float2 hi = __fmul2_rn(make_float2(o_acc[mt][nt][2], o_acc[mt][nt][3]), c2);
-                o_acc[mt][nt][0] = lo.x;
-                o_acc[mt][nt][1] = lo.y;
-                o_acc[mt][nt][2] = hi.x;
-                o_acc[mt][nt][3] = hi.y;
-            }
-        }
-
-        // O^T += V^T P^T, one 16-row slab of head_dim per ldmatrix
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(vs_u + swz(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                MmaOp<T>::run(o_acc[mt][nt], a, bhi[nt][0], bhi[nt][1]);
-                if constexpr (kSplitP) MmaOp<T>::run(o_acc[mt][nt], a, blo[nt][0], blo[nt][1]);
-            }
-        }
+        tc_tile_step<T, D, NT>(smem_u32(ks), smem_u32(vs), lo, nvalid, qb, p.scale_log2, o_acc, m_run,
+                               l_run, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && k + C::STAGES < my_tiles) issue(k + C::STAGES);

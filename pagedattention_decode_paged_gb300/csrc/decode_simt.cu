@@ -28,6 +28,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "simt_tile.cuh"
 
 namespace pa {
 
@@ -39,59 +40,7 @@ namespace pa {
 constexpr int kSimtWarps = 4;
 constexpr int kSimtStages = PA_SIMT_STAGES;
 constexpr int kSimtMinBlocks = kSimtStages <= 2 ? 3 : 2;
-constexpr int kTileBytes = 4096;    // K bytes per tile (V the same)
 constexpr int kSimtTableCap = 1024; // table entries staged per CTA (rest read from global)
-
-template <typename T, int D>
-struct SimtCfg {
-    static constexpr int S = sizeof(T);
-    static constexpr int ROWB = D * S;             // bytes per token row
-    static constexpr int VEC = 16 / S;             // elements per 16-byte load
-    static constexpr int LPT = ROWB / 16;          // lanes per token row
-    static constexpr int RPW = 32 / LPT;           // rows per warp instruction
-    static constexpr int TILE = kTileBytes / ROWB; // tokens per tile
-    static constexpr int NVALS = TILE / RPW;       // rows per lane per tile
-    static constexpr int NFIN = NVALS >= LPT ? NVALS / LPT : 1;  // scores per lane after reduce
-    static constexpr int LOG_LPT = LPT == 4 ? 2 : LPT == 8 ? 3 : LPT == 16 ? 4 : 5;
-    static constexpr int LOG_NVALS = 3;
-    static_assert(LPT == 4 || LPT == 8 || LPT == 16 || LPT == 32, "row must be 64..512 bytes");
-    static_assert(NVALS == 8, "tile holds 8 rows per lane");
-};
-
-// Transposing butterfly: v[0..N) per lane are partial sums of N different
-// rows; after the call each lane holds complete sums of fewer rows (see
-// row_of_value below for which ones).
-template <int N, int O>
-struct Butterfly {
-    static __device__ __forceinline__ void run(float *v, int lane) {
-        if constexpr (O == 0) {
-            return;
-        } else if constexpr (N > 1) {
-            constexpr int HALF = N / 2;
-            const bool upper = (lane & O) != 0;
-#pragma unroll
-            for (int k = 0; k < HALF; ++k) {
-                const float send = upper ? v[k] : v[k + HALF];
-                const float keep = upper ? v[k + HALF] : v[k];
-                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-            }
-            Butterfly<HALF, O / 2>::run(v, lane);
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-            Butterfly<1, O / 2>::run(v, lane);
-        }
-    }
-};
-
-// Index (0..NVALS) of the k-th value a lane holds after the butterfly.
-template <typename C>
-__device__ __forceinline__ int row_of_value(int c, int k) {
-    if constexpr (C::NVALS >= C::LPT) {
-        return c * C::NFIN + k;
-    } else {
-        return c >> (C::LOG_LPT - C::LOG_NVALS);
-    }
-}
 
 template <typename T, int D>
 struct SimtSmem {
@@ -326,77 +275,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
             __syncwarp();
         }
 
-        // scores: partial dot products of 8 rows, then the butterfly
-        float v[C::NVALS];
-#pragma unroll
-        for (int j = 0; j < C::NVALS; ++j) {
-            const uint4 kv = *reinterpret_cast<const uint4 *>(ks + (j * C::RPW + r) * C::ROWB + c * 16);
-            float2 k2[C::VEC / 2];
-            Elem<T>::unpack2x(kv, k2);
-            float2 a = __fmul2_rn(q2[0], k2[0]);
-#pragma unroll
-            for (int e = 1; e < C::VEC / 2; ++e) a = __ffma2_rn(q2[e], k2[e], a);
-            v[j] = a.x + a.y;
-        }
-        Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
-
-        float sc[C::NFIN];
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int kk = 0; kk < C::NFIN; ++kk) {
-            const int row = row_of_value<C>(c, kk) * C::RPW + r;
-            sc[kk] = row < nrows ? v[kk] * p.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, sc[kk]);
-        }
-        tmax = warp_max_f32(tmax);
-        const float m_new = fmaxf(m_run, tmax);
-        const float corr = ex2_approx(m_run - m_new);
-#pragma unroll
-        for (int kk = 0; kk < C::NFIN; ++kk)
-            pw[r * C::NVALS + row_of_value<C>(c, kk)] = ex2_approx(sc[kk] - m_new);
-        __syncwarp();
-        float pj[C::NVALS];
-#pragma unroll
-        for (int j = 0; j < C::NVALS; j += 4) {
-            const float4 f = *reinterpret_cast<const float4 *>(pw + r * C::NVALS + j);
-            pj[j] = f.x;
-            pj[j + 1] = f.y;
-            pj[j + 2] = f.z;
-            pj[j + 3] = f.w;
-        }
-        const float2 corr2 = make_float2(corr, corr);
-#pragma unroll
-        for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __fmul2_rn(acc2[e], corr2);
-        float psum = 0.f;
-        if (nrows == C::TILE) {
-#pragma unroll
-            for (int j = 0; j < C::NVALS; ++j) {
-                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
-                float2 v2[C::VEC / 2];
-                Elem<T>::unpack2x(vv, v2);
-                const float2 p2 = make_float2(pj[j], pj[j]);
-#pragma unroll
-                for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
-                psum += pj[j];
-            }
-        } else {
-            // rows past the valid length were never fetched: skip them
-            // (their weight is 0, but the buffer holds stale data)
-#pragma unroll
-            for (int j = 0; j < C::NVALS; ++j) {
-                if (j * C::RPW + r < nrows) {
-                    const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
-                    float2 v2[C::VEC / 2];
-                    Elem<T>::unpack2x(vv, v2);
-                    const float2 p2 = make_float2(pj[j], pj[j]);
-#pragma unroll
-                    for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
-                    psum += pj[j];
-                }
-            }
-        }
-        l_run = fmaf(l_run, corr, psum);
-        m_run = m_new;
+        simt_tile_step<T, D>(ks, vs, nrows, q2, p.scale_log2, m_run, l_run, acc2, pw, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && k + kSimtStages < my_tiles) issue(k + kSimtStages);
@@ -412,15 +291,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     }
 
     // combine the row groups of the warp, then the warps of the CTA
-#pragma unroll
-    for (int o = C::LPT; o < 32; o <<= 1) {
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
-#pragma unroll
-        for (int e = 0; e < C::VEC / 2; ++e) {
-            acc2[e].x += __shfl_xor_sync(0xffffffffu, acc2[e].x, o);
-            acc2[e].y += __shfl_xor_sync(0xffffffffu, acc2[e].y, o);
-        }
-    }
+    simt_rowgroup_reduce<T, D>(l_run, acc2);
     if (lane < C::LPT) {
 #pragma unroll
         for (int e = 0; e < C::VEC / 2; ++e) {

@@ -43,6 +43,12 @@ struct DecodeParams {
     char *v_pool_w;
     int32_t window;            // > 0: attend to the last `window` tokens only (final mode)
     float scale_log2;          // scale * log2(e)
+    // Load-balanced schedule: a warp's partial state for an item it shares
+    // with other warps goes to records[(warp * 2 + slot) * rec_floats ...];
+    // counters[item] counts the warps that have published theirs.
+    float *records;
+    int32_t *counters;
+    int32_t rec_floats;
 };
 
 struct AppendParams {
@@ -103,6 +109,42 @@ inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, int (&configured)[
     return e;
 }
 
+// Number of SMs of the current device (cached per device).
+inline cudaError_t device_sm_count(int *count) {
+    static int counts[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (counts[dev] == 0) {
+        e = cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *count = counts[dev];
+    return cudaSuccess;
+}
+
+// CTAs of `kern` (block threads, `smem` bytes of dynamic shared memory) that
+// one SM holds at once, cached per device for the last smem size asked.
+// `cache` is the caller's per-kernel record: {smem, result} per device.
+template <typename Kern>
+inline cudaError_t resident_ctas(Kern kern, int block, size_t smem, int64_t (&cache)[64][2],
+                                 int *count) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (cache[dev][0] != (int64_t)smem + 1) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block, smem);
+        if (e != cudaSuccess) return e;
+        cache[dev][0] = (int64_t)smem + 1;
+        cache[dev][1] = n;
+    }
+    *count = (int)cache[dev][1];
+    return cudaSuccess;
+}
+
 template <typename Kern, typename... Args>
 inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
                                     cudaStream_t stream, Args... args) {
@@ -148,5 +190,26 @@ cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtenso
 bool gqa_tc_supported(int dtype, int head_dim);
 
 cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream);
+
+// Load-balanced persistent decode (final mode; plain, fused append or sliding
+// window as DecodeParams says).  A plan fixes the grid for a shape on the
+// current device; the workspace holds 2 * grid * kBalWarps records of
+// rec_floats floats followed by one int32 counter per item.
+constexpr int kBalWarps = 4;
+struct BalancedPlan {
+    int grid = 0;              // CTAs (0: the shape cannot run on this schedule)
+    size_t smem = 0;           // dynamic shared memory per CTA
+    int rec_floats = 0;        // floats per record (multiple of 4)
+    int64_t items = 0;         // items (one counter each)
+};
+cudaError_t plan_balanced_simt(int dtype, int head_dim, int batch, int64_t max_tiles_total,
+                               BalancedPlan *plan);
+cudaError_t plan_balanced_tc(int dtype, int head_dim, int group, int batch,
+                             int64_t max_tiles_total, BalancedPlan *plan);
+cudaError_t launch_balanced_simt(int dtype, const DecodeParams &p, const BalancedPlan &plan,
+                                 cudaStream_t stream);
+cudaError_t launch_balanced_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, int box_rows, const BalancedPlan &plan,
+                               cudaStream_t stream);
 
 }  // namespace pa

@@ -120,3 +120,31 @@ def run_fused_step_and_check(w):
     ref, e = oracle_decode(w, ref_pool, w.lens + 1)
     assert not e.any()
     return out, assert_close(out, ref, w.dtype, w.name)
+
+
+def balanced_ws(g):
+    return pa.balanced_workspace_for(g.q, g.block_table, num_kv_heads=g.Hkv, **kw(g))
+
+
+def balanced_counters(g, ws):
+    """The per-item counters at the end of a balanced workspace (int32)."""
+    n = pa.paged_attention_balanced_workspace(shape_of(g))
+    if pa.paged_attention_decode_path(shape_of(g)) == pa.PA_PATH_TENSOR_GQA:
+        items = g.B * g.Hkv * ((g.H // g.Hkv + 15) // 16)
+    else:
+        items = g.B * g.H
+    return ws[n - 4 * items:n].view(torch.int32)
+
+
+def gpu_balanced(g, err, *, lens=None, positions=None, window=0, ws=None, out=None):
+    """One step through paged_attention_decode_balanced: plain decode over
+    `lens`, or the fused append at `positions` then decode."""
+    ws = balanced_ws(g) if ws is None else ws
+    out = torch.empty_like(g.q) if out is None else out
+    fused = positions is not None
+    pa.paged_attention_decode_balanced(out, g.q, g.k_flat(), g.v_flat(), g.block_table, g.scale, ws,
+                                       seq_lens=None if fused else lens, positions=positions,
+                                       k_new=g.k_new if fused else None,
+                                       v_new=g.v_new if fused else None, window=window,
+                                       num_kv_heads=g.Hkv, err_word=err, **kw(g))
+    return out, ws

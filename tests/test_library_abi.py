@@ -157,6 +157,31 @@ def test_split_rejects_bad_arguments(lib):
     assert red(ctypes.byref(s), None, FAKE, need, FAKE, 32, None, None) == pa.PA_ERR_INVALID_ARG
 
 
+def test_balanced_rejects_bad_arguments(lib):
+    f = lib.paged_attention_decode_balanced
+    s = base_shape()
+    # (out, q, k_pool, v_pool, block_table, seq_lens, positions, k_new, v_new)
+    plain = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None)
+    fused = (FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE)
+    tail = (0.1, 0, FAKE, 1 << 30, None, None)
+    assert f(None, *plain, *tail) == pa.PA_ERR_INVALID_ARG
+    both = plain[:6] + (FAKE,) + plain[7:]
+    neither = plain[:5] + (None,) + plain[6:]
+    assert f(ctypes.byref(s), *both, *tail) == pa.PA_ERR_INVALID_ARG      # seq_lens and positions
+    assert f(ctypes.byref(s), *neither, *tail) == pa.PA_ERR_INVALID_ARG   # neither
+    assert f(ctypes.byref(s), *fused[:7], None, FAKE, *tail) == pa.PA_ERR_INVALID_ARG  # k_new
+    assert f(ctypes.byref(s), *plain, 0.1, -1, FAKE, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), *plain, float("nan"), 0, FAKE, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), *plain, 0.1, 0, None, 1 << 30, None, None) == pa.PA_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), *plain, 0.1, 0, FAKE + 8, 1 << 30, None, None) == pa.PA_ERR_MISALIGNED
+    assert f(ctypes.byref(s), FAKE + 2, *plain[1:], *tail) == pa.PA_ERR_MISALIGNED
+    assert f(ctypes.byref(base_shape(head_dim=96, block_stride=2 * 2 * 16 * 96)), *plain, *tail) \
+        == pa.PA_ERR_UNSUPPORTED
+    assert f(ctypes.byref(base_shape(batch=0)), *plain, *tail) == pa.PA_OK
+    # sizes are queried on the device: no device here, so no size
+    assert pa.paged_attention_balanced_workspace(base_shape(batch=0)) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
     monkeypatch.setattr(pa, "_lib", None)
