@@ -175,17 +175,38 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def source_digest(name: str) -> str:
+    """sha256 over a kernel source file and every header it includes from the
+    tree (recursively), so that a change to shared device code also marks the
+    counters taken on the old build as stale."""
+    dirs = [ROOT / "pagedattention_decode_paged_gb300" / "csrc", ROOT / "include"]
+    seen, order, todo = set(), [], [name]
+    while todo:
+        n = todo.pop(0)
+        path = next((d / n for d in dirs if (d / n).exists()), None)
+        if path is None or n in seen:
+            continue
+        seen.add(n)
+        order.append(path)
+        todo += re.findall(r'^#include "([^"]+)"', path.read_text(), flags=re.M)
+    h = hashlib.sha256()
+    for path in order:
+        h.update(path.read_bytes())
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel: str, workload: str, fused: bool = False) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if still current.
 
-    The summary records the sha256 of the kernel's source file; when the
-    source has changed since the counters were taken, the figure is stale
-    and None is returned.
+    Summaries are named <kernel>__<description>_<workload>[_fused].md.  Each
+    records the source_digest() of its kernel at capture time; when the
+    sources have changed since, the figure is stale and None is returned.
     """
-    src = ROOT / "pagedattention_decode_paged_gb300" / "csrc" / KERNEL_SOURCES[kernel]
-    digest = hashlib.sha256(src.read_bytes()).hexdigest()
-    for f in sorted(PROFILE_DIR.glob(f"{kernel}*{workload}*.md")):
-        if ("fused" in f.name) != fused:
+    digest = source_digest(KERNEL_SOURCES[kernel])
+    pat = re.compile(rf"^{re.escape(kernel)}__.*_{re.escape(workload)}(_fused)?\.md$")
+    for f in sorted(PROFILE_DIR.glob(f"{kernel}__*.md")):
+        m = pat.match(f.name)
+        if m is None or (m.group(1) is not None) != fused:
             continue
         text = f.read_text()
         m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
@@ -234,6 +255,10 @@ def run_gpu(args) -> None:
     # each rank holds its own replica of the workload (weak scaling)
     w = workloads.make_workload(args.workload, block_size=args.block_size, device=dev,
                                 seed=1000 + args.workload + 7 * rank, batch=args.batch)
+    workload_key = f"w{args.workload}" + (f"_bs{args.block_size}" if args.block_size else "")
+    if args.long_seq:
+        w = workloads.with_long_sequence(w, args.long_seq, seed=7 + rank, device=dev)
+        workload_key += f"_long{args.long_seq}"
     kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
     shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
                           block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
@@ -484,7 +509,7 @@ def run_gpu(args) -> None:
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": kernel_traffic(kernel, f"w{args.workload}", fused),
+                         "traffic": kernel_traffic(kernel, workload_key, fused),
                          "kernel": kernel, "timed_launches": len(sampled),
                          "kernel_timing": "graph step" if graph is not None else "events"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -544,6 +569,8 @@ def run_reference(args) -> None:
         return
     w = workloads.make_workload(args.workload, block_size=args.block_size, device="cpu",
                                 batch=args.batch)
+    if args.long_seq:
+        w = workloads.with_long_sequence(w, args.long_seq)
     lens_after = w.lens + 1
     for i in range(args.warmup):
         _oracle_sample(w, lens_after, [i % w.B])
@@ -589,6 +616,8 @@ def main() -> None:
                     help="time the prompt write of every sequence's full length instead")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many steps into one CUDA graph and replay it")
+    ap.add_argument("--long-seq", type=int, default=0,
+                    help="replace the last sequence by one of this many tokens (skewed batch)")
     ap.add_argument("--balanced", action="store_true",
                     help="time paged_attention_decode_balanced (persistent load-balanced grid)")
     ap.add_argument("--unfused", action="store_true",

@@ -144,6 +144,57 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
         }
     };
 
+    // Merge the records of the item (b*H + h = bh) whose first tile is F,
+    // shared by warps g0..g1, and write its output: log-sum-exp over the
+    // records in slice order (the maximum first, lanes over records; then
+    // the weighted sums, eight records in flight per lane).
+    auto merge_item = [&](int64_t bh, int32_t F, int g0, int g1) {
+        const int n = g1 - g0 + 1;
+        auto rec_of = [&](int w) {
+            return p.records + ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) *
+                                   p.rec_floats;
+        };
+        float mloc = -INFINITY;
+        bool badloc = false;
+        for (int r = lane; r < n; r += 32) {
+            const float *rw = rec_of(g0 + r);
+            mloc = fmaxf(mloc, __ldcg(rw));
+            badloc |= __ldcg(rw + 2) != 0.f;
+        }
+        const float M = warp_max_f32(mloc);
+        const bool bad = __any_sync(0xffffffffu, badloc);
+        constexpr int DPL = (D + 31) / 32;
+        constexpr int U = 8;
+        float a[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) a[i] = 0.f;
+        float lsum = 0.f;
+        for (int r0 = 0; r0 < n; r0 += U) {
+            float mv[U], lv[U], av[U][DPL];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool live = r0 + u < n;
+                const float *rw = rec_of(g0 + min(r0 + u, n - 1));
+                mv[u] = live ? __ldcg(rw) : -INFINITY;
+                lv[u] = live ? __ldcg(rw + 1) : 0.f;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i)
+                    av[u][i] = (live && lane + 32 * i < D) ? __ldcg(rw + 4 + lane + 32 * i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float wt = merge_weight(mv[u], M);
+                lsum = fmaf(lv[u], wt, lsum);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) a[i] = fmaf(av[u][i], wt, a[i]);
+            }
+        }
+        const float inv = 1.f / lsum;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i)
+            if (lane + 32 * i < D) out[bh * D + lane + 32 * i] = Elem<T>::from_float(bad ? 0.f : a[i] * inv);
+    };
+
     TileCursor cc;   // the tile being computed
     cc.seek(pre, p.B, p.H, start);
     TileCursor ic = cc;   // the next tile to fetch (lane 0)
@@ -161,10 +212,6 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
     bool item_bad = false;
     float *pw = pbuf + warp * C::TILE;
     int dead_at = -1;   // tile whose copy never landed (the warp stops fetching)
-    // items shared with the neighbouring slices: [0] the slice's first item,
-    // [1] its last (F < 0: none)
-    int64_t pend_bh[2] = {0, 0};
-    int32_t pend_F[2] = {-1, -1}, pend_Lt[2] = {-1, -1};
 
     for (int idx = 0; idx < ntiles; ++idx) {
         const int slot = idx % S;
@@ -221,8 +268,8 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
                     *reinterpret_cast<uint4 *>(out + ((int64_t)b * p.H + h) * D + c * C::VEC) =
                         pack_out16<T, C::VEC>(acc2, 1.f / l_run, item_bad);
             } else {
-                // shared with the neighbouring slice: publish a record (counted
-                // after the loop, so its stores drain while the warp works on)
+                // shared with the neighbouring slices: publish a record; the
+                // last sharer to arrive merges them all
                 const int sid = F <= start ? 0 : 1;
                 float *rec = p.records + ((int64_t)gw * 2 + sid) * p.rec_floats;
                 if (lane < C::LPT) {
@@ -235,9 +282,10 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
                     rec[1] = l_run;
                     rec[2] = item_bad ? 1.f : 0.f;
                 }
-                pend_bh[sid] = (int64_t)b * p.H + h;
-                pend_F[sid] = F;
-                pend_Lt[sid] = Lt;
+                release_records();
+                const int g0 = slice_owner(F, total, W), g1 = slice_owner(Lt, total, W);
+                if (count_and_check_last(p.counters + (int64_t)b * p.H + h, g1 - g0 + 1, lane))
+                    merge_item((int64_t)b * p.H + h, F, g0, g1);
             }
         }
 
@@ -253,45 +301,6 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
         // let the copies already in flight land before the CTA can exit
         for (int kk = dead_at; kk < min(ntiles, dead_at + S); ++kk)
             mbar_wait(smem_u32(&wbar[kk % S]), (kk / S) & 1);
-    }
-
-    // count this warp on the items it shares; the last sharer of each merges
-    // the records (log-sum-exp, in slice order) and writes the output
-    if (pend_F[0] >= 0 || pend_F[1] >= 0) release_records();
-#pragma unroll
-    for (int sid = 0; sid < 2; ++sid) {
-        const int32_t F = pend_F[sid], Lt = pend_Lt[sid];
-        if (F < 0) continue;
-        const int g0 = slice_owner(F, total, W), g1 = slice_owner(Lt, total, W);
-        if (!count_and_check_last(p.counters + pend_bh[sid], g1 - g0 + 1, lane)) continue;
-        auto rec_of = [&](int w) {
-            return p.records + ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) *
-                                   p.rec_floats;
-        };
-        float M = -INFINITY;
-        bool bad = false;
-        for (int w = g0; w <= g1; ++w) {
-            M = fmaxf(M, __ldcg(rec_of(w)));
-            bad |= __ldcg(rec_of(w) + 2) != 0.f;
-        }
-        constexpr int DPL = (D + 31) / 32;
-        float a[DPL];
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) a[i] = 0.f;
-        float lsum = 0.f;
-        for (int w = g0; w <= g1; ++w) {
-            const float *rw = rec_of(w);
-            const float wt = merge_weight(__ldcg(rw), M);
-            lsum = fmaf(__ldcg(rw + 1), wt, lsum);
-#pragma unroll
-            for (int i = 0; i < DPL; ++i)
-                if (lane + 32 * i < D) a[i] = fmaf(__ldcg(rw + 4 + lane + 32 * i), wt, a[i]);
-        }
-        const float inv = 1.f / lsum;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i)
-            if (lane + 32 * i < D)
-                out[pend_bh[sid] * D + lane + 32 * i] = Elem<T>::from_float(bad ? 0.f : a[i] * inv);
     }
 }
 

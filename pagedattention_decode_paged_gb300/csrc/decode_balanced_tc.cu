@@ -177,10 +177,6 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
     float m_run[NT][2], l_run[NT][2];
     bool item_bad = false;
     int dead_at = -1;   // tile whose copy never landed (the warp stops fetching)
-    // items shared with the neighbouring slices: [0] the slice's first item,
-    // [1] its last (F < 0: none)
-    int pend_b[2] = {0, 0}, pend_it[2] = {0, 0};
-    int32_t pend_F[2] = {-1, -1}, pend_Lt[2] = {-1, -1};
 
     // write the item's output from the (merged) state; zeros when bad
     auto write_out = [&](int b, int h0, int nh, const float (&acc)[C::MT][NT][4], const float (&lsum)[NT][2],
@@ -199,6 +195,85 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
                     orow[mt * 16 + gid + 8] = Elem<T>::from_float(bad ? 0.f : acc[mt][nt][j + 2] * inv);
                 }
             }
+    };
+
+    // Merge the records of an item whose first tile is F, shared by warps
+    // g0..g1, register by register (log-sum-exp in slice order: the maxima
+    // first, then the weighted sums, several records in flight per lane),
+    // and write its output.
+    auto merge_item = [&](int b, int h0, int nh, int32_t F, int g0, int g1) {
+        const int n = g1 - g0 + 1;
+        auto rec_of = [&](int w) {
+            return p.records + ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) *
+                                   p.rec_floats;
+        };
+        constexpr int UM = 8, UA = NT == 1 ? 2 : 1;
+        float M[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) M[nt][0] = M[nt][1] = -INFINITY;
+        bool bad = false;
+        for (int r0 = 0; r0 < n; r0 += UM) {
+            float mv[UM][NT][2];
+            bool bv[UM];
+#pragma unroll
+            for (int u = 0; u < UM; ++u) {
+                const bool live = r0 + u < n;
+                const float *rw = rec_of(g0 + min(r0 + u, n - 1));
+                bv[u] = live && __ldcg(rw) != 0.f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        mv[u][nt][j] = live ? __ldcg(rw + 4 + (C::NF + nt * 2 + j) * 32 + lane) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < UM; ++u) {
+                bad |= bv[u];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) M[nt][j] = fmaxf(M[nt][j], mv[u][nt][j]);
+            }
+        }
+        float acc[C::MT][NT][4], lsum[NT][2];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
+        for (int r0 = 0; r0 < n; r0 += UA) {
+            float rv[UA][C::NF + NT * 4];
+#pragma unroll
+            for (int u = 0; u < UA; ++u) {
+                const bool live = r0 + u < n;
+                const float *rw = rec_of(g0 + min(r0 + u, n - 1)) + 4;
+#pragma unroll
+                for (int f = 0; f < C::NF + NT * 4; ++f)
+                    rv[u][f] = live ? __ldcg(rw + f * 32 + lane) : (f >= C::NF && f < C::NF + NT * 2 ? -INFINITY : 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < UA; ++u) {
+                float wt[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        wt[nt][j] = merge_weight(rv[u][C::NF + nt * 2 + j], M[nt][j]);
+                        lsum[nt][j] = fmaf(rv[u][C::NF + NT * 2 + nt * 2 + j], wt[nt][j], lsum[nt][j]);
+                    }
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[mt][nt][e] = fmaf(rv[u][(mt * NT + nt) * 4 + e], wt[nt][e & 1], acc[mt][nt][e]);
+            }
+        }
+        write_out(b, h0, nh, acc, lsum, bad);
     };
 
     for (int idx = 0; idx < ntiles; ++idx) {
@@ -297,8 +372,8 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
             if (F >= start && Lt < end) {
                 write_out(b, h0, nh, o_acc, l_run, item_bad);
             } else {
-                // shared with the neighbouring slice: publish a record (counted
-                // after the loop, so its stores drain while the warp works on)
+                // shared with the neighbouring slices: publish a record; the
+                // last sharer to arrive merges them all
                 const int sid = F <= start ? 0 : 1;
                 float *rec = p.records + ((int64_t)gw * 2 + sid) * p.rec_floats;
                 if (lane == 0) rec[0] = item_bad ? 1.f : 0.f;
@@ -316,10 +391,10 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
                         rf[(C::NF + nt * 2 + j) * 32 + lane] = m_run[nt][j];
                         rf[(C::NF + NT * 2 + nt * 2 + j) * 32 + lane] = l_run[nt][j];
                     }
-                pend_b[sid] = b;
-                pend_it[sid] = cc.it;
-                pend_F[sid] = F;
-                pend_Lt[sid] = Lt;
+                release_records();
+                const int g0 = slice_owner(F, total, W), g1 = slice_owner(Lt, total, W);
+                if (count_and_check_last(p.counters + (int64_t)b * NI + cc.it, g1 - g0 + 1, lane))
+                    merge_item(b, h0, nh, F, g0, g1);
             }
         }
 
@@ -335,66 +410,6 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
         // let the copies already in flight land before the CTA can exit
         for (int kk = dead_at; kk < min(ntiles, dead_at + S); ++kk)
             mbar_wait(smem_u32(&wbar[kk % S]), (kk / S) & 1);
-    }
-
-    // count this warp on the items it shares; the last sharer of each merges
-    // the records (log-sum-exp, in slice order, register by register)
-    if (pend_F[0] >= 0 || pend_F[1] >= 0) release_records();
-#pragma unroll
-    for (int sid = 0; sid < 2; ++sid) {
-        const int32_t F = pend_F[sid], Lt = pend_Lt[sid];
-        if (F < 0) continue;
-        const int g0 = slice_owner(F, total, W), g1 = slice_owner(Lt, total, W);
-        if (!count_and_check_last(p.counters + (int64_t)pend_b[sid] * NI + pend_it[sid], g1 - g0 + 1, lane))
-            continue;
-        auto rec_of = [&](int w) {
-            return p.records + ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) *
-                                   p.rec_floats;
-        };
-        float M[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) M[nt][0] = M[nt][1] = -INFINITY;
-        bool bad = false;
-        for (int w = g0; w <= g1; ++w) {
-            const float *rw = rec_of(w);
-            bad |= __ldcg(rw) != 0.f;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    M[nt][j] = fmaxf(M[nt][j], __ldcg(rw + 4 + (C::NF + nt * 2 + j) * 32 + lane));
-        }
-        float acc[C::MT][NT][4], lsum[NT][2];
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) lsum[nt][0] = lsum[nt][1] = 0.f;
-        for (int w = g0; w <= g1; ++w) {
-            const float *rw = rec_of(w) + 4;
-            float wt[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    wt[nt][j] = merge_weight(__ldcg(rw + (C::NF + nt * 2 + j) * 32 + lane), M[nt][j]);
-                    lsum[nt][j] = fmaf(__ldcg(rw + (C::NF + NT * 2 + nt * 2 + j) * 32 + lane), wt[nt][j],
-                                       lsum[nt][j]);
-                }
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        acc[mt][nt][e] = fmaf(__ldcg(rw + ((mt * NT + nt) * 4 + e) * 32 + lane), wt[nt][e & 1],
-                                              acc[mt][nt][e]);
-        }
-        const int hk = pend_it[sid] / ngroups, hg = pend_it[sid] % ngroups;
-        write_out(pend_b[sid], hk * g + hg * 16, min(16, g - hg * 16), acc, lsum, bad);
     }
 }
 

@@ -325,3 +325,15 @@ class SeparatePoolWorkload(Workload):
         copied = {k: (v.clone() if isinstance(v, torch.Tensor) else v)
                   for k, v in self.__dict__.items()}
         return SeparatePoolWorkload(**copied)
+
+
+def with_long_sequence(w: Workload, length: int, *, seed: int = 7, device="cpu") -> Workload:
+    """The same shape as `w` with its last sequence replaced by one of
+    `length` tokens (pre-append): a serving batch where one long-context
+    request runs beside many ordinary ones.  Fresh seeded data, shuffled
+    block ids, unpoisoned."""
+    lens = [int(x) for x in w.lens.cpu()]
+    lens[-1] = int(length)
+    return make_generic(B=w.B, H=w.H, Hkv=w.Hkv, D=w.D, bs=w.bs, dtype=w.dtype, lens=lens,
+                        seed=seed, device=device, poison=False,
+                        name=f"{w.name}+1x{length}")
