@@ -83,6 +83,18 @@ def _lib():
             lib.pao_attention_decode_window.restype = i32
             lib.pao_attention_decode_window.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i32,
                                                         vp, vp, vp, vp, vp, dbl, i64, vp, vp, i32]
+            lib.pao_quantize_i8.restype = ctypes.c_byte
+            lib.pao_quantize_i8.argtypes = [ctypes.c_float, ctypes.c_float]
+            lib.pao_quantize_i8_array.restype = None
+            lib.pao_quantize_i8_array.argtypes = [vp, i64, ctypes.c_float, vp]
+            lib.pao_kv_append_i8.restype = i32
+            lib.pao_kv_append_i8.argtypes = [i32, i32, i32, i32, i32, i64, i64, i32,
+                                             vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.pao_gather_i8.restype = None
+            lib.pao_gather_i8.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, i32, i64, vp, vp]
+            lib.pao_attention_decode_i8.restype = i32
+            lib.pao_attention_decode_i8.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i32,
+                                                    vp, vp, vp, vp, vp, vp, dbl, vp, vp, i32]
             lib.pao_kv_append.restype = i32
             lib.pao_kv_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, i32,
                                           vp, vp, vp, vp, vp, vp, vp]
@@ -116,6 +128,12 @@ def _ptr(x) -> int:
     if not x.is_contiguous():
         raise ValueError("oracle: tensor must be contiguous")
     return x.data_ptr()
+
+
+def _f32(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
 
 
 def _i32(x) -> np.ndarray:
@@ -274,4 +292,73 @@ def attention_decode_window(q, k_pool, v_pool, block_table, seq_lens, scale: flo
                                        _ptr(v_pool), bt.ctypes.data, sl.ctypes.data,
                                        float(scale), int(window), out.ctypes.data,
                                        err.ctypes.data, int(threads))
+    return out, err
+
+
+# ---------------------------------------------------------------------------
+# int8 cache blocks with per-(block, kv head) scales
+# ---------------------------------------------------------------------------
+# The pages name int8-quantised cache blocks ("KV Cache and BlockManager"
+# s6.3; the "quantized" element size of its s3 block-size rule) without a
+# scheme.  The reading implemented in pa_oracle.c: a code c in [-127, 127]
+# stands for c * s, with one fp32 scale s per (physical block, kv head) for K
+# and one for V, kv_scales[(blk*2 + 0)*Hkv + hk] and [(blk*2 + 1)*Hkv + hk];
+# writing x stores clamp(round_half_even(x / s), -127, 127), decided in IEEE
+# binary32 (a NaN quotient stores 0).
+
+def quantize_i8(x, scale: float) -> np.ndarray:
+    """int8 codes of the float32 values x under one scale (binary32 x / s,
+    ties to even, clamped to [-127, 127])."""
+    xs = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(xs.shape, dtype=np.int8)
+    _lib().pao_quantize_i8_array(xs.ctypes.data, xs.size, float(np.float32(scale)), out.ctypes.data)
+    return out
+
+
+def kv_append_i8(k_new, v_new, k_pool, v_pool, kv_scales, block_table, positions, *,
+                 block_size: int, block_stride: int, num_blocks: int):
+    """Append one token per (sequence, kv head) into int8 pools, quantising
+    with the scales of the target block (in place; returns seq_err)."""
+    B, Hkv, D = (int(s) for s in k_new.shape)
+    bt = _i32(block_table)
+    pos = _i32(positions)
+    sc = _f32(kv_scales)
+    MB = bt.shape[1]
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_kv_append_i8(B, Hkv, D, block_size, MB, num_blocks, block_stride,
+                            _dtype_code(k_new), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                            _ptr(v_pool), sc.ctypes.data, bt.ctypes.data, pos.ctypes.data,
+                            err.ctypes.data)
+    return err
+
+
+def gather_i8(k_pool, v_pool, kv_scales, table_row, kv_head: int, length: int, *,
+              block_size: int, head_dim: int, num_kv_heads: int, block_stride: int):
+    """Contiguous [length][head_dim] dequantised K and V of one kv head."""
+    row = _i32(table_row)
+    sc = _f32(kv_scales)
+    Kc = np.empty((max(length, 1), head_dim), dtype=np.float64)
+    Vc = np.empty_like(Kc)
+    _lib().pao_gather_i8(head_dim, block_size, num_kv_heads, block_stride, _ptr(k_pool),
+                         _ptr(v_pool), sc.ctypes.data, row.ctypes.data, kv_head, length,
+                         Kc.ctypes.data, Vc.ctypes.data)
+    return Kc[:length], Vc[:length]
+
+
+def attention_decode_i8(q, k_pool, v_pool, kv_scales, block_table, seq_lens, scale: float, *,
+                        num_kv_heads: int, block_size: int, block_stride: int,
+                        num_blocks: int, threads: int = 0):
+    """Decode attention over an int8 cache (the values the codes stand for),
+    masked to seq_lens.  Returns (out float64 [B][H][D], seq_err int32 [B])."""
+    B, H, D = (int(s) for s in q.shape)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    sc = _f32(kv_scales)
+    MB = bt.shape[1]
+    out = np.empty((B, H, D), dtype=np.float64)
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_attention_decode_i8(B, H, num_kv_heads, D, block_size, MB, num_blocks,
+                                   block_stride, _dtype_code(q), _ptr(q), _ptr(k_pool),
+                                   _ptr(v_pool), sc.ctypes.data, bt.ctypes.data, sl.ctypes.data,
+                                   float(scale), out.ctypes.data, err.ctypes.data, int(threads))
     return out, err

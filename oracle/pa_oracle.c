@@ -511,3 +511,148 @@ int pao_attention_decode_window(int B, int H, int Hkv, int D, int bs, int MB, in
     }
     return any;
 }
+
+/* ------------------------------------------------------------------------ */
+/* int8 cache blocks with per-block scales                                   */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name quantised cache blocks (int8 blocks in the semantic
+ * compression scheme of [BM] s6.3, a "quantized" element size in the block
+ * sizing rule of [BM] s3) but fix no scheme.  The reading used here, the
+ * plainest one that matches "int8 blocks with per-block scales":
+ *   - a cached K (or V) element is a signed code c in [-127, 127] that
+ *     stands for the value c * s, where s is the fp32 scale of its
+ *     (physical block, kv head) for K (or for V);
+ *   - scales are stored as kv_scales[(blk*2 + 0)*Hkv + hk] (K) and
+ *     kv_scales[(blk*2 + 1)*Hkv + hk] (V), set by whoever allocates the
+ *     block;
+ *   - writing a value x gives c = clamp(round_half_even(x / s), -127, 127),
+ *     the division and the rounding taken in IEEE binary32 (the precision
+ *     in which the GPU decides the integer); a NaN quotient gives 0.
+ * Pools hold one byte per element, laid out like the 16-bit pools. */
+
+signed char pao_quantize_i8(float x, float s)
+{
+    volatile float q = x / s;   /* binary32 division, round to nearest even */
+    float r = rintf(q);         /* nearest integer, ties to even */
+    if (r != r)
+        return 0;
+    if (r > 127.0f)
+        r = 127.0f;
+    if (r < -127.0f)
+        r = -127.0f;
+    return (signed char)r;
+}
+
+void pao_quantize_i8_array(const float *x, int64_t n, float s, signed char *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = pao_quantize_i8(x[i], s);
+}
+
+/* As pao_kv_append, but the new rows (k_new, v_new of `dtype`) are written
+ * as int8 codes with the scale of their target (block, kv head). */
+int pao_kv_append_i8(int B, int Hkv, int D, int bs, int MB, int64_t NB,
+                     int64_t block_stride, int dtype, const void *k_new,
+                     const void *v_new, signed char *k_pool, signed char *v_pool,
+                     const float *kv_scales, const int32_t *block_table,
+                     const int32_t *positions, int32_t *seq_err)
+{
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t pos = positions[b];
+        seq_err[b] = 0;
+        if (pos < 0 || pos >= (int64_t)MB * bs) {
+            seq_err[b] = PAO_SEQ_BAD_POS;
+            any |= seq_err[b];
+            continue;
+        }
+        int64_t blk = block_table[(int64_t)b * MB + pos / bs];
+        if (blk < 0 || blk >= NB) {
+            seq_err[b] = PAO_SEQ_BAD_BLOCK;
+            any |= seq_err[b];
+            continue;
+        }
+        for (int hk = 0; hk < Hkv; ++hk) {
+            int64_t dst = blk * block_stride + (int64_t)hk * bs * D + (pos % bs) * D;
+            int64_t src = ((int64_t)b * Hkv + hk) * D;
+            float sk = kv_scales[(blk * 2 + 0) * Hkv + hk];
+            float sv = kv_scales[(blk * 2 + 1) * Hkv + hk];
+            for (int d = 0; d < D; ++d) {
+                k_pool[dst + d] = pao_quantize_i8((float)pao_element(k_new, src + d, dtype), sk);
+                v_pool[dst + d] = pao_quantize_i8((float)pao_element(v_new, src + d, dtype), sv);
+            }
+        }
+    }
+    return any;
+}
+
+/* Gather of an int8 cache: the values c * s of kv head hk, tokens [0, len). */
+void pao_gather_i8(int D, int bs, int Hkv, int64_t block_stride,
+                   const signed char *k_pool, const signed char *v_pool,
+                   const float *kv_scales, const int32_t *table_row, int hk,
+                   int64_t len, double *Kc, double *Vc)
+{
+    for (int64_t t = 0; t < len; ++t) {
+        int64_t blk = table_row[t / bs];
+        int64_t base = blk * block_stride + (int64_t)hk * bs * D + (t % bs) * D;
+        double sk = kv_scales[(blk * 2 + 0) * Hkv + hk];
+        double sv = kv_scales[(blk * 2 + 1) * Hkv + hk];
+        for (int d = 0; d < D; ++d) {
+            Kc[t * D + d] = (double)k_pool[base + d] * sk;
+            Vc[t * D + d] = (double)v_pool[base + d] * sv;
+        }
+    }
+}
+
+/* Decode attention over an int8 cache: the textbook attention of
+ * pao_attention_decode over the values the codes stand for.  q is [B][H][D]
+ * of `dtype`. */
+int pao_attention_decode_i8(int B, int H, int Hkv, int D, int bs, int MB,
+                            int64_t NB, int64_t block_stride, int dtype,
+                            const void *q, const signed char *k_pool,
+                            const signed char *v_pool, const float *kv_scales,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            double scale, double *out, int32_t *seq_err,
+                            int nthreads)
+{
+    int group = H / Hkv;
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        seq_err[b] = validate_sequence(seq_lens[b], bs, MB, NB,
+                                       block_table + (int64_t)b * MB);
+        any |= seq_err[b];
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+        int b = (int)(u / Hkv);
+        int hk = (int)(u % Hkv);
+        int64_t len = seq_lens[b];
+        if (seq_err[b]) {
+            for (int h = hk * group; h < (hk + 1) * group; ++h)
+                for (int d = 0; d < D; ++d)
+                    out[((int64_t)b * H + h) * D + d] = 0.0;
+            continue;
+        }
+        size_t n = (size_t)(len > 0 ? len : 1) * D;
+        double *Kc = (double *)malloc(n * sizeof(double));
+        double *Vc = (double *)malloc(n * sizeof(double));
+        double *qd = (double *)malloc((size_t)D * sizeof(double));
+        pao_gather_i8(D, bs, Hkv, block_stride, k_pool, v_pool, kv_scales,
+                      block_table + (int64_t)b * MB, hk, len, Kc, Vc);
+        for (int h = hk * group; h < (hk + 1) * group; ++h) {
+            for (int d = 0; d < D; ++d)
+                qd[d] = pao_element(q, ((int64_t)b * H + h) * D + d, dtype);
+            pao_attention_contiguous(len, D, qd, Kc, Vc, scale,
+                                     out + ((int64_t)b * H + h) * D);
+        }
+        free(Kc);
+        free(Vc);
+        free(qd);
+    }
+    return any;
+}

@@ -602,6 +602,141 @@ def test_window_decode_pins():
 
 
 # ---------------------------------------------------------------------------
+# int8 cache blocks with per-(block, kv head) scales
+# ---------------------------------------------------------------------------
+
+def _np_quantize(x, s):
+    """Independent restatement of the code rule: IEEE binary32 quotient,
+    numpy's round-half-to-even, clamp to [-127, 127], NaN to 0."""
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        r = np.rint(np.asarray(x, dtype=np.float32) / np.float32(s))
+    r = np.where(np.isnan(r), 0.0, np.clip(r, -127.0, 127.0))
+    return r.astype(np.int8)
+
+
+def test_quantize_i8_pins():
+    # worked by hand: ties go to the even integer, out-of-range values clamp
+    cases = [(2.5, 1.0, 2), (3.5, 1.0, 4), (-2.5, 1.0, -2), (-3.5, 1.0, -4), (0.5, 1.0, 0),
+             (1.5, 1.0, 2), (0.75, 0.5, 2), (0.25, 0.5, 0), (127.5, 1.0, 127), (-127.5, 1.0, -127),
+             (1e6, 1.0, 127), (-1e6, 1.0, -127), (float("inf"), 1.0, 127),
+             (float("-inf"), 1.0, -127), (float("nan"), 1.0, 0), (0.3, 0.1, 3), (-0.0, 2.0, 0)]
+    for x, sc, c in cases:
+        assert int(oracle.quantize_i8([x], sc)[0]) == c, (x, sc, c)
+    rng = np.random.default_rng(5)
+    x = (rng.normal(0.0, 3.0, 20000)).astype(np.float32)
+    sc = np.float32(0.037)
+    codes = oracle.quantize_i8(x, sc)
+    assert np.array_equal(codes, _np_quantize(x, sc))
+    inside = np.abs(x) <= 127 * sc
+    err = np.abs(x[inside].astype(np.float64) - codes[inside].astype(np.float64) * float(sc))
+    assert err.max() <= float(sc) / 2 * (1 + 1e-6)
+
+
+def _i8_case(seed, B=3, H=4, Hkv=2, D=16, bs=4, lens=(0, 5, 11)):
+    rng = np.random.default_rng(seed)
+    nblk = [-(-L // bs) for L in lens]
+    NB = sum(nblk) + 3
+    MB = max(nblk) + 1
+    perm = rng.permutation(NB)
+    table = np.full((B, MB), -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        table[b, :nblk[b]] = perm[k:k + nblk[b]]
+        k += nblk[b]
+    pool = rng.integers(-127, 128, size=(NB, 2, Hkv, bs, D)).astype(np.int8)
+    scales = rng.uniform(0.01, 0.1, size=(NB, 2, Hkv)).astype(np.float32)
+    q = rng.normal(size=(B, H, D)).astype(np.float32)
+    return dict(B=B, H=H, Hkv=Hkv, D=D, bs=bs, NB=NB, MB=MB, lens=np.array(lens, dtype=np.int32),
+                table=table, pool=pool, scales=scales, q=q, stride=2 * Hkv * bs * D)
+
+
+def test_i8_decode_brute_force():
+    """Tiny case against per-token Python loops over the dequantised values."""
+    c = _i8_case(11)
+    flat = c["pool"].reshape(-1)
+    out, err = oracle.attention_decode_i8(c["q"], flat, flat[c["Hkv"] * c["bs"] * c["D"]:],
+                                          c["scales"], c["table"], c["lens"], 0.3,
+                                          num_kv_heads=c["Hkv"], block_size=c["bs"],
+                                          block_stride=c["stride"], num_blocks=c["NB"])
+    assert not err.any()
+    g = c["H"] // c["Hkv"]
+    for b in range(c["B"]):
+        for h in range(c["H"]):
+            hk = h // g
+            L = int(c["lens"][b])
+            if L == 0:
+                assert not out[b, h].any()
+                continue
+            K = np.empty((L, c["D"]))
+            V = np.empty((L, c["D"]))
+            for t in range(L):
+                blk = c["table"][b, t // c["bs"]]
+                K[t] = c["pool"][blk, 0, hk, t % c["bs"]].astype(np.float64) * float(c["scales"][blk, 0, hk])
+                V[t] = c["pool"][blk, 1, hk, t % c["bs"]].astype(np.float64) * float(c["scales"][blk, 1, hk])
+            x = 0.3 * (K @ c["q"][b, h].astype(np.float64))
+            w = np.exp(x - x.max())
+            np.testing.assert_allclose(out[b, h], (w[:, None] * V).sum(0) / w.sum(), rtol=0, atol=1e-12)
+
+
+def test_i8_decode_equals_float_decode_on_exact_values():
+    """Codes times power-of-two scales are exact in binary32: the int8 oracle
+    and the float oracle (pinned to torch's attention above) see the same
+    values, so they agree to rounding."""
+    c = _i8_case(12, B=2, H=8, Hkv=2, D=32, bs=8, lens=(40, 17))
+    c["scales"] = (2.0 ** np.random.default_rng(3).integers(-8, -2, size=c["scales"].shape)).astype(np.float32)
+    deq = c["pool"].astype(np.float32) * c["scales"][:, :, :, None, None]
+    fflat = np.ascontiguousarray(deq).reshape(-1)
+    iflat = c["pool"].reshape(-1)
+    off = c["Hkv"] * c["bs"] * c["D"]
+    kw = dict(num_kv_heads=c["Hkv"], block_size=c["bs"], block_stride=c["stride"], num_blocks=c["NB"])
+    ref, e1 = oracle.attention_decode(c["q"], fflat, fflat[off:], c["table"], c["lens"], 0.2, **kw)
+    got, e2 = oracle.attention_decode_i8(c["q"], iflat, iflat[off:], c["scales"], c["table"], c["lens"],
+                                         0.2, **kw)
+    assert not e1.any() and not e2.any()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+
+
+def test_i8_append_writes_the_codes_of_its_block_scale():
+    c = _i8_case(13, B=3, H=4, Hkv=2, D=16, bs=4, lens=(3, 8, 9))
+    NB, Hkv, D, bs = c["NB"], c["Hkv"], c["D"], c["bs"]
+    # give every sequence a block for position len
+    used = set(int(x) for x in c["table"].ravel() if x >= 0)
+    free = [i for i in range(NB) if i not in used]
+    for b in range(c["B"]):
+        for j in range(-(-(int(c["lens"][b]) + 1) // bs)):
+            if c["table"][b, j] < 0:
+                c["table"][b, j] = free.pop()
+    gen = torch.Generator().manual_seed(4)
+    kn = torch.randn((c["B"], Hkv, D), generator=gen).to(torch.bfloat16)
+    vn = torch.randn((c["B"], Hkv, D), generator=gen).to(torch.bfloat16)
+    pool = c["pool"].copy()
+    flat = pool.reshape(-1)
+    err = oracle.kv_append_i8(kn, vn, flat, flat[Hkv * bs * D:], c["scales"], c["table"], c["lens"],
+                              block_size=bs, block_stride=c["stride"], num_blocks=NB)
+    assert not err.any()
+    want = c["pool"].copy()
+    for b in range(c["B"]):
+        pos = int(c["lens"][b])
+        blk = c["table"][b, pos // bs]
+        for hk in range(Hkv):
+            want[blk, 0, hk, pos % bs] = _np_quantize(kn[b, hk].float().numpy(), c["scales"][blk, 0, hk])
+            want[blk, 1, hk, pos % bs] = _np_quantize(vn[b, hk].float().numpy(), c["scales"][blk, 1, hk])
+    assert np.array_equal(pool, want)
+    # a position past the row and a hole in the table are skipped and flagged
+    pos = c["lens"].copy()
+    pos[0] = c["MB"] * bs
+    tab = c["table"].copy()
+    tab[1, int(c["lens"][1]) // bs] = -1
+    pool2 = c["pool"].copy()
+    f2 = pool2.reshape(-1)
+    err = oracle.kv_append_i8(kn, vn, f2, f2[Hkv * bs * D:], c["scales"], tab, pos,
+                              block_size=bs, block_stride=c["stride"], num_blocks=NB)
+    assert list(err) == [oracle.SEQ_BAD_POS, oracle.SEQ_BAD_BLOCK, 0]
+    changed = np.nonzero((pool2 != c["pool"]).reshape(NB, -1).any(1))[0]
+    assert list(changed) == [int(c["table"][2, int(c["lens"][2]) // bs])]
+
+
+# ---------------------------------------------------------------------------
 # the battery catches plausible mistakes planted in a copy of the oracle
 # ---------------------------------------------------------------------------
 
@@ -621,6 +756,15 @@ MUTANTS = {
                                "for (int64_t t = 0; t < T && start + t < (int64_t)MB * bs; ++t) {\n                int64_t pos = start + t;"),
     "one padding slot read": ("int64_t len = seq_lens[b];\n        if (seq_err[b]) {",
                               "int64_t len = seq_lens[b] + (seq_lens[b] % bs != 0);\n        if (seq_err[b]) {"),
+    "int8 codes truncated": ("float r = rintf(q);", "float r = truncf(q);"),
+    "int8 ties away from zero": ("float r = rintf(q);", "float r = roundf(q);"),
+    "int8 not clamped": ("    if (r > 127.0f)\n        r = 127.0f;\n", ""),
+    "int8 K read with the V scale": ("double sk = kv_scales[(blk * 2 + 0) * Hkv + hk];",
+                                     "double sk = kv_scales[(blk * 2 + 1) * Hkv + hk];"),
+    "int8 scale of the logical block": ("double sv = kv_scales[(blk * 2 + 1) * Hkv + hk];",
+                                        "double sv = kv_scales[((t / bs) * 2 + 1) * Hkv + hk];"),
+    "int8 append with the V scale": ("float sk = kv_scales[(blk * 2 + 0) * Hkv + hk];",
+                                     "float sk = kv_scales[(blk * 2 + 1) * Hkv + hk];"),
 }
 
 
@@ -635,7 +779,10 @@ def _battery(lib) -> bool:
                  test_single_token_returns_v0_exactly,
                  test_constant_values_give_that_constant,
                  test_window_decode_pins,
-                 lambda: test_multi_token_append_equals_token_by_token("f32")]
+                 lambda: test_multi_token_append_equals_token_by_token("f32"),
+                 test_quantize_i8_pins,
+                 test_i8_decode_brute_force,
+                 test_i8_append_writes_the_codes_of_its_block_scale]
         for t in tests:
             try:
                 t()
@@ -652,7 +799,8 @@ def _load_like_real(path):
     for fn in ("pao_blocks_needed", "pao_kv_bytes", "pao_convert", "pao_gather",
                "pao_attention_contiguous", "pao_attention_decode", "pao_attention_partial",
                "pao_merge_partials", "pao_kv_append", "pao_kv_append_tokens",
-               "pao_attention_decode_window"):
+               "pao_attention_decode_window", "pao_quantize_i8", "pao_quantize_i8_array",
+               "pao_kv_append_i8", "pao_gather_i8", "pao_attention_decode_i8"):
         getattr(lib, fn).restype = getattr(real, fn).restype
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
     return lib
