@@ -49,6 +49,7 @@ PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
                   "decode_simt_balanced": "decode_balanced_simt.cu",
                   "decode_tc_balanced": "decode_balanced_tc.cu",
+                  "decode_int8": "decode_int8.cu",
                   "append_tokens": "append.cu"}
 
 
@@ -63,9 +64,10 @@ def decode_bytes(w, lens_after, window: int = 0) -> int:
     HBM once).  With a sliding window only the last `window` rows count.
     """
     s = w.q.element_size()
+    s_kv = w.pool.element_size()           # 1 for an int8 cache
     lens = [int(x) for x in lens_after]
     tab = w.block_table.cpu()
-    row_bytes = w.Hkv * w.D * s            # one token, all kv heads, K or V
+    row_bytes = w.Hkv * w.D * s_kv         # one token, all kv heads, K or V
     rows = {}                              # (block, slot) rows read, shared ones once
     tables = 0
     for b, L in enumerate(lens):
@@ -78,7 +80,9 @@ def decode_bytes(w, lens_after, window: int = 0) -> int:
             cur = rows.get(blk)
             rows[blk] = (a, e) if cur is None else (min(cur[0], a), max(cur[1], e))
     kv = 2 * row_bytes * sum(e - a for a, e in rows.values())
-    return kv + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
+    # an int8 cache also reads the K and V scales of every block it touches
+    scales = 2 * 4 * w.Hkv * len(rows) if getattr(w, "scales", None) is not None else 0
+    return kv + scales + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
 
 
 def prefill_bytes(w) -> int:
@@ -93,13 +97,18 @@ def prefill_bytes(w) -> int:
 
 
 def logical_kv_bytes(w, lens_after) -> int:
-    s = w.q.element_size()
+    s = w.pool.element_size()
     return 2 * w.Hkv * w.D * s * sum(int(x) for x in lens_after)
 
 
 def append_bytes(w) -> int:
+    """Read the new K/V rows, write them into the pool (as codes for an int8
+    cache, which also reads the target blocks' scales), plus positions and
+    table entries."""
     s = w.k_new.element_size()
-    return 2 * 2 * w.B * w.Hkv * w.D * s + 4 * w.B + 4 * w.B
+    s_kv = w.pool.element_size()
+    scales = 2 * 4 * w.B * w.Hkv if getattr(w, "scales", None) is not None else 0
+    return 2 * w.B * w.Hkv * w.D * (s + s_kv) + scales + 4 * w.B + 4 * w.B
 
 
 # ---------------------------------------------------------------------------
@@ -259,12 +268,19 @@ def run_gpu(args) -> None:
     if args.long_seq:
         w = workloads.with_long_sequence(w, args.long_seq, seed=7 + rank, device=dev)
         workload_key += f"_long{args.long_seq}"
+    if args.int8:
+        if args.prefill or args.window or args.balanced or args.graph:
+            raise SystemExit("--int8 times the int8 append + decode pair only")
+        w = workloads.to_int8(w, seed=17 + rank).to(dev)
+        workload_key += "_int8"
     kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
     shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
                           block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
                           block_stride=w.block_stride, dtype=w.dtype)
     path = pa.paged_attention_decode_path(shape)
     kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
+    if args.int8:
+        kernel = "decode_int8"
     if args.prefill:
         kernel = "append_tokens"
     ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
@@ -276,13 +292,15 @@ def run_gpu(args) -> None:
           if ptok else None)
     stream = torch.cuda.current_stream()
 
-    fused = not ptok and not args.unfused
+    fused = not ptok and not args.unfused and not args.int8
 
     window = args.window or 0
     balanced = args.balanced
     if window and not balanced:
         fused = False
     bws = None
+    if args.int8:
+        ptok = None
     if balanced:
         ptok = None
         fused = not args.unfused
@@ -317,6 +335,11 @@ def run_gpu(args) -> None:
             calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
                               w.block_table, prefill["start"], w.lens, **kw))
             return calls, []
+        if args.int8:
+            calls.append(bind(pa.paged_attention_decode_int8, out, w.q, kflat, vflat, w.scales,
+                              w.block_table, lens_after, w.scale, num_kv_heads=w.Hkv, **kw))
+            return calls, [bind(pa.paged_kv_append_int8, w.k_new, w.v_new, kflat, vflat, w.scales,
+                                w.block_table, positions, **kw)]
         if balanced:
             if fused:
                 calls.append(bind(pa.paged_attention_decode_balanced, out, w.q, kflat, vflat,
@@ -537,12 +560,18 @@ def _oracle_sample(w, lens_after, seqs):
     lens = lens_after.index_select(0, sub).contiguous()
     flat = w.pool.view(-1)
     t = time.perf_counter()
-    oracle.attention_decode(q, flat, flat[w.v_offset:], table, lens, w.scale,
-                            num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
-                            num_blocks=w.NB, threads=os.cpu_count() or 1)
+    if getattr(w, "scales", None) is not None:
+        oracle.attention_decode_i8(q, flat, flat[w.v_offset:], w.scales, table, lens, w.scale,
+                                   num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
+                                   num_blocks=w.NB, threads=os.cpu_count() or 1)
+    else:
+        oracle.attention_decode(q, flat, flat[w.v_offset:], table, lens, w.scale,
+                                num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
+                                num_blocks=w.NB, threads=os.cpu_count() or 1)
     dt = time.perf_counter() - t
-    s = w.q.element_size()
-    nbytes = sum(2 * w.Hkv * w.D * s * int(L) + 4 * -(-int(L) // w.bs) + 4 + 2 * w.H * w.D * s
+    s = w.pool.element_size()
+    sq = w.q.element_size()
+    nbytes = sum(2 * w.Hkv * w.D * s * int(L) + 4 * -(-int(L) // w.bs) + 4 + 2 * w.H * w.D * sq
                  for L in lens)
     return nbytes, dt
 
@@ -571,6 +600,8 @@ def run_reference(args) -> None:
                                 batch=args.batch)
     if args.long_seq:
         w = workloads.with_long_sequence(w, args.long_seq)
+    if args.int8:
+        w = workloads.to_int8(w)
     lens_after = w.lens + 1
     for i in range(args.warmup):
         _oracle_sample(w, lens_after, [i % w.B])
@@ -618,6 +649,9 @@ def main() -> None:
                     help="capture this many steps into one CUDA graph and replay it")
     ap.add_argument("--long-seq", type=int, default=0,
                     help="replace the last sequence by one of this many tokens (skewed batch)")
+    ap.add_argument("--int8", action="store_true",
+                    help="int8 cache with per-block scales (paged_kv_append_int8 + "
+                         "paged_attention_decode_int8)")
     ap.add_argument("--balanced", action="store_true",
                     help="time paged_attention_decode_balanced (persistent load-balanced grid)")
     ap.add_argument("--unfused", action="store_true",

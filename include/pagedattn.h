@@ -14,6 +14,8 @@
  *                                   long contexts or few sequences)
  *   paged_attention_decode_balanced the same step on a persistent grid with
  *                                   equal work per warp (mixed lengths)
+ *   paged_kv_append_int8,           the same write and attention over an
+ *   paged_attention_decode_int8     int8 cache with per-block scales
  *
  * Sources (web pages on paged KV caches), cited by title and section:
  *   "KV Cache and BlockManager" (dpshk.com/news/5906718)            [BM]
@@ -340,6 +342,44 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
                                           const void *v_new, float scale, int32_t window,
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *err_word, pa_stream_t stream);
+
+/*
+ * int8 KV cache: quantised blocks with per-block scales.
+ *
+ * The sources name int8-quantised cache blocks ([BM] s6.3, and the
+ * "quantized" element size of the block-size rule in [BM] s3) without fixing
+ * a scheme.  The scheme of these two calls: a pool element is a code c in
+ * [-127, 127] (one byte) that stands for c * s, where s is the fp32 scale of
+ * its (physical block, kv head) for K, or for V:
+ *     kv_scales[(blk*2 + 0)*num_kv_heads + h]   scale of K in block blk, kv head h
+ *     kv_scales[(blk*2 + 1)*num_kv_heads + h]   scale of V
+ * (device fp32 [num_blocks][2][num_kv_heads], set by whoever allocates the
+ * block; scales must be positive and finite).  The pools keep the layout of
+ * the 16-bit pools above with one byte per element (block_stride counts
+ * bytes; it and head_dim must keep rows and blocks on 16-byte boundaries).
+ * shape->dtype is the element type of q, out, k_new and v_new; head_dim must
+ * be 64, 128 or 256.
+ *
+ * paged_kv_append_int8 writes k_new/v_new [B][Hkv][D] like paged_kv_append,
+ * each value x as clamp(round_half_even(x / s), -127, 127) with the quotient
+ * taken in IEEE binary32 (NaN -> 0), s the scale of the target block; the
+ * codes are exactly those of that rule.
+ *
+ * paged_attention_decode_int8 is paged_attention_decode over the values the
+ * codes stand for ([PG] s2.2): x_t = scale * s_K * <q, c_t>, weights w_t as
+ * there, out = sum_t w_t s_V c_t / sum_t w_t.  Same device checks, zeros and
+ * PA_DEVERR_* bits.  Both run on the CUDA cores for every head layout.
+ */
+pa_status paged_kv_append_int8(const pa_shape *shape, const void *k_new, const void *v_new,
+                               int8_t *k_pool, int8_t *v_pool, const float *kv_scales,
+                               const int32_t *block_table, const int32_t *positions,
+                               int32_t *err_word, pa_stream_t stream);
+
+pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const void *q,
+                                      const int8_t *k_pool, const int8_t *v_pool,
+                                      const float *kv_scales, const int32_t *block_table,
+                                      const int32_t *seq_lens, float scale, int32_t *err_word,
+                                      pa_stream_t stream);
 
 /*
  * paged_attention_decode_split_static -- the split-KV pair without any

@@ -1,0 +1,438 @@
+// decode_int8.cu -- the int8 KV cache: quantising append and decode attention.
+//
+// The pages name int8-quantised cache blocks ("KV Cache and BlockManager",
+// dpshk.com/news/5906718, s6.3; the "quantized" element size in its s3
+// block-size rule) but fix no scheme.  The one implemented: a cached K (or
+// V) element is a code c in [-127, 127] standing for c * s, with one fp32
+// scale s per (physical block, kv head) for K and one for V,
+//     kv_scales[(blk*2 + 0)*Hkv + hk]  (K)    kv_scales[(blk*2 + 1)*Hkv + hk]  (V),
+// and a value x is written as clamp(round_half_even(x / s), -127, 127) with
+// the quotient taken in IEEE binary32.  A pool holds one byte per element in
+// the 16-bit pools' layout, so a block's (kv head) chunk is block_size*D
+// contiguous bytes.
+//
+// Decode is the per-block decomposition of "KV Cache paging in LLM
+// inference" (intelliparadigm.com) s2.2 over the values the codes stand
+// for: one CTA per (sequence, query head), each warp streaming its own ring
+// of 4 KB K + 4 KB V tiles (twice the tokens of a 16-bit tile) with bulk
+// copies.  Scores are scale_K(block) * <q, codes>, and the softmax weight of
+// a token is multiplied by scale_V(block) before it meets the V codes; both
+// scales of every block of the sequence are staged in shared memory next to
+// its block-table row.
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "simt_tile.cuh"
+
+namespace pa {
+
+constexpr int kI8Warps = 4;
+constexpr int kI8Stages = 2;
+constexpr int kI8TableCap = 1024;   // table entries (and scales) staged per CTA
+
+// Tile geometry for int8 rows of D bytes (same roles as SimtCfg).
+template <int D>
+struct I8Cfg {
+    static constexpr int ROWB = D;                 // bytes per token row
+    static constexpr int VEC = 16;                 // codes per 16-byte load
+    static constexpr int LPT = ROWB / 16;          // lanes per token row
+    static constexpr int RPW = 32 / LPT;           // rows per warp instruction
+    static constexpr int TILE = kTileBytes / ROWB; // tokens per tile
+    static constexpr int NVALS = TILE / RPW;       // rows per lane per tile
+    static constexpr int NFIN = NVALS >= LPT ? NVALS / LPT : 1;
+    static constexpr int LOG_LPT = LPT == 4 ? 2 : LPT == 8 ? 3 : LPT == 16 ? 4 : 5;
+    static constexpr int LOG_NVALS = 3;
+    static_assert(LPT == 4 || LPT == 8 || LPT == 16, "int8 rows must be 64..256 bytes");
+    static_assert(NVALS == 8, "tile holds 8 rows per lane");
+};
+
+template <int D>
+struct I8Smem {
+    using C = I8Cfg<D>;
+    static constexpr size_t kStages = (size_t)kI8Warps * kI8Stages * 2 * kTileBytes;
+    static constexpr size_t kBars = (size_t)kI8Warps * kI8Stages * 8;
+    static constexpr size_t kP = (size_t)kI8Warps * C::TILE * 4 * 2;   // weights, and weights * scale_V
+    static constexpr size_t kRed = (size_t)kI8Warps * (D + 2) * 4;
+    static constexpr size_t kFlags = 16;
+    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags;
+    static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 12; }   // ids, scale_K, scale_V
+};
+
+// 16 int8 codes -> 8 float pairs, exactly: each byte (biased to 0..255) is
+// placed in the mantissa of 2^23 by a byte permute, and 2^23 + 128 is
+// subtracted.
+__device__ __forceinline__ void codes_to_float2(const uint4 &v, float2 *f) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 lo = make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)),
+                                      __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541)));
+        const float2 hi = make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)),
+                                      __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543)));
+        f[2 * i] = __fadd2_rn(lo, bias);
+        f[2 * i + 1] = __fadd2_rn(hi, bias);
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
+    grid_dependency_wait();
+    allow_dependents();
+    using C = I8Cfg<D>;
+    using L = I8Smem<D>;
+    constexpr int S = kI8Stages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kStages);
+    float *pbuf = reinterpret_cast<float *>(smem + L::kStages + L::kBars);
+    float *red_m = reinterpret_cast<float *>(smem + L::kStages + L::kBars + L::kP);
+    float *red_l = red_m + kI8Warps;
+    float *red_acc = red_l + kI8Warps;
+    int *flags = reinterpret_cast<int *>(smem + L::kStages + L::kBars + L::kP + L::kRed);
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kFixed);
+    float *sk_tab = reinterpret_cast<float *>(tbl + p.table_cap);
+    float *sv_tab = sk_tab + p.table_cap;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x % p.B;
+    const int h = blockIdx.x / p.B;
+    const int hk = h / (p.H / p.Hkv);
+    const int64_t bh = (int64_t)b * p.H + h;
+    T *out = reinterpret_cast<T *>(p.out);
+    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
+
+    const int32_t len = p.seq_lens[b];
+    if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
+        if (threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+        for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
+        return;
+    }
+    if (len == 0) {
+        for (int d = threadIdx.x; d < D; d += blockDim.x) out[bh * D + d] = Elem<T>::from_float(0.f);
+        return;
+    }
+    auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
+    const int nblk = (len - 1) / p.bs + 1;
+    const int ncache = min(nblk, p.table_cap);
+    for (int j = threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j];
+    if (threadIdx.x == 0) flags[0] = 0;
+    if (threadIdx.x < kI8Warps * S) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
+    mbar_init_fence();
+    __syncthreads();
+    // the scales of the staged blocks (0 for an entry outside the pool: the
+    // copy of such a block is refused and the output zeroed)
+    for (int j = threadIdx.x; j < ncache; j += blockDim.x) {
+        const int32_t blk = tbl[j];
+        sk_tab[j] = good(blk) ? kv_scales[((int64_t)blk * 2 + 0) * p.Hkv + hk] : 0.f;
+        sv_tab[j] = good(blk) ? kv_scales[((int64_t)blk * 2 + 1) * p.Hkv + hk] : 0.f;
+    }
+    __syncthreads();
+
+    const int ntiles = (len + C::TILE - 1) / C::TILE;
+    const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kI8Warps + 1 : 0;
+    const int r = lane / C::LPT;   // row group
+    const int c = lane % C::LPT;   // 16-byte column
+    const int64_t head_off = (int64_t)hk * p.bs * C::ROWB;
+    auto lookup = [&](int j) -> int32_t { return j < ncache ? tbl[j] : trow[j]; };
+    auto blk_of = [&](int t) { return p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs; };
+    auto scale_of = [&](int j, int kv) -> float {
+        if (j < ncache) return kv ? sv_tab[j] : sk_tab[j];
+        const int32_t blk = trow[j];
+        return good(blk) ? kv_scales[((int64_t)blk * 2 + kv) * p.Hkv + hk] : 0.f;
+    };
+
+    // lane 0 of the warp fetches local tile k into ring slot k % S
+    auto issue = [&](int k) {
+        const int t0 = (warp + k * kI8Warps) * C::TILE;
+        const int t1 = min(t0 + C::TILE, len);
+        const int slot = k % S;
+        const uint32_t dst_k = smem_u32(stages + (size_t)((warp * S + slot) * 2) * kTileBytes);
+        const uint32_t dst_v = dst_k + kTileBytes;
+        const uint32_t bar = smem_u32(&bars[warp * S + slot]);
+        uint32_t bytes = 0;
+        bool ok = true;
+        for (int t = t0, jj = blk_of(t0), e; t < t1; t = e, ++jj) {
+            e = min(t1, (jj + 1) * p.bs);
+            if (good(lookup(jj))) bytes += (uint32_t)(e - t) * C::ROWB * 2;
+            else ok = false;
+        }
+        if (!ok) {
+            flags[0] = 1;
+            report(p.err_word, PA_DEVERR_BAD_BLOCK);
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int t = t0, jj = blk_of(t0), e; t < t1; t = e, ++jj) {
+            e = min(t1, (jj + 1) * p.bs);
+            const int32_t blk = lookup(jj);
+            if (!good(blk)) continue;
+            const int64_t off = (int64_t)blk * p.block_stride_bytes + head_off + (int64_t)(t - jj * p.bs) * C::ROWB;
+            const uint32_t n = (uint32_t)(e - t) * C::ROWB;
+            const uint32_t so = (uint32_t)(t - t0) * C::ROWB;
+            bulk_g2s(dst_k + so, p.k_pool + off, n, bar);
+            bulk_g2s(dst_v + so, p.v_pool + off, n, bar);
+        }
+    };
+
+    // this lane's 16 query elements, in fp32 pairs
+    float2 q2[C::VEC / 2];
+    {
+        const T *qrow = reinterpret_cast<const T *>(p.q) + bh * D + c * C::VEC;
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e)
+            q2[e] = make_float2(Elem<T>::to_float(qrow[2 * e]), Elem<T>::to_float(qrow[2 * e + 1]));
+    }
+
+    if (lane == 0)
+        for (int k = 0; k < min(S, my_tiles); ++k) issue(k);
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float2 acc2[C::VEC / 2];
+#pragma unroll
+    for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = make_float2(0.f, 0.f);
+    float *pw = pbuf + warp * C::TILE * 2;   // [row group][value]: weights, then weights * scale_V
+    float *pws = pw + C::TILE;
+
+    int k = 0;
+    bool aborted = false;
+    for (; k < my_tiles; ++k) {
+        const int slot = k % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[warp * S + slot]), (k / S) & 1))) {
+            aborted = true;
+            break;
+        }
+        const unsigned char *ks = stages + (size_t)((warp * S + slot) * 2) * kTileBytes;
+        const unsigned char *vs = ks + kTileBytes;
+        const int t0 = (warp + k * kI8Warps) * C::TILE;
+        const int nrows = min(C::TILE, len - t0);
+
+        // scores: partial dot products of 8 rows, then the butterfly
+        float v[C::NVALS];
+#pragma unroll
+        for (int j = 0; j < C::NVALS; ++j) {
+            const uint4 kv = *reinterpret_cast<const uint4 *>(ks + (j * C::RPW + r) * C::ROWB + c * 16);
+            float2 k2[C::VEC / 2];
+            codes_to_float2(kv, k2);
+            float2 a = __fmul2_rn(q2[0], k2[0]);
+#pragma unroll
+            for (int e = 1; e < C::VEC / 2; ++e) a = __ffma2_rn(q2[e], k2[e], a);
+            v[j] = a.x + a.y;
+        }
+        Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
+
+        float sc[C::NFIN];
+        int jrow[C::NFIN];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int kk = 0; kk < C::NFIN; ++kk) {
+            const int row = row_of_value<C>(c, kk) * C::RPW + r;
+            jrow[kk] = blk_of(t0 + min(row, nrows - 1));
+            sc[kk] = row < nrows ? v[kk] * scale_of(jrow[kk], 0) * p.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, sc[kk]);
+        }
+        tmax = warp_max_f32(tmax);
+        const float m_new = fmaxf(m_run, tmax);
+        const float corr = ex2_approx(m_run - m_new);
+#pragma unroll
+        for (int kk = 0; kk < C::NFIN; ++kk) {
+            const float pr = ex2_approx(sc[kk] - m_new);
+            pw[r * C::NVALS + row_of_value<C>(c, kk)] = pr;
+            pws[r * C::NVALS + row_of_value<C>(c, kk)] = pr * scale_of(jrow[kk], 1);
+        }
+        __syncwarp();
+        float pj[C::NVALS], pjs[C::NVALS];
+#pragma unroll
+        for (int j = 0; j < C::NVALS; j += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(pw + r * C::NVALS + j);
+            const float4 g = *reinterpret_cast<const float4 *>(pws + r * C::NVALS + j);
+            pj[j] = f.x; pj[j + 1] = f.y; pj[j + 2] = f.z; pj[j + 3] = f.w;
+            pjs[j] = g.x; pjs[j + 1] = g.y; pjs[j + 2] = g.z; pjs[j + 3] = g.w;
+        }
+        const float2 corr2 = make_float2(corr, corr);
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __fmul2_rn(acc2[e], corr2);
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < C::NVALS; ++j) {
+            // rows past the valid length were never fetched: skip them
+            if (j * C::RPW + r < nrows) {
+                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
+                float2 v2[C::VEC / 2];
+                codes_to_float2(vv, v2);
+                const float2 p2 = make_float2(pjs[j], pjs[j]);
+#pragma unroll
+                for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
+                psum += pj[j];
+            }
+        }
+        l_run = fmaf(l_run, corr, psum);
+        m_run = m_new;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && k + S < my_tiles) issue(k + S);
+    }
+    if (aborted) {
+        if (lane == 0) {
+            flags[0] = 1;
+            report(p.err_word, PA_DEVERR_TIMEOUT);
+        }
+        for (int kk = k; kk < min(my_tiles, k + S); ++kk)
+            mbar_wait(smem_u32(&bars[warp * S + kk % S]), (kk / S) & 1);
+    }
+
+    // combine the row groups of the warp, then the warps of the CTA
+#pragma unroll
+    for (int o = C::LPT; o < 32; o <<= 1) {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e) {
+            acc2[e].x += __shfl_xor_sync(0xffffffffu, acc2[e].x, o);
+            acc2[e].y += __shfl_xor_sync(0xffffffffu, acc2[e].y, o);
+        }
+    }
+    if (lane < C::LPT) {
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e) {
+            red_acc[warp * D + lane * C::VEC + 2 * e] = acc2[e].x;
+            red_acc[warp * D + lane * C::VEC + 2 * e + 1] = acc2[e].y;
+        }
+    }
+    if (lane == 0) {
+        red_m[warp] = m_run;
+        red_l[warp] = l_run;
+    }
+    __syncthreads();
+    const bool bad = flags[0] != 0;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kI8Warps; ++w) M = fmaxf(M, red_m[w]);
+    float wsc[kI8Warps];
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kI8Warps; ++w) {
+        wsc[w] = merge_weight(red_m[w], M);
+        lsum = fmaf(red_l[w], wsc[w], lsum);
+    }
+    const float inv = 1.f / lsum;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kI8Warps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
+        out[bh * D + d] = Elem<T>::from_float(bad ? 0.f : a * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// quantising append: one thread per 16 codes of a new row
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_int8_kernel(AppendParams p, const float *kv_scales, int D) {
+    grid_dependency_wait();
+    allow_dependents();
+    const int vecs = D / 16;
+    const int64_t total = (int64_t)p.B * p.Hkv * 2 * vecs;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int v = (int)(i % vecs);
+    int64_t rest = i / vecs;
+    const int kv = (int)(rest % 2);
+    rest /= 2;
+    const int h = (int)(rest % p.Hkv);
+    const int b = (int)(rest / p.Hkv);
+    const bool reporter = (v == 0 && kv == 0 && h == 0);
+
+    const int32_t pos = p.positions[b];
+    if (pos < 0 || (int64_t)pos >= (int64_t)p.MB * p.bs) {
+        if (reporter) report(p.err_word, PA_DEVERR_BAD_POS);
+        return;
+    }
+    const int32_t blk = p.block_table[(int64_t)b * p.MB + pos / p.bs];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        if (reporter) report(p.err_word, PA_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const float s = kv_scales[((int64_t)blk * 2 + kv) * p.Hkv + h];
+    const T *src = reinterpret_cast<const T *>(kv ? p.v_new : p.k_new) + ((int64_t)b * p.Hkv + h) * D + v * 16;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            // binary32 quotient, nearest integer with ties to even (NaN -> 0),
+            // clamped to the symmetric code range
+            int c = __float2int_rn(__fdiv_rn(Elem<T>::to_float(src[q * 4 + e]), s));
+            c = max(-127, min(127, c));
+            word |= (uint32_t)(c & 0xff) << (8 * e);
+        }
+        w[q] = word;
+    }
+    const int64_t dst = (int64_t)blk * p.block_stride_bytes + ((int64_t)h * p.bs + pos % p.bs) * D + v * 16;
+    *reinterpret_cast<uint4 *>((kv ? p.v_pool : p.k_pool) + dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+template <typename T, int D>
+static cudaError_t launch_int8_t(const DecodeParams &params, const float *kv_scales, cudaStream_t stream) {
+    DecodeParams p = params;
+    p.table_cap = min(p.table_cap, kI8TableCap);
+    const size_t smem = I8Smem<D>::bytes(p.table_cap);
+    auto kern = decode_int8_kernel<T, D>;
+    static int configured[64] = {};   // per template instance of this launcher
+    cudaError_t e = ensure_smem_limit(kern, smem, configured);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)p.B * p.H;
+    if (grid == 0) return cudaSuccess;
+    return launch_clustered(kern, grid, kI8Warps * 32, smem, 1, stream, p, kv_scales);
+}
+
+template <typename T>
+static cudaError_t launch_int8_d(const DecodeParams &p, const float *kv_scales, cudaStream_t stream) {
+    switch (p.D) {
+        case 64: return launch_int8_t<T, 64>(p, kv_scales, stream);
+        case 128: return launch_int8_t<T, 128>(p, kv_scales, stream);
+        case 256: return launch_int8_t<T, 256>(p, kv_scales, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool int8_supported(int dtype, int head_dim) {
+    return (dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16) &&
+           (head_dim == 64 || head_dim == 128 || head_dim == 256);
+}
+
+cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv_scales,
+                               cudaStream_t stream) {
+    switch (dtype) {
+        case PA_F32: return launch_int8_d<float>(p, kv_scales, stream);
+        case PA_F16: return launch_int8_d<__half>(p, kv_scales, stream);
+        case PA_BF16: return launch_int8_d<__nv_bfloat16>(p, kv_scales, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv_scales, int head_dim,
+                               cudaStream_t stream) {
+    const int64_t total = (int64_t)p.B * p.Hkv * 2 * (head_dim / 16);
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    switch (dtype) {
+        case PA_F32:
+            return launch_clustered(append_int8_kernel<float>, blocks, threads, 0, 1, stream, p, kv_scales, head_dim);
+        case PA_F16:
+            return launch_clustered(append_int8_kernel<__half>, blocks, threads, 0, 1, stream, p, kv_scales, head_dim);
+        case PA_BF16:
+            return launch_clustered(append_int8_kernel<__nv_bfloat16>, blocks, threads, 0, 1, stream, p, kv_scales,
+                                    head_dim);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

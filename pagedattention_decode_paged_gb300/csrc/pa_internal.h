@@ -191,6 +191,14 @@ bool gqa_tc_supported(int dtype, int head_dim);
 
 cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream);
 
+// int8 KV cache (pools of codes, fp32 scales [NB][2][Hkv]); `dtype` is the
+// element type of q/out (decode) or k_new/v_new (append).
+bool int8_supported(int dtype, int head_dim);
+cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv_scales,
+                               cudaStream_t stream);
+cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv_scales,
+                               int head_dim, cudaStream_t stream);
+
 // Load-balanced persistent decode (final mode; plain, fused append or sliding
 // window as DecodeParams says).  A plan fixes the grid for a shape on the
 // current device; the workspace holds 2 * grid * kBalWarps records of

@@ -182,6 +182,28 @@ def test_balanced_rejects_bad_arguments(lib):
     assert pa.paged_attention_balanced_workspace(base_shape(batch=0)) == 0
 
 
+def test_int8_rejects_bad_arguments(lib):
+    s8 = base_shape(block_stride=2 * 2 * 16 * 128)   # bytes: one per element
+    dec = lib.paged_attention_decode_int8
+    app = lib.paged_kv_append_int8
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # out, q, k_pool, v_pool, scales, table, lens
+    assert dec(None, *ok, 0.1, None, None) == pa.PA_ERR_INVALID_ARG
+    assert dec(ctypes.byref(base_shape(head_dim=32, block_stride=2 * 2 * 16 * 32)), *ok, 0.1, None, None) \
+        == pa.PA_ERR_UNSUPPORTED
+    assert dec(ctypes.byref(base_shape(block_stride=2 * 2 * 16 * 128 + 8)), *ok, 0.1, None, None) \
+        == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), *ok[:4], None, *ok[5:], 0.1, None, None) == pa.PA_ERR_INVALID_ARG
+    assert dec(ctypes.byref(s8), *ok[:4], FAKE + 2, *ok[5:], 0.1, None, None) == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), FAKE, FAKE, FAKE + 8, *ok[3:], 0.1, None, None) == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), *ok, float("inf"), None, None) == pa.PA_ERR_INVALID_ARG
+    assert dec(ctypes.byref(base_shape(batch=0)), *ok, 0.1, None, None) == pa.PA_OK
+    ok_a = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)  # k_new, v_new, k_pool, v_pool, scales, table, pos
+    assert app(ctypes.byref(s8), *ok_a[:4], None, *ok_a[5:], None, None) == pa.PA_ERR_INVALID_ARG
+    assert app(ctypes.byref(s8), *ok_a[:2], FAKE + 4, *ok_a[3:], None, None) == pa.PA_ERR_MISALIGNED
+    assert app(ctypes.byref(base_shape(head_dim=96, block_stride=2 * 2 * 16 * 96)), *ok_a, None, None) \
+        == pa.PA_ERR_UNSUPPORTED
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
     monkeypatch.setattr(pa, "_lib", None)

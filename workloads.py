@@ -337,3 +337,62 @@ def with_long_sequence(w: Workload, length: int, *, seed: int = 7, device="cpu")
     return make_generic(B=w.B, H=w.H, Hkv=w.Hkv, D=w.D, bs=w.bs, dtype=w.dtype, lens=lens,
                         seed=seed, device=device, poison=False,
                         name=f"{w.name}+1x{length}")
+
+
+@dataclass
+class Int8Workload:
+    """An int8 cache in the layout of `Workload`: pool [NB][2][Hkv][bs][D] of
+    codes, scales [NB][2][Hkv] fp32 (K, V per block and kv head), q and the
+    new rows in `dtype`."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    D: int
+    bs: int
+    NB: int
+    MB: int
+    dtype: torch.dtype
+    lens: torch.Tensor
+    block_table: torch.Tensor
+    pool: torch.Tensor
+    scales: torch.Tensor
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    scale: float
+    meta: dict
+
+    @property
+    def block_stride(self) -> int:
+        return 2 * self.Hkv * self.bs * self.D
+
+    @property
+    def v_offset(self) -> int:
+        return self.Hkv * self.bs * self.D
+
+    def k_flat(self) -> torch.Tensor:
+        return self.pool.view(-1)
+
+    def v_flat(self) -> torch.Tensor:
+        return self.pool.view(-1)[self.v_offset:]
+
+    def to(self, device) -> "Int8Workload":
+        moved = {k: (v.to(device) if isinstance(v, torch.Tensor) else v)
+                 for k, v in self.__dict__.items()}
+        return Int8Workload(**moved)
+
+
+def to_int8(w: Workload, *, seed: int = 17, scale_range=(0.004, 0.012)) -> Int8Workload:
+    """The int8 counterpart of workload `w` (same shape, table, lengths, q
+    and new rows): seeded uniform codes in [-127, 127] and per-(block, K|V,
+    kv head) scales drawn uniformly from scale_range, so the values the
+    codes stand for have a spread comparable to N(0, 1) data."""
+    gen = torch.Generator().manual_seed(seed)
+    pool = torch.randint(-127, 128, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.int8)
+    lo, hi = scale_range
+    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32) * (hi - lo) + lo)
+    cpu = lambda t: t.cpu() if isinstance(t, torch.Tensor) else t
+    return Int8Workload(w.name + "-int8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
+                        cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
+                        cpu(w.v_new), w.scale, dict(w.meta, int8_seed=seed))
