@@ -44,12 +44,14 @@ import workloads  # noqa: E402
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); attention tokens/s"
 UNIT = "GB/s"
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
-SPLIT_PTOK = {5: 1024}          # workloads timed through the split-KV pair
+SPLIT_PTOK = {5: 2048}          # workloads timed through split-KV partitions
+SHARED_PREFIX = {5}             # ... with the shared prefix read once per group
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
                   "decode_simt_balanced": "decode_balanced_simt.cu",
                   "decode_tc_balanced": "decode_balanced_tc.cu",
                   "decode_int8": "decode_int8.cu",
+                  "decode_prefix_tc": "decode_prefix_tc.cu",
                   "append_tokens": "append.cu"}
 
 
@@ -301,6 +303,18 @@ def run_gpu(args) -> None:
     bws = None
     if args.int8:
         ptok = None
+    groups = None
+    if args.shared_prefix is None:
+        args.shared_prefix = args.workload in SHARED_PREFIX and not args.int8 and not args.balanced \
+            and not args.long_seq and not args.prefill and not window
+    if args.shared_prefix:
+        if "shared_blocks" not in w.meta:
+            raise SystemExit("--shared-prefix needs a workload with a shared prefix (workload 5)")
+        groups = {"first": [0, w.B], "shared": [w.meta["shared_blocks"] * w.bs]}
+        ptok = ptok or 2048
+        ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
+        fused = False
+        kernel = "decode_prefix_tc"
     if balanced:
         ptok = None
         fused = not args.unfused
@@ -335,6 +349,13 @@ def run_gpu(args) -> None:
             calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
                               w.block_table, prefill["start"], w.lens, **kw))
             return calls, []
+        if args.shared_prefix:
+            calls.append(bind(pa.paged_attention_decode_shared_prefix, out, w.q, kflat, vflat,
+                              w.block_table, lens_after, w.scale, ptok, ws,
+                              group_first=groups["first"], shared_tokens=groups["shared"],
+                              num_kv_heads=w.Hkv, **kw))
+            return calls, [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table,
+                                positions, **kw)]
         if args.int8:
             calls.append(bind(pa.paged_attention_decode_int8, out, w.q, kflat, vflat, w.scales,
                               w.block_table, lens_after, w.scale, num_kv_heads=w.Hkv, **kw))
@@ -649,6 +670,9 @@ def main() -> None:
                     help="capture this many steps into one CUDA graph and replay it")
     ap.add_argument("--long-seq", type=int, default=0,
                     help="replace the last sequence by one of this many tokens (skewed batch)")
+    ap.add_argument("--shared-prefix", action=argparse.BooleanOptionalAction, default=None,
+                    help="paged_attention_decode_shared_prefix (shared blocks read once per "
+                         "group; the default for workload 5)")
     ap.add_argument("--int8", action="store_true",
                     help="int8 cache with per-block scales (paged_kv_append_int8 + "
                          "paged_attention_decode_int8)")

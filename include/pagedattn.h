@@ -116,6 +116,7 @@ typedef enum pa_dtype {
 #define PA_DEVERR_BAD_BLOCK 2  /* a needed table entry is outside [0, num_blocks) */
 #define PA_DEVERR_BAD_POS   4  /* append position outside the table row         */
 #define PA_DEVERR_TIMEOUT   8  /* a bounded wait for a copy gave up              */
+#define PA_DEVERR_BAD_PREFIX 16 /* a declared shared prefix is not shared/held   */
 
 typedef struct pa_shape {
     int32_t batch;              /* sequences B (0 is allowed: nothing to do) */
@@ -293,6 +294,45 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
                                         const void *workspace, size_t workspace_bytes,
                                         const int32_t *seq_lens, int32_t partition_tokens,
                                         int32_t *err_word, pa_stream_t stream);
+
+/*
+ * paged_attention_decode_shared_prefix -- the split-KV pair for groups of
+ * sequences that share a prefix, reading the shared blocks once per group.
+ *
+ * Sequences forked from one prompt (beam search, parallel sampling) name the
+ * same physical blocks for their common prefix ([KB] s3.4: blocks shared by
+ * reference count instead of copied).  Group i is the run of sequences
+ * [group_first[i], group_first[i+1]) whose table rows agree on the blocks
+ * holding their first shared_tokens[i] tokens (group_first and
+ * shared_tokens are HOST arrays of num_groups + 1 and num_groups entries;
+ * group_first ascends strictly, at most 16 groups; a group whose
+ * shared_tokens is below partition_tokens shares nothing and may be any
+ * size, the others need members x H/Hkv <= 16).
+ * For each group and kv head, the partitions of partition_tokens tokens that
+ * lie wholly inside the shared prefix are read once and attended by every
+ * member's queries at once (tensor cores; the members are the MMA columns);
+ * all other partitions are computed per sequence, and the log-sum-exp reduce
+ * merges them.  The result is paged_attention_decode's, up to rounding
+ * order; it equals the partial + reduce pair's output formula.
+ *
+ * Device checks: as paged_attention_decode; in addition, a member whose
+ * table differs from the group's first member inside a shared partition, or
+ * whose length does not cover it, gets zeros and PA_DEVERR_BAD_PREFIX.
+ * Workspace: exactly that of the partial/reduce pair
+ * (paged_attention_partial_workspace).  Shapes: those of the tensor-core
+ * path (paged_attention_decode_path() == PA_PATH_TENSOR_GQA, or the same
+ * conditions with num_heads == num_kv_heads); others give
+ * PA_ERR_UNSUPPORTED.  Three launches on `stream`.
+ */
+pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out, const void *q,
+                                               const void *k_pool, const void *v_pool,
+                                               const int32_t *block_table,
+                                               const int32_t *seq_lens, int32_t num_groups,
+                                               const int32_t *group_first,
+                                               const int32_t *shared_tokens, float scale,
+                                               int32_t partition_tokens, void *workspace,
+                                               size_t workspace_bytes, int32_t *err_word,
+                                               pa_stream_t stream);
 
 /*
  * paged_attention_decode_balanced -- one decode step under a load-balanced,

@@ -29,7 +29,7 @@ LIB_PATH = _PKG / "_lib" / "libpagedattn.so"
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_PATH_INVALID, PA_PATH_SIMT, PA_PATH_TENSOR_GQA = 0, 1, 2
-DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT, DEVERR_BAD_PREFIX = 1, 2, 4, 8, 16
 
 EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attention_decode",
             "paged_attention_decode_append", "paged_attention_decode_split_static",
@@ -37,7 +37,8 @@ EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attentio
             "paged_attention_decode_path", "paged_attention_partial_workspace",
             "paged_attention_decode_partial", "paged_attention_decode_reduce",
             "paged_attention_balanced_workspace", "paged_attention_decode_balanced",
-            "paged_kv_append_int8", "paged_attention_decode_int8")
+            "paged_kv_append_int8", "paged_attention_decode_int8",
+            "paged_attention_decode_shared_prefix")
 
 
 class PagedAttnError(RuntimeError):
@@ -95,6 +96,9 @@ def load() -> ctypes.CDLL:
                                                            vp, vp]
             lib.paged_attention_decode_reduce.restype = ctypes.c_int
             lib.paged_attention_decode_reduce.argtypes = [sp, vp, vp, sz, vp, i32, vp, vp]
+            lib.paged_attention_decode_shared_prefix.restype = ctypes.c_int
+            lib.paged_attention_decode_shared_prefix.argtypes = [sp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
+                                                                 f32, i32, vp, sz, vp, vp]
             lib.paged_kv_append_int8.restype = ctypes.c_int
             lib.paged_kv_append_int8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.paged_attention_decode_int8.restype = ctypes.c_int
@@ -361,3 +365,24 @@ def paged_attention_decode_int8(out, q, k_pool, v_pool, kv_scales, block_table, 
             _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(err_word), _stream(stream))
     return _issue(load().paged_attention_decode_int8, args, "paged_attention_decode_int8", prepare,
                   (shape,))
+
+
+def paged_attention_decode_shared_prefix(out, q, k_pool, v_pool, block_table, seq_lens, scale,
+                                         partition_tokens, workspace, *, group_first, shared_tokens,
+                                         num_kv_heads, block_size, num_blocks, block_stride,
+                                         err_word=None, stream=None, prepare=False):
+    """Split-KV decode where each group of sequences [group_first[i],
+    group_first[i+1]) shares the blocks of its first shared_tokens[i] tokens:
+    those partitions are read once per group (host lists)."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    n = len(shared_tokens)
+    first = (ctypes.c_int32 * (n + 1))(*[int(x) for x in group_first])
+    shared = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in shared_tokens])
+    nbytes = workspace.numel() * workspace.element_size()
+    args = (ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+            _ptr(seq_lens), n, ctypes.cast(first, ctypes.c_void_p), ctypes.cast(shared, ctypes.c_void_p),
+            float(scale), int(partition_tokens), _ptr(workspace), nbytes, _ptr(err_word),
+            _stream(stream))
+    return _issue(load().paged_attention_decode_shared_prefix, args,
+                  "paged_attention_decode_shared_prefix", prepare, (shape, first, shared))

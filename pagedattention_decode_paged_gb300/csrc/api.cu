@@ -59,15 +59,20 @@ EncodeTiledFn encode_fn() {
 
 int box_rows_for(const pa_shape *s) { return s->block_size % 16 == 0 ? 16 : 8; }
 
-bool tc_eligible(const pa_shape *s) {
+// The tensor-core tile path can read this pool (16-bit, D 64/128, boxes of
+// 8 or 16 rows inside a block, row coordinates in int32).
+bool tc_layout_ok(const pa_shape *s) {
     if (!pa::gqa_tc_supported(s->dtype, s->head_dim)) return false;
-    if (s->num_heads / s->num_kv_heads < 2) return false;
     if (!(s->block_size % 16 == 0 || s->block_size == 8)) return false;
     if (s->block_stride % s->head_dim != 0) return false;
     const int64_t rows_per_block = s->block_stride / s->head_dim;
     // TMA row coordinates are signed 32-bit
     if (s->num_blocks * rows_per_block > (int64_t)INT32_MAX) return false;
     return true;
+}
+
+bool tc_eligible(const pa_shape *s) {
+    return s->num_heads / s->num_kv_heads >= 2 && tc_layout_ok(s);
 }
 
 // View a pool as a [rows][head_dim] matrix; boxes of 64 x box_rows elements,
@@ -562,6 +567,86 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
         e = pa::launch_balanced_simt(shape->dtype, p, plan, s);
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out, const void *q,
+                                               const void *k_pool, const void *v_pool,
+                                               const int32_t *block_table,
+                                               const int32_t *seq_lens, int32_t num_groups,
+                                               const int32_t *group_first,
+                                               const int32_t *shared_tokens, float scale,
+                                               int32_t partition_tokens, void *workspace,
+                                               size_t workspace_bytes, int32_t *err_word,
+                                               pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK) return st;
+    if (partition_tokens <= 0 || partition_tokens % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_groups < 0 || num_groups > pa::kMaxPrefixGroups) return PA_ERR_INVALID_ARG;
+    if (num_groups > 0 && (group_first == nullptr || shared_tokens == nullptr)) return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    if (!tc_layout_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (out == nullptr || workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(workspace)) return PA_ERR_MISALIGNED;
+    const int64_t P = num_partitions(shape, partition_tokens);
+    if (P > kMaxPartitions || (int64_t)shape->batch * shape->num_heads * P > INT32_MAX)
+        return PA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(shape, P);
+    if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+    const int g = shape->num_heads / shape->num_kv_heads;
+    pa::PrefixGroups groups{};
+    groups.n = num_groups;
+    int widest = 0;
+    const int64_t row_tokens = (int64_t)shape->max_blocks_per_seq * shape->block_size;
+    for (int i = 0; i < num_groups; ++i) {
+        const int32_t a = group_first[i], e = group_first[i + 1];
+        if (a < 0 || e <= a || e > shape->batch) return PA_ERR_INVALID_ARG;
+        if (shared_tokens[i] < 0 || shared_tokens[i] > row_tokens) return PA_ERR_INVALID_ARG;
+        groups.first[i] = a;
+        groups.parts[i] = shared_tokens[i] / partition_tokens;
+        if (groups.parts[i] == 0) continue;   // a run that shares no whole partition
+        if ((e - a) * g > 16) return PA_ERR_UNSUPPORTED;
+        widest = (e - a) * g > widest ? (e - a) * g : widest;
+    }
+    if (num_groups > 0) groups.first[num_groups] = group_first[num_groups];
+
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    char *ws = static_cast<char *>(workspace);
+    p.ws_m = reinterpret_cast<float *>(ws + w.off_m);
+    p.ws_l = reinterpret_cast<float *>(ws + w.off_l);
+    p.ws_acc = reinterpret_cast<float *>(ws + w.off_acc);
+    p.partition_tokens = partition_tokens;
+    p.num_partitions = (int32_t)P;
+    const int64_t need = partition_tokens / shape->block_size + 2;
+    p.table_cap = (int)(need < kTableCap ? need : kTableCap);
+    p.groups = groups;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // 1. the shared partitions, once per group
+    CUtensorMap kmap, vmap;
+    if (!cached_pool_map(&kmap, shape, k_pool) || !cached_pool_map(&vmap, shape, v_pool)) return PA_ERR_CUDA;
+    if (pa::launch_prefix_tc(shape->dtype, p, kmap, vmap, box_rows_for(shape), widest, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // 2. every other partition, per sequence
+    st = launch_decode(shape, p, true, s);
+    if (st != PA_OK) return st;
+    // 3. the merge
+    pa::ReduceParams r{};
+    r.out = out;
+    r.ws_m = p.ws_m;
+    r.ws_l = p.ws_l;
+    r.ws_acc = p.ws_acc;
+    r.seq_lens = seq_lens;
+    r.err_word = err_word;
+    r.B = shape->batch;
+    r.H = shape->num_heads;
+    r.D = shape->head_dim;
+    r.MB = shape->max_blocks_per_seq;
+    r.bs = shape->block_size;
+    r.partition_tokens = partition_tokens;
+    r.num_partitions = (int32_t)P;
+    return pa::launch_reduce(shape->dtype, r, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

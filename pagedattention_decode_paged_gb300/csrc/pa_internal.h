@@ -10,6 +10,24 @@
 
 namespace pa {
 
+// Groups of consecutive sequences whose first partitions lie in blocks they
+// all share (split mode): group i holds sequences [first[i], first[i+1]) and
+// its first parts[i] partitions are computed once for all members by the
+// shared-prefix kernel; the per-sequence partial kernels skip them.
+constexpr int kMaxPrefixGroups = 16;
+struct PrefixGroups {
+    int32_t n;                               // 0: no groups
+    int32_t first[kMaxPrefixGroups + 1];
+    int32_t parts[kMaxPrefixGroups];
+};
+
+// Partitions [0, n) of sequence b that a shared-prefix group computes.
+__host__ __device__ inline int32_t prefix_parts_of(const PrefixGroups &g, int b) {
+    for (int i = 0; i < g.n; ++i)
+        if (b >= g.first[i] && b < g.first[i + 1]) return g.parts[i];
+    return 0;
+}
+
 // Everything a decode kernel needs, passed by value (fits the 4 KB parameter
 // space together with the tensor maps of the tensor-core path).
 struct DecodeParams {
@@ -49,6 +67,7 @@ struct DecodeParams {
     float *records;
     int32_t *counters;
     int32_t rec_floats;
+    PrefixGroups groups;       // split mode: partitions computed by the shared-prefix kernel
 };
 
 struct AppendParams {
@@ -190,6 +209,13 @@ cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtenso
 bool gqa_tc_supported(int dtype, int head_dim);
 
 cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream);
+
+// Shared-prefix partials (split mode, tensor-core shapes): one CTA per
+// (group, kv head, shared partition) writes the workspace slots of every
+// member sequence.  `members_times_group` = largest group size x H/Hkv.
+cudaError_t launch_prefix_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, int box_rows, int members_times_group,
+                             cudaStream_t stream);
 
 // int8 KV cache (pools of codes, fp32 scales [NB][2][Hkv]); `dtype` is the
 // element type of q/out (decode) or k_new/v_new (append).

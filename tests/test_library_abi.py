@@ -204,6 +204,32 @@ def test_int8_rejects_bad_arguments(lib):
         == pa.PA_ERR_UNSUPPORTED
 
 
+def test_shared_prefix_rejects_bad_arguments(lib):
+    f = lib.paged_attention_decode_shared_prefix
+    s = base_shape()
+    need = pa.paged_attention_partial_workspace(s, 32)
+    first = (ctypes.c_int32 * 3)(0, 1, 2)
+    shared = (ctypes.c_int32 * 2)(32, 0)
+    io = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # out, q, k_pool, v_pool, table, lens
+
+    def call(shape=s, n=2, fst=first, sh=shared, ptok=32, ws=FAKE, nbytes=need):
+        return f(ctypes.byref(shape), *io, n, ctypes.cast(fst, ctypes.c_void_p) if fst is not None else None,
+                 ctypes.cast(sh, ctypes.c_void_p) if sh is not None else None, 0.1, ptok, ws, nbytes, None, None)
+
+    assert call(ptok=24) == pa.PA_ERR_INVALID_ARG
+    assert call(n=17) == pa.PA_ERR_INVALID_ARG
+    assert call(fst=None) == pa.PA_ERR_INVALID_ARG
+    assert call(shape=base_shape(dtype=pa.PA_F32, block_stride=2 * 2 * 16 * 128)) == pa.PA_ERR_UNSUPPORTED
+    assert call(nbytes=need - 1) == pa.PA_ERR_WORKSPACE
+    assert call(fst=(ctypes.c_int32 * 3)(0, 2, 1)) == pa.PA_ERR_INVALID_ARG       # not ascending
+    assert call(fst=(ctypes.c_int32 * 3)(0, 1, 3)) == pa.PA_ERR_INVALID_ARG       # past the batch
+    assert call(sh=(ctypes.c_int32 * 2)(-16, 0)) == pa.PA_ERR_INVALID_ARG
+    wide = base_shape(batch=3, num_heads=16, num_kv_heads=2)   # 2 members x 8 heads = 16: fine; 3 x 8 not
+    assert call(shape=wide, n=1, fst=(ctypes.c_int32 * 2)(0, 3), sh=(ctypes.c_int32 * 1)(64),
+                nbytes=1 << 30) == pa.PA_ERR_UNSUPPORTED
+    assert call(shape=base_shape(batch=0)) == pa.PA_OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
     monkeypatch.setattr(pa, "_lib", None)

@@ -396,3 +396,46 @@ def to_int8(w: Workload, *, seed: int = 17, scale_range=(0.004, 0.012)) -> Int8W
     return Int8Workload(w.name + "-int8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
                         cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
                         cpu(w.v_new), w.scale, dict(w.meta, int8_seed=seed))
+
+
+def make_prefix_groups(*, group_sizes, shared_blocks, tails, H, Hkv, D, bs, dtype, seed=0,
+                       poison=True, device="cpu") -> Workload:
+    """Sequences forked from common prompts: group i has group_sizes[i]
+    members whose tables share the same shared_blocks[i] physical blocks
+    (reference count = group size), then each member's private blocks for
+    its own tails[b] tokens.  meta["group_first"] / meta["shared_tokens"]
+    describe the groups (group_first has one entry more than the groups)."""
+    gen = torch.Generator().manual_seed(seed)
+    B = sum(group_sizes)
+    assert len(tails) == B and len(shared_blocks) == len(group_sizes)
+    lens, first, shared = [], [0], []
+    for gi, n in enumerate(group_sizes):
+        for m in range(n):
+            lens.append(shared_blocks[gi] * bs + tails[first[-1] + m])
+        shared.append(shared_blocks[gi] * bs)
+        first.append(first[-1] + n)
+    nblk = [_ceil_div(L + 1, bs) for L in lens]
+    MB = max(nblk) + 2
+    NB = sum(shared_blocks) + sum(nblk[b] - shared_blocks[gi] for gi in range(len(group_sizes))
+                                  for b in range(first[gi], first[gi + 1])) + 4
+    perm = torch.randperm(NB, generator=gen).to(torch.int32)
+    table = torch.full((B, MB), -1, dtype=torch.int32)
+    k = 0
+    for gi in range(len(group_sizes)):
+        common = perm[k:k + shared_blocks[gi]]
+        k += shared_blocks[gi]
+        for b in range(first[gi], first[gi + 1]):
+            table[b, :shared_blocks[gi]] = common
+            own = nblk[b] - shared_blocks[gi]
+            table[b, shared_blocks[gi]:nblk[b]] = perm[k:k + own]
+            k += own
+    pool = _randn((NB, 2, Hkv, bs, D), gen, dtype, "cpu")
+    q = _randn((B, H, D), gen, dtype, "cpu")
+    k_new = _randn((B, Hkv, D), gen, dtype, "cpu")
+    v_new = _randn((B, Hkv, D), gen, dtype, "cpu")
+    w = Workload("prefix-groups", B, H, Hkv, D, bs, NB, MB, dtype,
+                 torch.tensor(lens, dtype=torch.int32), table, pool, q, k_new, v_new,
+                 1.0 / math.sqrt(D), {"seed": seed, "group_first": first, "shared_tokens": shared})
+    if poison:
+        poison_pool(w)
+    return w.to(device) if str(device) != "cpu" else w
