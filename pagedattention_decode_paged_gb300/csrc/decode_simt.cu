@@ -1,5 +1,5 @@
 // decode_simt.cu -- decode attention on the CUDA cores (one CTA per
-// (sequence, query head[, partition])), and the split-KV reduce.
+// (sequence, query head[, partition])).
 //
 // The computation is the per-block decomposition of attention described in
 // "KV Cache paging in LLM inference" (intelliparadigm.com) s2.2: the query
@@ -378,40 +378,6 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
 }
 
 // ---------------------------------------------------------------------------
-// split-KV reduce: log-sum-exp merge of the partitions of each (b, h)
-// ---------------------------------------------------------------------------
-
-template <typename T>
-__global__ void __launch_bounds__(128) reduce_kernel(ReduceParams p) {
-    grid_dependency_wait();
-    allow_dependents();
-    const int64_t bh = blockIdx.x;
-    const int b = (int)(bh / p.H);
-    T *out = reinterpret_cast<T *>(p.out);
-    const int32_t len = p.seq_lens[b];
-    const bool bad_len = len < 0 || (int64_t)len > (int64_t)p.MB * p.bs;
-    if (bad_len && threadIdx.x == 0 && (bh % p.H) == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
-    const int np = bad_len || len == 0 ? 0 : (len + p.partition_tokens - 1) / p.partition_tokens;
-    const float *m = p.ws_m + bh * p.num_partitions;
-    const float *l = p.ws_l + bh * p.num_partitions;
-    const float *acc = p.ws_acc + bh * p.num_partitions * p.D;
-    float M = -INFINITY;
-    bool bad = false;
-    for (int q = 0; q < np; ++q) {
-        M = fmaxf(M, m[q]);
-        bad |= l[q] < 0.f;
-    }
-    float lsum = 0.f;
-    for (int q = 0; q < np; ++q) lsum = fmaf(l[q], exp2f(m[q] - M), lsum);
-    const float inv = 1.f / lsum;
-    for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
-        float o = 0.f;
-        for (int q = 0; q < np; ++q) o = fmaf(acc[(int64_t)q * p.D + d], exp2f(m[q] - M), o);
-        out[bh * p.D + d] = Elem<T>::from_float((np == 0 || bad) ? 0.f : o * inv);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // host-side dispatch
 // ---------------------------------------------------------------------------
 
@@ -466,17 +432,6 @@ cudaError_t launch_decode_simt(int dtype, const DecodeParams &p, bool split, cud
         case PA_BF16:
             return split ? launch_simt_d<__nv_bfloat16, true>(p, stream)
                          : launch_simt_d<__nv_bfloat16, false>(p, stream);
-    }
-    return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream) {
-    const int64_t grid = (int64_t)p.B * p.H;
-    if (grid == 0) return cudaSuccess;
-    switch (dtype) {
-        case PA_F32: return launch_clustered(reduce_kernel<float>, grid, 128, 0, 1, stream, p);
-        case PA_F16: return launch_clustered(reduce_kernel<__half>, grid, 128, 0, 1, stream, p);
-        case PA_BF16: return launch_clustered(reduce_kernel<__nv_bfloat16>, grid, 128, 0, 1, stream, p);
     }
     return cudaErrorInvalidValue;
 }
