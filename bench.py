@@ -44,8 +44,8 @@ import workloads  # noqa: E402
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); attention tokens/s"
 UNIT = "GB/s"
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
-SPLIT_PTOK = {5: 2048}          # workloads timed through split-KV partitions
-SHARED_PREFIX = {5}             # ... with the shared prefix read once per group
+SPLIT_PTOK = {5: 1024}          # workloads timed through split-KV partitions
+SHARED_PREFIX = {5: 4096}       # ... or with the shared prefix read once per group (partition)
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
                   "decode_simt_balanced": "decode_balanced_simt.cu",
@@ -311,7 +311,7 @@ def run_gpu(args) -> None:
         if "shared_blocks" not in w.meta:
             raise SystemExit("--shared-prefix needs a workload with a shared prefix (workload 5)")
         groups = {"first": [0, w.B], "shared": [w.meta["shared_blocks"] * w.bs]}
-        ptok = ptok or 2048
+        ptok = args.split_tokens or SHARED_PREFIX.get(args.workload, 4096)
         ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
         fused = False
         kernel = "decode_prefix_tc"

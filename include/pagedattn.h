@@ -311,8 +311,8 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
  * For each group and kv head, the partitions of partition_tokens tokens that
  * lie wholly inside the shared prefix are read once and attended by every
  * member's queries at once (tensor cores; the members are the MMA columns);
- * all other partitions are computed per sequence, and the log-sum-exp reduce
- * merges them.  The result is paged_attention_decode's, up to rounding
+ * in the same launch all other partitions are computed per sequence, and
+ * the log-sum-exp reduce merges them.  The result is paged_attention_decode's, up to rounding
  * order; it equals the partial + reduce pair's output formula.
  *
  * Device checks: as paged_attention_decode; in addition, a member whose
@@ -321,8 +321,8 @@ pa_status paged_attention_decode_reduce(const pa_shape *shape, void *out,
  * Workspace: exactly that of the partial/reduce pair
  * (paged_attention_partial_workspace).  Shapes: those of the tensor-core
  * path (paged_attention_decode_path() == PA_PATH_TENSOR_GQA, or the same
- * conditions with num_heads == num_kv_heads); others give
- * PA_ERR_UNSUPPORTED.  Three launches on `stream`.
+ * conditions with num_heads == num_kv_heads) with num_heads/num_kv_heads
+ * <= 16; others give PA_ERR_UNSUPPORTED.  Two launches on `stream`.
  */
 pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out, const void *q,
                                                const void *k_pool, const void *v_pool,

@@ -595,9 +595,10 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
     if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
     const int g = shape->num_heads / shape->num_kv_heads;
+    if (g > 16) return PA_ERR_UNSUPPORTED;
     pa::PrefixGroups groups{};
     groups.n = num_groups;
-    int widest = 0;
+    int widest = g;   // the per-sequence units: the query heads of one kv head
     const int64_t row_tokens = (int64_t)shape->max_blocks_per_seq * shape->block_size;
     for (int i = 0; i < num_groups; ++i) {
         const int32_t a = group_first[i], e = group_first[i + 1];
@@ -623,15 +624,12 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
     p.groups = groups;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    // 1. the shared partitions, once per group
+    // 1. the shared partitions once per group, every other one per sequence
     CUtensorMap kmap, vmap;
     if (!cached_pool_map(&kmap, shape, k_pool) || !cached_pool_map(&vmap, shape, v_pool)) return PA_ERR_CUDA;
     if (pa::launch_prefix_tc(shape->dtype, p, kmap, vmap, box_rows_for(shape), widest, s) != cudaSuccess)
         return PA_ERR_CUDA;
-    // 2. every other partition, per sequence
-    st = launch_decode(shape, p, true, s);
-    if (st != PA_OK) return st;
-    // 3. the merge
+    // 2. the merge
     pa::ReduceParams r{};
     r.out = out;
     r.ws_m = p.ws_m;

@@ -94,8 +94,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, kTcMinBlocks)
     unit /= ngroups;
     const int hk = unit % p.Hkv;
     const int part = unit / p.Hkv;
-    // a shared-prefix group has already written this partition's slots
-    if (SPLIT && p.groups.n > 0 && part < prefix_parts_of(p.groups, b)) return;
     const int h0 = hk * g + hg * 16;       // first query head of this CTA
     const int nh = min(16, g - hg * 16);   // live MMA columns
     T *out = reinterpret_cast<T *>(p.out);

@@ -1,5 +1,5 @@
-// decode_prefix_tc.cu -- split-KV partials of a shared prefix, read once for
-// all the sequences that share it.
+// decode_prefix_tc.cu -- split-KV partials where a shared prefix is read once
+// for all the sequences that share it.
 //
 // Sequences forked from one prompt (beam search, parallel sampling) name the
 // same physical blocks for their common prefix, reference-counted instead of
@@ -10,10 +10,13 @@
 // of every member sequence at once: on the tensor cores the member queries
 // (times the query heads of the kv head) are the MMA columns, exactly as the
 // heads of a grouped-query group are in decode_gqa_tc.cu.  It writes the
-// split-KV workspace slot (m, l, acc) of each member for that partition; the
-// per-sequence partial kernels skip those partitions and the usual reduce
-// merges everything ("KV Cache paging in LLM inference", intelliparadigm.com,
-// s2.2: block results are aggregated before the final softmax).
+// split-KV workspace slot (m, l, acc) of each member for that partition.
+// The same launch computes every other partition of every sequence as a
+// unit of one member (the MMA columns are then the query heads of one kv
+// head), so the per-sequence work fills the shared work's tail, and the
+// usual reduce merges everything ("KV Cache paging in LLM inference",
+// intelliparadigm.com, s2.2: block results are aggregated before the final
+// softmax).
 //
 // A member whose table differs from the first member's inside the declared
 // prefix, or whose length does not cover it, gets l = -1 in its slots (the
@@ -63,20 +66,43 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
     const int tig = lane & 3;
     const int g = p.H / p.Hkv;   // query heads per kv head
 
-    // unit -> (group, kv head, partition): groups in order, kv head fastest
-    int unit = blockIdx.x;
-    int grp = 0;
-    while (grp < p.groups.n - 1 && unit >= p.groups.parts[grp] * p.Hkv) {
-        unit -= p.groups.parts[grp] * p.Hkv;
-        ++grp;
+    // Units: first the shared ones, (group, kv head, shared partition) with
+    // groups in order and the kv head fastest; then the per-sequence ones,
+    // (k, kv head, sequence) with the sequence fastest, for partition
+    // (the sequence's shared partitions) + k.
+    int n_shared = 0;
+    for (int i = 0; i < p.groups.n; ++i) n_shared += p.groups.parts[i] * p.Hkv;
+    int b0, nmem, hk, part, t_begin, t_end;
+    const bool shared_unit = (int)blockIdx.x < n_shared;
+    if (shared_unit) {
+        int unit = blockIdx.x;
+        int grp = 0;
+        while (unit >= p.groups.parts[grp] * p.Hkv) {
+            unit -= p.groups.parts[grp] * p.Hkv;
+            ++grp;
+        }
+        hk = unit % p.Hkv;
+        part = unit / p.Hkv;
+        b0 = p.groups.first[grp];
+        nmem = p.groups.first[grp + 1] - b0;
+        t_begin = part * p.partition_tokens;
+        t_end = t_begin + p.partition_tokens;
+    } else {
+        int unit = blockIdx.x - n_shared;
+        b0 = unit % p.B;
+        unit /= p.B;
+        hk = unit % p.Hkv;
+        part = prefix_parts_of(p.groups, b0) + unit / p.Hkv;
+        nmem = 1;
+        const int32_t len = p.seq_lens[b0];
+        // a bad length is the reduce's to report; a partition past the end
+        // is never read by it
+        if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) return;
+        t_begin = part * p.partition_tokens;
+        if (part >= p.num_partitions || t_begin >= len) return;
+        t_end = min(len, t_begin + p.partition_tokens);
     }
-    const int hk = unit % p.Hkv;
-    const int part = unit / p.Hkv;
-    const int b0 = p.groups.first[grp];
-    const int nmem = p.groups.first[grp + 1] - b0;
     const int ncols = nmem * g;                 // live MMA columns: (member, head)
-    const int t_begin = part * p.partition_tokens;
-    const int t_end = t_begin + p.partition_tokens;
     const int j0 = t_begin / p.bs;
     const int nblk = (t_end - 1) / p.bs + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
@@ -91,8 +117,8 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
     if (threadIdx.x < kPfxWarps * C::STAGES) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
     mbar_init_fence();
     __syncthreads();
-    // every member must hold the partition and name the same blocks for it
-    {
+    if (shared_unit) {
+        // every member must hold the partition and name the same blocks for it
         bool bad = false;
         const int64_t need = (int64_t)nmem * nblk;
         for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
@@ -112,7 +138,7 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
     }
     __syncthreads();
 
-    const int ntiles = p.partition_tokens / kTcTile;
+    const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
     const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kPfxWarps + 1 : 0;
     const int subs = kTcTile / box_rows;
     auto lookup = [&](int j) -> int32_t { return (j - j0 < ncache) ? tbl[j - j0] : trow0[j]; };
@@ -128,6 +154,7 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
         bool ok = true;
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
+            if (t >= t_end) break;
             const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
             if (good(lookup(j))) bytes += (uint32_t)(box_rows * 128 * C::HALVES * 2);
             else ok = false;
@@ -139,6 +166,7 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
         mbar_arrive_expect_tx(bar, bytes);
         for (int s = 0; s < subs; ++s) {
             const int t = t0 + s * box_rows;
+            if (t >= t_end) break;
             const int j = p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs;
             const int32_t blk = lookup(j);
             if (!good(blk)) continue;
@@ -198,10 +226,16 @@ __global__ void __launch_bounds__(kPfxWarps * 32, 3)
             aborted = true;
             break;
         }
-        const unsigned char *ks = stages + (size_t)((warp * C::STAGES + slot) * 2) * C::TILE_BYTES;
-        const unsigned char *vs = ks + C::TILE_BYTES;
-        // every row of a shared partition is a valid token of every member
-        tc_tile_step<T, D, NT>(smem_u32(ks), smem_u32(vs), 0, kTcTile, qb, p.scale_log2, o_acc, m_run, l_run,
+        unsigned char *ks = stages + (size_t)((warp * C::STAGES + slot) * 2) * C::TILE_BYTES;
+        unsigned char *vs = ks + C::TILE_BYTES;
+        const int t0 = t_begin + (warp + k * kPfxWarps) * kTcTile;
+        const int nvalid = min(kTcTile, t_end - t0);
+        if (nvalid < kTcTile) {
+            // rows past the sequence's end: weight 0, V kept finite
+            tc_zero_v_rows<D>(vs, nvalid, kTcTile, lane);
+            __syncwarp();
+        }
+        tc_tile_step<T, D, NT>(smem_u32(ks), smem_u32(vs), 0, nvalid, qb, p.scale_log2, o_acc, m_run, l_run,
                                lane);
         fence_proxy_async_smem();
         __syncwarp();
@@ -285,7 +319,14 @@ static cudaError_t launch_prefix_t(const DecodeParams &params, const CUtensorMap
     if (e != cudaSuccess) return e;
     int64_t grid = 0;
     for (int i = 0; i < p.groups.n; ++i) grid += (int64_t)p.groups.parts[i] * p.Hkv;
+    // per-sequence units: enough partitions after the shared ones for the
+    // sequence that shares the fewest
+    int32_t fewest = p.groups.n > 0 && p.groups.first[0] == 0 && p.groups.first[p.groups.n] == p.B ? INT32_MAX : 0;
+    for (int i = 0; i < p.groups.n; ++i) fewest = min(fewest, p.groups.parts[i]);
+    if (fewest == INT32_MAX) fewest = 0;
+    grid += (int64_t)(p.num_partitions - fewest) * p.Hkv * p.B;
     if (grid == 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
     return launch_clustered(kern, grid, kPfxWarps * 32, smem, 1, stream, kmap, vmap, p, box_rows);
 }
 

@@ -91,8 +91,6 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
     unit /= p.B;
     const int h = unit % p.H;
     const int part = unit / p.H;
-    // a shared-prefix group has already written this partition's slots
-    if (SPLIT && p.groups.n > 0 && part < prefix_parts_of(p.groups, b)) return;
     const int hk = h / (p.H / p.Hkv);
     const int64_t bh = (int64_t)b * p.H + h;
     T *out = reinterpret_cast<T *>(p.out);

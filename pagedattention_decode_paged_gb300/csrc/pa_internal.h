@@ -13,7 +13,8 @@ namespace pa {
 // Groups of consecutive sequences whose first partitions lie in blocks they
 // all share (split mode): group i holds sequences [first[i], first[i+1]) and
 // its first parts[i] partitions are computed once for all members by the
-// shared-prefix kernel; the per-sequence partial kernels skip them.
+// shared-prefix kernel, which also computes every other partition per
+// sequence.
 constexpr int kMaxPrefixGroups = 16;
 struct PrefixGroups {
     int32_t n;                               // 0: no groups
@@ -212,7 +213,8 @@ cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream)
 
 // Shared-prefix partials (split mode, tensor-core shapes): one CTA per
 // (group, kv head, shared partition) writes the workspace slots of every
-// member sequence.  `members_times_group` = largest group size x H/Hkv.
+// member sequence, and one per (sequence, kv head, other partition) the rest.
+// `members_times_group` = the widest unit's MMA columns (<= 16).
 cudaError_t launch_prefix_tc(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, int box_rows, int members_times_group,
                              cudaStream_t stream);
