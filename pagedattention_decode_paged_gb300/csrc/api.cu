@@ -71,8 +71,12 @@ bool tc_layout_ok(const pa_shape *s) {
     return true;
 }
 
+#ifndef PA_TC_MIN_GROUP
+#define PA_TC_MIN_GROUP 2   // query heads per kv head from which the tensor-core path is taken
+#endif
+
 bool tc_eligible(const pa_shape *s) {
-    return s->num_heads / s->num_kv_heads >= 2 && tc_layout_ok(s);
+    return s->num_heads / s->num_kv_heads >= PA_TC_MIN_GROUP && tc_layout_ok(s);
 }
 
 // View a pool as a [rows][head_dim] matrix; boxes of 64 x box_rows elements,

@@ -37,9 +37,12 @@ namespace pa {
 #ifndef PA_SIMT_STAGES
 #define PA_SIMT_STAGES 2
 #endif
-constexpr int kSimtWarps = 4;
+#ifndef PA_SIMT_WARPS
+#define PA_SIMT_WARPS 4
+#endif
+constexpr int kSimtWarps = PA_SIMT_WARPS;
 constexpr int kSimtStages = PA_SIMT_STAGES;
-constexpr int kSimtMinBlocks = kSimtStages <= 2 ? 3 : 2;
+constexpr int kSimtMinBlocks = (12 / kSimtWarps) * 2 / kSimtStages > 0 ? (12 / kSimtWarps) * 2 / kSimtStages : 1;
 constexpr int kSimtTableCap = 1024; // table entries staged per CTA (rest read from global)
 
 template <typename T, int D>
