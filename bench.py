@@ -227,6 +227,28 @@ def kernel_traffic(kernel: str, workload: str, fused: bool = False) -> int | Non
     return None
 
 
+def replica_seed(workload: int, rank: int) -> int:
+    """Seed of rank `rank`'s replica of a workload: every rank holds its own
+    independent data (weak scaling, no collective on the data path)."""
+    return 1000 + workload + 7 * rank
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of the ranks' values (the elapsed time a multi-rank run
+    reports); `dist` is torch.distributed or None for one rank."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: the bytes every rank moved in a step over the slowest
+    rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def local_gpu_index(local_rank: int) -> int:
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -265,7 +287,7 @@ def run_gpu(args) -> None:
 
     # each rank holds its own replica of the workload (weak scaling)
     w = workloads.make_workload(args.workload, block_size=args.block_size, device=dev,
-                                seed=1000 + args.workload + 7 * rank, batch=args.batch)
+                                seed=replica_seed(args.workload, rank), batch=args.batch)
     workload_key = f"w{args.workload}" + (f"_bs{args.block_size}" if args.block_size else "")
     if args.long_seq:
         w = workloads.with_long_sequence(w, args.long_seq, seed=7 + rank, device=dev)
@@ -468,10 +490,7 @@ def run_gpu(args) -> None:
     else:
         decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
         append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     # end to end through the C ABI with host buffers: H2D of the step's
     # inputs from pinned memory, append + decode, D2H of the output
@@ -506,10 +525,7 @@ def run_gpu(args) -> None:
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during timing")
 
@@ -523,8 +539,8 @@ def run_gpu(args) -> None:
     peaks = measured_peaks()
     achieved = kbytes / (decode_ms * 1e-3) / 1e9
     ms_step = total_ms / K
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    e2e_value = world * step_bytes / (e2e_ms / Ke * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, ms_step)
+    e2e_value = job_throughput(world, step_bytes, e2e_ms / Ke)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
