@@ -15,10 +15,14 @@
 // inference" (intelliparadigm.com) s2.2 over the values the codes stand
 // for: one CTA per (sequence, query head), each warp streaming its own ring
 // of 4 KB K + 4 KB V tiles (twice the tokens of a 16-bit tile) with bulk
-// copies.  Scores are scale_K(block) * <q, codes>, and the softmax weight of
-// a token is multiplied by scale_V(block) before it meets the V codes; both
-// scales of every block of the sequence are staged in shared memory next to
-// its block-table row.
+// copies.  Scores are scale_K(block) * <q, codes>: each lane holds its 16
+// query elements as int16 fixed point with a power-of-two step (15
+// significant bits, relative error below 2^-15) and takes the dot product
+// with the K codes in integer dp2a instructions (two int16 x int8 products
+// per instruction, exact int32 sums).  The softmax weight of a token is
+// multiplied by scale_V(block) before it meets the V codes, which become
+// exact fp32 values through a byte permute.  Both scales of every block of
+// the sequence are staged in shared memory next to its block-table row.
 #include <math.h>
 
 #include "pa_device.cuh"
@@ -123,7 +127,8 @@ __global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodePar
     mbar_init_fence();
     __syncthreads();
     // the scales of the staged blocks (0 for an entry outside the pool: the
-    // copy of such a block is refused and the output zeroed)
+    // copy of such a block is refused and the output zeroed); gathering them
+    // after the first copies are issued measured slower
     for (int j = threadIdx.x; j < ncache; j += blockDim.x) {
         const int32_t blk = tbl[j];
         sk_tab[j] = good(blk) ? kv_scales[((int64_t)blk * 2 + 0) * p.Hkv + hk] : 0.f;
@@ -176,17 +181,35 @@ __global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodePar
         }
     };
 
-    // this lane's 16 query elements, in fp32 pairs
-    float2 q2[C::VEC / 2];
-    {
-        const T *qrow = reinterpret_cast<const T *>(p.q) + bh * D + c * C::VEC;
-#pragma unroll
-        for (int e = 0; e < C::VEC / 2; ++e)
-            q2[e] = make_float2(Elem<T>::to_float(qrow[2 * e]), Elem<T>::to_float(qrow[2 * e + 1]));
-    }
-
     if (lane == 0)
         for (int k = 0; k < min(S, my_tiles); ++k) issue(k);
+
+    // this lane's 16 query elements as 15-bit fixed point, q ~= Q * 2^-qs,
+    // packed in int16 pairs: the K codes then meet them in integer dot
+    // products (dp2a), exact, with one conversion per row of 16 codes
+    uint32_t qpk[C::VEC / 2];
+    float q_unit;
+    {
+        const T *qrow = reinterpret_cast<const T *>(p.q) + bh * D + c * C::VEC;
+        float qf[C::VEC];
+        float qmax = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::VEC; ++e) {
+            qf[e] = Elem<T>::to_float(qrow[e]);
+            qmax = fmaxf(qmax, fabsf(qf[e]));
+        }
+        int ex = 0;
+        frexpf(qmax, &ex);                  // qmax = m * 2^ex, m in [0.5, 1)
+        const int qs = qmax > 0.f ? 14 - ex : 0;   // |Q| < 2^14
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e) {
+            const int lo = __float2int_rn(ldexpf(qf[2 * e], qs));
+            const int hi = __float2int_rn(ldexpf(qf[2 * e + 1], qs));
+            qpk[e] = ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
+        }
+        q_unit = ldexpf(1.f, -qs);
+    }
+    __syncthreads();
 
     float m_run = -INFINITY, l_run = 0.f;
     float2 acc2[C::VEC / 2];
@@ -208,17 +231,20 @@ __global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodePar
         const int t0 = (warp + k * kI8Warps) * C::TILE;
         const int nrows = min(C::TILE, len - t0);
 
-        // scores: partial dot products of 8 rows, then the butterfly
+        // scores: partial dot products of 8 rows (integer, exact), then the
+        // butterfly
         float v[C::NVALS];
 #pragma unroll
         for (int j = 0; j < C::NVALS; ++j) {
             const uint4 kv = *reinterpret_cast<const uint4 *>(ks + (j * C::RPW + r) * C::ROWB + c * 16);
-            float2 k2[C::VEC / 2];
-            codes_to_float2(kv, k2);
-            float2 a = __fmul2_rn(q2[0], k2[0]);
+            const int w[4] = {(int)kv.x, (int)kv.y, (int)kv.z, (int)kv.w};
+            int a = 0;
 #pragma unroll
-            for (int e = 1; e < C::VEC / 2; ++e) a = __ffma2_rn(q2[e], k2[e], a);
-            v[j] = a.x + a.y;
+            for (int e = 0; e < 4; ++e) {
+                a = __dp2a_lo((int)qpk[2 * e], w[e], a);
+                a = __dp2a_hi((int)qpk[2 * e + 1], w[e], a);
+            }
+            v[j] = (float)a * q_unit;
         }
         Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
 
