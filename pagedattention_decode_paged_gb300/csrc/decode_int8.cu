@@ -20,9 +20,10 @@
 // significant bits, relative error below 2^-15) and takes the dot product
 // with the K codes in integer dp2a instructions (two int16 x int8 products
 // per instruction, exact int32 sums).  The softmax weight of a token is
-// multiplied by scale_V(block) before it meets the V codes, which become
-// exact fp32 values through a byte permute.  Both scales of every block of
-// the sequence are staged in shared memory next to its block-table row.
+// multiplied by scale_V(block), rounded to int16 with one step per tile
+// (relative error of the largest weight below 2^-14), and meets the V codes
+// in dp2a as well, two tokens per instruction.  Both scales of every block
+// of the sequence are staged in shared memory next to its block-table row.
 #include <math.h>
 
 #include "pa_device.cuh"
@@ -62,23 +63,6 @@ struct I8Smem {
     static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 12; }   // ids, scale_K, scale_V
 };
-
-// 16 int8 codes -> 8 float pairs, exactly: each byte (biased to 0..255) is
-// placed in the mantissa of 2^23 by a byte permute, and 2^23 + 128 is
-// subtracted.
-__device__ __forceinline__ void codes_to_float2(const uint4 &v, float2 *f) {
-    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-    const float2 bias = make_float2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 lo = make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)),
-                                      __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541)));
-        const float2 hi = make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)),
-                                      __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543)));
-        f[2 * i] = __fadd2_rn(lo, bias);
-        f[2 * i + 1] = __fadd2_rn(hi, bias);
-    }
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
@@ -276,23 +260,45 @@ __global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodePar
             pj[j] = f.x; pj[j + 1] = f.y; pj[j + 2] = f.z; pj[j + 3] = f.w;
             pjs[j] = g.x; pjs[j + 1] = g.y; pjs[j + 2] = g.z; pjs[j + 3] = g.w;
         }
-        const float2 corr2 = make_float2(corr, corr);
+        // P.V in integers: the weights times the V scales of their blocks
+        // become int16 with one power-free step per tile (largest = 16383),
+        // two tokens' codes of each column are interleaved by a byte
+        // permute, and dp2a accumulates both products exactly in int32.
+        // Rows past the valid length have weight 0 (their stale bytes add 0).
+        float pmax = 0.f;
 #pragma unroll
-        for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __fmul2_rn(acc2[e], corr2);
-        float psum = 0.f;
+        for (int j = 0; j < C::NVALS; ++j) pmax = fmaxf(pmax, pjs[j]);
+        pmax = warp_max_f32(pmax);
+        const float to_int = pmax > 0.f ? 16383.f / pmax : 0.f;
+        int acc_i[C::VEC];
 #pragma unroll
-        for (int j = 0; j < C::NVALS; ++j) {
-            // rows past the valid length were never fetched: skip them
-            if (j * C::RPW + r < nrows) {
-                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
-                float2 v2[C::VEC / 2];
-                codes_to_float2(vv, v2);
-                const float2 p2 = make_float2(pjs[j], pjs[j]);
+        for (int e = 0; e < C::VEC; ++e) acc_i[e] = 0;
 #pragma unroll
-                for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __ffma2_rn(p2, v2[e], acc2[e]);
-                psum += pj[j];
+        for (int j = 0; j < C::NVALS; j += 2) {
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(vs + ((j + 1) * C::RPW + r) * C::ROWB + c * 16);
+            const int p0 = __float2int_rn(pjs[j] * to_int), p1 = __float2int_rn(pjs[j + 1] * to_int);
+            const int pp = (int)(((uint32_t)p0 & 0xffffu) | ((uint32_t)p1 << 16));
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int lo = (int)__byte_perm(w0[e], w1[e], 0x5140);   // columns 4e, 4e+1 of both rows
+                const int hi = (int)__byte_perm(w0[e], w1[e], 0x7362);   // columns 4e+2, 4e+3
+                acc_i[4 * e + 0] = __dp2a_lo(pp, lo, acc_i[4 * e + 0]);
+                acc_i[4 * e + 1] = __dp2a_hi(pp, lo, acc_i[4 * e + 1]);
+                acc_i[4 * e + 2] = __dp2a_lo(pp, hi, acc_i[4 * e + 2]);
+                acc_i[4 * e + 3] = __dp2a_hi(pp, hi, acc_i[4 * e + 3]);
             }
         }
+        const float from_int = pmax * (1.f / 16383.f);
+        const float2 corr2 = make_float2(corr, corr);
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e)
+            acc2[e] = __ffma2_rn(acc2[e], corr2,
+                                 make_float2((float)acc_i[2 * e] * from_int, (float)acc_i[2 * e + 1] * from_int));
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < C::NVALS; ++j) psum += pj[j];
         l_run = fmaf(l_run, corr, psum);
         m_run = m_new;
         fence_proxy_async_smem();
