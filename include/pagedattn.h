@@ -408,7 +408,9 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
  * paged_attention_decode_int8 is paged_attention_decode over the values the
  * codes stand for ([PG] s2.2): x_t = scale * s_K * <q, c_t>, weights w_t as
  * there, out = sum_t w_t s_V c_t / sum_t w_t.  Same device checks, zeros and
- * PA_DEVERR_* bits.  Both run on the CUDA cores for every head layout.
+ * PA_DEVERR_* bits.  Grouped-query shapes with 16-bit q and head_dim 64 or
+ * 128 run on the tensor cores (codes turned into exact fp16 in shared
+ * memory, queries rounded to fp16); the rest on the CUDA cores.
  */
 pa_status paged_kv_append_int8(const pa_shape *shape, const void *k_new, const void *v_new,
                                int8_t *k_pool, int8_t *v_pool, const float *kv_scales,

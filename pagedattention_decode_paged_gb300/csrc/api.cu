@@ -719,10 +719,12 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
     p.partition_tokens = 0;
     p.num_partitions = 1;
     p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
-    return pa::launch_decode_int8(shape->dtype, p, kv_scales, reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? PA_OK
-               : PA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = shape->num_heads / shape->num_kv_heads >= 2 &&
+                    pa::int8_tc_supported(shape->dtype, shape->head_dim);
+    const cudaError_t e = tc ? pa::launch_decode_int8_tc(shape->dtype, p, kv_scales, s)
+                             : pa::launch_decode_int8(shape->dtype, p, kv_scales, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -226,6 +226,10 @@ cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv
                                cudaStream_t stream);
 cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv_scales,
                                int head_dim, cudaStream_t stream);
+// grouped-query shapes of the int8 cache on the tensor cores
+bool int8_tc_supported(int dtype, int head_dim);
+cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                  cudaStream_t stream);
 
 // Load-balanced persistent decode (final mode; plain, fused append or sliding
 // window as DecodeParams says).  A plan fixes the grid for a shape on the

@@ -45,11 +45,17 @@ __device__ __forceinline__ void tc_zero_v_rows(unsigned char *vs, int r0, int r1
 // nt; m_run / l_run[nt][j] belong to head column nt*8 + 2*tig + j, and
 // l_run is this lane's share of the column sum (complete it over the 8 lanes
 // of a column group before use).
-template <typename T, int D, int NT>
+// With ROWSCALE, token row gid (gid + 8) of K stands for its stored values
+// times row_k.x (row_k.y) and of V times row_v.x (row_v.y): the scores are
+// multiplied by the K factor, and the weights that meet V by the V factor
+// (the running sum keeps the weights themselves).
+template <typename T, int D, int NT, bool ROWSCALE = false>
 __device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int lo, int nvalid,
                                              const uint32_t (&qb)[D / 16][NT][2], float scale_log2,
                                              float (&o_acc)[D / 16][NT][4], float (&m_run)[NT][2],
-                                             float (&l_run)[NT][2], int lane) {
+                                             float (&l_run)[NT][2], int lane,
+                                             float2 row_k = make_float2(1.f, 1.f),
+                                             float2 row_v = make_float2(1.f, 1.f)) {
     constexpr int KSTEPS = D / 16;   // MMA K steps of K.Q^T
     constexpr int MT = D / 16;       // MMA M tiles of V^T.P^T
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
@@ -83,8 +89,8 @@ __device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int l
         float corr[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float x0 = v0 ? s[nt][j] * scale_log2 : -INFINITY;
-            const float x1 = v1 ? s[nt][j + 2] * scale_log2 : -INFINITY;
+            const float x0 = v0 ? s[nt][j] * (ROWSCALE ? scale_log2 * row_k.x : scale_log2) : -INFINITY;
+            const float x1 = v1 ? s[nt][j + 2] * (ROWSCALE ? scale_log2 * row_k.y : scale_log2) : -INFINITY;
             float mx = fmaxf(x0, x1);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -97,14 +103,27 @@ __device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int l
         }
         // 16-bit P^T fragments (row = token, columns = 2 heads), then the
         // in-register transpose into the B operand (row = head)
-        const uint32_t h0w = Elem<T>::pack2(pv[0], pv[1]);
-        const uint32_t h1w = Elem<T>::pack2(pv[2], pv[3]);
+        float pm[4];   // the weights that meet V
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pm[e] = ROWSCALE ? pv[e] * (e < 2 ? row_v.x : row_v.y) : pv[e];
+        const uint32_t h0w = Elem<T>::pack2(pm[0], pm[1]);
+        const uint32_t h1w = Elem<T>::pack2(pm[2], pm[3]);
         bhi[nt][0] = movmatrix_trans(h0w);
         bhi[nt][1] = movmatrix_trans(h1w);
         float r0, r1, r2, r3;
         Elem<T>::unpack2(h0w, r0, r1);
         Elem<T>::unpack2(h1w, r2, r3);
-        if constexpr (kSplitP) {
+        if constexpr (ROWSCALE) {
+            // the running sum takes the weights; the MMA their scaled copies
+            if constexpr (kSplitP) {
+                blo[nt][0] = movmatrix_trans(Elem<T>::pack2(pm[0] - r0, pm[1] - r1));
+                blo[nt][1] = movmatrix_trans(Elem<T>::pack2(pm[2] - r2, pm[3] - r3));
+            } else {
+                blo[nt][0] = blo[nt][1] = 0u;
+            }
+            l_run[nt][0] = fmaf(l_run[nt][0], corr[0], pv[0] + pv[2]);
+            l_run[nt][1] = fmaf(l_run[nt][1], corr[1], pv[1] + pv[3]);
+        } else if constexpr (kSplitP) {
             // bf16 keeps 8 mantissa bits: carry the rounding error as a
             // second bf16 term so P is good to about 16 bits
             blo[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0] - r0, pv[1] - r1));

@@ -97,10 +97,15 @@ def test_int8_block_sizes(bs):
     run_step8(w)
 
 
-@pytest.mark.parametrize("H,Hkv", [(8, 2), (16, 1), (64, 8)])
-def test_int8_grouped_query(H, Hkv):
-    w = workloads.to_int8(workloads.make_generic(B=len(LENS), H=H, Hkv=Hkv, D=128, bs=16, dtype=BF16,
-                                                 lens=LENS, seed=H, poison=False), seed=H)
+@pytest.mark.parametrize("H,Hkv,dtype,D,bs", [(8, 2, BF16, 128, 16), (16, 1, BF16, 128, 16),
+                                              (64, 8, BF16, 128, 16), (48, 2, F16, 128, 16),
+                                              (16, 2, F16, 64, 8), (8, 2, BF16, 128, 3),
+                                              (8, 2, F32, 128, 16)])
+def test_int8_grouped_query(H, Hkv, dtype, D, bs):
+    """Tensor-core int8 path (16-bit queries, head_dim 64/128, any block
+    size) and the CUDA-core one for fp32 queries."""
+    w = workloads.to_int8(workloads.make_generic(B=len(LENS), H=H, Hkv=Hkv, D=D, bs=bs, dtype=dtype,
+                                                 lens=LENS, seed=H + bs, poison=False), seed=H)
     run_step8(w)
 
 
@@ -127,9 +132,10 @@ def test_int8_append_rounding_edges():
     assert torch.equal(g.pool.cpu(), ref_pool)
 
 
-def test_int8_errors_reported_and_zeroed():
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (16, 2)])
+def test_int8_errors_reported_and_zeroed(H, Hkv):
     lens = [40, 40, 40, 40]
-    w = workloads.to_int8(workloads.make_generic(B=4, H=4, Hkv=4, D=128, bs=16, dtype=BF16, lens=lens,
+    w = workloads.to_int8(workloads.make_generic(B=4, H=H, Hkv=Hkv, D=128, bs=16, dtype=BF16, lens=lens,
                                                  seed=9, poison=False), seed=9)
     w.block_table[1, 1] = -1                 # hole inside the valid range
     w.block_table[2, 0] = w.NB + 2           # id past the pool
