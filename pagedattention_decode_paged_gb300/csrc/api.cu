@@ -276,14 +276,16 @@ pa_status balanced_plan(const pa_shape *s, int32_t window, pa::BalancedPlan *pla
     return PA_OK;
 }
 
-// Workspace of the balanced schedule: records, then one counter per item.
+// Workspace of the balanced schedule: two records per warp, one group
+// counter per record, then one counter per item (at the very end).
 struct BalWs {
-    size_t off_counters, total;
+    size_t off_group_counters, off_counters, total;
 };
 BalWs balanced_ws(const pa::BalancedPlan &plan) {
     BalWs w;
-    const size_t rec = (size_t)2 * plan.grid * pa::kBalWarps * plan.rec_floats * 4;
-    w.off_counters = (rec + 15) & ~(size_t)15;
+    const size_t nrec = (size_t)2 * plan.grid * pa::kBalWarps;
+    w.off_group_counters = nrec * plan.rec_floats * 4;   // rec_floats is a multiple of 4
+    w.off_counters = w.off_group_counters + nrec * 4;
     w.total = w.off_counters + (size_t)plan.items * 4;
     return w;
 }
@@ -559,6 +561,7 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
     char *ws = static_cast<char *>(workspace);
     p.records = reinterpret_cast<float *>(ws);
     p.counters = reinterpret_cast<int32_t *>(ws + w.off_counters);
+    p.group_counters = reinterpret_cast<int32_t *>(ws + w.off_group_counters);
     p.rec_floats = plan.rec_floats;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

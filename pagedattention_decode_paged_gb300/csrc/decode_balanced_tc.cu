@@ -21,6 +21,12 @@
 
 namespace pa {
 
+// Sharers of one item above which its records are merged in two levels.
+#ifndef PA_BAL_TC_MERGE_GROUP
+#define PA_BAL_TC_MERGE_GROUP 8
+#endif
+constexpr int kMergeGroup = PA_BAL_TC_MERGE_GROUP;
+
 #ifndef PA_BAL_TC_STAGES
 #define PA_BAL_TC_STAGES 2
 #endif
@@ -197,18 +203,20 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
             }
     };
 
-    // Merge the records of an item whose first tile is F, shared by warps
-    // g0..g1, register by register (log-sum-exp in slice order: the maxima
-    // first, then the weighted sums, several records in flight per lane),
-    // and write its output.
-    auto merge_item = [&](int b, int h0, int nh, int32_t F, int g0, int g1) {
-        const int n = g1 - g0 + 1;
-        auto rec_of = [&](int w) {
-            return p.records + ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) *
-                                   p.rec_floats;
-        };
+    // The record of sharer w of an item whose first tile is F and whose
+    // first sharer is g0 (slot 1 when the item is g0's second one).
+    auto rec_of = [&](int32_t F, int g0, int w) {
+        return p.records +
+               ((int64_t)w * 2 + ((w == g0 && slice_start(w, total, W) < F) ? 1 : 0)) * p.rec_floats;
+    };
+
+    // Combine the records of sharers w0, w0 + stride, ... (n of them) of an
+    // item (F, g0) register by register: log-sum-exp in slice order, the
+    // maxima first, then the weighted sums, several records in flight per
+    // lane.  Returns the state of the combination in M, acc and lsum.
+    auto combine = [&](int32_t F, int g0, int w0, int stride, int n, float (&M)[NT][2],
+                       float (&acc)[C::MT][NT][4], float (&lsum)[NT][2]) {
         constexpr int UM = 8, UA = NT == 1 ? 2 : 1;
-        float M[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) M[nt][0] = M[nt][1] = -INFINITY;
         bool bad = false;
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
 #pragma unroll
             for (int u = 0; u < UM; ++u) {
                 const bool live = r0 + u < n;
-                const float *rw = rec_of(g0 + min(r0 + u, n - 1));
+                const float *rw = rec_of(F, g0, w0 + min(r0 + u, n - 1) * stride);
                 bv[u] = live && __ldcg(rw) != 0.f;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -235,7 +243,6 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
                     for (int j = 0; j < 2; ++j) M[nt][j] = fmaxf(M[nt][j], mv[u][nt][j]);
             }
         }
-        float acc[C::MT][NT][4], lsum[NT][2];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
 #pragma unroll
             for (int u = 0; u < UA; ++u) {
                 const bool live = r0 + u < n;
-                const float *rw = rec_of(g0 + min(r0 + u, n - 1)) + 4;
+                const float *rw = rec_of(F, g0, w0 + min(r0 + u, n - 1) * stride) + 4;
 #pragma unroll
                 for (int f = 0; f < C::NF + NT * 4; ++f)
                     rv[u][f] = live ? __ldcg(rw + f * 32 + lane) : (f >= C::NF && f < C::NF + NT * 2 ? -INFINITY : 0.f);
@@ -273,6 +280,57 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
                             acc[mt][nt][e] = fmaf(rv[u][(mt * NT + nt) * 4 + e], wt[nt][e & 1], acc[mt][nt][e]);
             }
         }
+        return bad;
+    };
+
+    // Store a partial state as record `rec` (fragment order).
+    auto store_record = [&](float *rec, bool bad, const float (&acc)[C::MT][NT][4], const float (&m)[NT][2],
+                            const float (&l)[NT][2]) {
+        if (lane == 0) rec[0] = bad ? 1.f : 0.f;
+        float *rf = rec + 4;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) rf[((mt * NT + nt) * 4 + e) * 32 + lane] = acc[mt][nt][e];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                rf[(C::NF + nt * 2 + j) * 32 + lane] = m[nt][j];
+                rf[(C::NF + NT * 2 + nt * 2 + j) * 32 + lane] = l[nt][j];
+            }
+    };
+
+    // This warp (sharer gw of the item (b, it) with first tile F, shared by
+    // g0..g1) has published its record: the last sharer to arrive merges the
+    // records and writes the output.  An item with more than kMergeGroup
+    // sharers is merged in two levels so that no warp combines more than
+    // about sqrt(sharers) records in a row: each run of kMergeGroup
+    // consecutive sharers is combined by its last arrival into the run's
+    // first record, and the last run to finish combines the runs.
+    auto finish_item = [&](int b, int it, int h0, int nh, int32_t F, int g0, int g1) {
+        const int n = g1 - g0 + 1;
+        float M[NT][2], acc[C::MT][NT][4], lsum[NT][2];
+        int32_t *counter = p.counters + (int64_t)b * NI + it;
+        if (n <= kMergeGroup) {
+            if (!count_and_check_last(counter, n, lane)) return;
+            const bool bad = combine(F, g0, g0, 1, n, M, acc, lsum);
+            write_out(b, h0, nh, acc, lsum, bad);
+            return;
+        }
+        const int a = g0 + (gw - g0) / kMergeGroup * kMergeGroup;   // first sharer of this run
+        const int na = min(g1 - a + 1, kMergeGroup);
+        float *head = rec_of(F, g0, a);
+        if (!count_and_check_last(p.group_counters + (head - p.records) / p.rec_floats, na, lane)) return;
+        const bool bad_run = combine(F, g0, a, 1, na, M, acc, lsum);
+        __syncwarp();   // every lane has read the run's first record before it is replaced
+        store_record(head, bad_run, acc, M, lsum);
+        release_records();
+        const int runs = (n + kMergeGroup - 1) / kMergeGroup;
+        if (!count_and_check_last(counter, runs, lane)) return;
+        const bool bad = combine(F, g0, g0, kMergeGroup, runs, M, acc, lsum);
         write_out(b, h0, nh, acc, lsum, bad);
     };
 
@@ -375,26 +433,9 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
                 // shared with the neighbouring slices: publish a record; the
                 // last sharer to arrive merges them all
                 const int sid = F <= start ? 0 : 1;
-                float *rec = p.records + ((int64_t)gw * 2 + sid) * p.rec_floats;
-                if (lane == 0) rec[0] = item_bad ? 1.f : 0.f;
-                float *rf = rec + 4;
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) rf[((mt * NT + nt) * 4 + e) * 32 + lane] = o_acc[mt][nt][e];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        rf[(C::NF + nt * 2 + j) * 32 + lane] = m_run[nt][j];
-                        rf[(C::NF + NT * 2 + nt * 2 + j) * 32 + lane] = l_run[nt][j];
-                    }
+                store_record(p.records + ((int64_t)gw * 2 + sid) * p.rec_floats, item_bad, o_acc, m_run, l_run);
                 release_records();
-                const int g0 = slice_owner(F, total, W), g1 = slice_owner(Lt, total, W);
-                if (count_and_check_last(p.counters + (int64_t)b * NI + cc.it, g1 - g0 + 1, lane))
-                    merge_item(b, h0, nh, F, g0, g1);
+                finish_item(b, cc.it, h0, nh, F, slice_owner(F, total, W), slice_owner(Lt, total, W));
             }
         }
 

@@ -33,12 +33,15 @@
 
 namespace pa {
 
-constexpr int kTcWarps = 4;
+#ifndef PA_TC_WARPS
+#define PA_TC_WARPS 4
+#endif
+constexpr int kTcWarps = PA_TC_WARPS;
 constexpr int kTcTableCap = 1024;  // table entries staged per CTA (rest read from global)
 #ifndef PA_TC_STAGES
 #define PA_TC_STAGES 2                 // tiles in flight per warp at head_dim >= 128
 #endif
-constexpr int kTcMinBlocks = PA_TC_STAGES <= 2 ? 3 : 2;
+constexpr int kTcMinBlocks = (PA_TC_STAGES <= 2 ? 12 : 8) / kTcWarps;
 
 template <int D>
 struct TcCfg {
@@ -47,10 +50,12 @@ struct TcCfg {
     static constexpr int STAGES = D == 64 ? 4 : PA_TC_STAGES;  // tiles in flight per warp
     static constexpr int KSTEPS = D / 16;                // MMA K steps of K.Q^T
     static constexpr int MT = D / 16;                    // MMA M tiles of V^T.P^T
-    static constexpr size_t kStageBytes = (size_t)kTcWarps * STAGES * 2 * TILE_BYTES;
     static constexpr size_t kRedBytes = (size_t)kTcWarps * 16 * (D + 2) * 4;
     static constexpr size_t kXchgBytes = (size_t)16 * (D + 3) * 4;  // CTA result for the cluster leader
-    static_assert(kRedBytes + kXchgBytes <= kStageBytes, "merge areas reuse the stage buffers");
+    // the stage buffers, which the merge areas reuse afterwards
+    static constexpr size_t kStageBytes = (size_t)kTcWarps * STAGES * 2 * TILE_BYTES > kRedBytes + kXchgBytes
+                                              ? (size_t)kTcWarps * STAGES * 2 * TILE_BYTES
+                                              : ((kRedBytes + kXchgBytes + 1023) & ~(size_t)1023);
     static constexpr size_t kBars = (size_t)kTcWarps * STAGES * 8;
     static constexpr size_t kFixed = 1024 /*alignment slack*/ + kStageBytes + kBars + 16;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 4; }

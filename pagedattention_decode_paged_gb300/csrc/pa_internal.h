@@ -64,9 +64,12 @@ struct DecodeParams {
     float scale_log2;          // scale * log2(e)
     // Load-balanced schedule: a warp's partial state for an item it shares
     // with other warps goes to records[(warp * 2 + slot) * rec_floats ...];
-    // counters[item] counts the warps that have published theirs.
+    // counters[item] counts the warps that have published theirs;
+    // group_counters[warp * 2 + slot] counts, for an item shared by many
+    // warps, the members of the group of sharers that this record heads.
     float *records;
     int32_t *counters;
+    int32_t *group_counters;
     int32_t rec_floats;
     PrefixGroups groups;       // split mode: partitions computed by the shared-prefix kernel
 };
