@@ -51,6 +51,7 @@ KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_
                   "decode_simt_balanced": "decode_balanced_simt.cu",
                   "decode_tc_balanced": "decode_balanced_tc.cu",
                   "decode_int8": "decode_int8.cu",
+                  "decode_int8_tc": "decode_int8_tc.cu",
                   "decode_prefix_tc": "decode_prefix_tc.cu",
                   "append_tokens": "append.cu"}
 
@@ -304,7 +305,10 @@ def run_gpu(args) -> None:
     path = pa.paged_attention_decode_path(shape)
     kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
     if args.int8:
-        kernel = "decode_int8"
+        # grouped-query shapes with 16-bit queries and head_dim 64/128 run on
+        # the tensor cores (the rule of paged_attention_decode_int8)
+        tc8 = w.H // w.Hkv >= 2 and w.D in (64, 128) and w.dtype in (torch.float16, torch.bfloat16)
+        kernel = "decode_int8_tc" if tc8 else "decode_int8"
     if args.prefill:
         kernel = "append_tokens"
     ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
