@@ -98,6 +98,34 @@ bool encode_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// View an int8 pool as a [rows][head_dim] byte matrix; boxes of the whole
+// row x box_rows rows, swizzled over the row (128-byte rows: 128-byte
+// swizzle, 64-byte rows: 64-byte swizzle).
+bool encode_int8_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const int64_t rows_per_block = s->block_stride / s->head_dim;
+    const int64_t rows = (s->num_blocks - 1) * rows_per_block +
+                         (int64_t)s->num_kv_heads * s->block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)s->head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)s->head_dim};
+    cuuint32_t box[2] = {(cuuint32_t)s->head_dim, (cuuint32_t)box_rows_for(s)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              s->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The int8 tensor-core kernel can fetch this pool's tiles as tensor boxes
+// (boxes of 8 or 16 rows inside a block, row coordinates in int32);
+// otherwise it copies row by row.
+bool int8_tc_boxes_ok(const pa_shape *s) {
+    if (!(s->block_size % 16 == 0 || s->block_size == 8)) return false;
+    if (s->block_stride % s->head_dim != 0) return false;
+    return s->num_blocks * (s->block_stride / s->head_dim) <= (int64_t)INT32_MAX;
+}
+
 int64_t num_partitions(const pa_shape *s, int32_t ptok) {
     return ((int64_t)s->max_blocks_per_seq * s->block_size + ptok - 1) / ptok;
 }
@@ -185,7 +213,7 @@ struct MapKey {
     }
 };
 
-bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
+bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool int8 = false) {
     constexpr int kSlots = 16;
     static std::mutex mu;
     static MapKey keys[kSlots];
@@ -195,14 +223,14 @@ bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const int64_t rows = (s->num_blocks - 1) * (s->block_stride / s->head_dim) +
                          (int64_t)s->num_kv_heads * s->block_size;
-    const MapKey key{pool, rows, s->head_dim, box_rows_for(s), s->dtype, dev};
+    const MapKey key{pool, rows, s->head_dim, box_rows_for(s), int8 ? -1 - s->dtype : s->dtype, dev};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (keys[i] == key) {
             *map = maps[i];
             return true;
         }
-    if (!encode_pool_map(map, s, pool)) return false;
+    if (!(int8 ? encode_int8_pool_map(map, s, pool) : encode_pool_map(map, s, pool))) return false;
     const int slot = used < kSlots ? used++ : (next++ % kSlots);
     keys[slot] = key;
     maps[slot] = *map;
@@ -725,8 +753,13 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tc = shape->num_heads / shape->num_kv_heads >= 2 &&
                     pa::int8_tc_supported(shape->dtype, shape->head_dim);
-    const cudaError_t e = tc ? pa::launch_decode_int8_tc(shape->dtype, p, kv_scales, s)
-                             : pa::launch_decode_int8(shape->dtype, p, kv_scales, s);
+    if (!tc) return pa::launch_decode_int8(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    CUtensorMap kmap{}, vmap{};
+    const bool boxes = int8_tc_boxes_ok(shape);
+    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
+        return PA_ERR_CUDA;
+    const cudaError_t e = pa::launch_decode_int8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
+                                                    boxes ? &vmap : nullptr, box_rows_for(shape), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -5,14 +5,29 @@
 // c * s, one fp32 scale per (block, kv head) for K and one for V) read by one
 // CTA per (sequence, kv head, group of up to 16 query heads), as in
 // decode_gqa_tc.cu: every K/V row crosses HBM once for all heads of the
-// group.  A warp fetches 16-token tiles of codes with bulk copies, turns them
-// into exact fp16 values in a swizzled shared-memory tile (each byte, biased
-// by 128, is placed in the mantissa of 1024 by a byte permute and 1152 is
-// subtracted, two codes per instruction), and runs the tensor-core tile step
-// with the query heads as the MMA columns (queries rounded to fp16); the K
-// scale of each row's block multiplies its scores, the V scale its weights.
-// The per-block attention decomposition is that of "KV Cache paging in LLM
-// inference" (intelliparadigm.com) s2.2.
+// group.  The per-block attention decomposition is that of "KV Cache paging
+// in LLM inference" (intelliparadigm.com) s2.2.
+//
+// A warp streams 16-token tiles of codes into its own ring, as tensor boxes
+// of 8 or 16 rows (block sizes that are multiples of 16, or 8) swizzled over
+// the row (128-byte swizzle for head_dim 128, 64-byte for 64), or, for other
+// block sizes, one row per lane (lanes 0-15 the K rows, 16-31 the V rows)
+// into rows padded to head_dim + 16 bytes; either layout keeps the fragment
+// loads below free of shared-memory bank conflicts (but for the V loads of
+// head_dim 64, two-way).  The codes go from the ring straight into MMA A
+// fragments, with no fp16 staging tile: each byte, biased by 128, is placed
+// in the mantissa of 1024 by a byte permute and 1152 is subtracted, which
+// gives the code exactly as fp16, two codes per instruction.  The contraction may visit head_dim in any
+// order, so the fragments are laid out to make every load a wide one:
+//   K step kk of S = K Q^T takes, in lane (gid, tig), the 4 consecutive codes
+//   at head_dim 16*(tig*CPT + kk/4) + 4*(kk%4) of tokens gid and gid + 8
+//   (CPT = head_dim / 64 chunks of 16 codes per lane and row), and the
+//   queries are packed in the same order;
+//   M tile mt of O^T = V^T P^T covers head_dim DPT*gid + 2*mt (row gid) and
+//   DPT*gid + 2*mt + 1 (row gid + 8), DPT = head_dim / 8, so a lane reads DPT
+//   consecutive codes of each of its 4 tokens.
+// The K scale of each row's block multiplies its scores and the V scale its
+// weights (the ROWSCALE tile step); queries are rounded to fp16.
 #include <math.h>
 
 #include "pa_device.cuh"
@@ -21,61 +36,89 @@
 
 namespace pa {
 
-constexpr int kI8TcWarps = 4;
-constexpr int kI8TcTableCap = 1024;
-#ifndef PA_I8TC_STAGES
-#define PA_I8TC_STAGES 2
+#ifndef PA_I8TC_WARPS
+#define PA_I8TC_WARPS 8
 #endif
-constexpr int kI8TcMinBlocks = PA_I8TC_STAGES <= 2 ? 3 : 2;
+#ifndef PA_I8TC_STAGES
+#define PA_I8TC_STAGES 2   // code tiles in flight per warp
+#endif
+constexpr int kI8TcWarps = PA_I8TC_WARPS;
+constexpr int kI8TcTableCap = 512;   // table entries (and their scales) staged per CTA
 
-template <int D>
+template <int D, bool BOXES>
 struct I8TcCfg {
-    static constexpr int CODE_BYTES = kTcTile * D;       // one tile of K (or V) codes
-    static constexpr int TILE_BYTES = kTcTile * D * 2;   // the same tile as fp16, swizzled
-    static constexpr int STAGES = D == 64 ? 2 * PA_I8TC_STAGES : PA_I8TC_STAGES;   // code tiles in flight per warp
+    static constexpr int ROW = BOXES ? D : D + 16;   // row of codes in the ring (padded without boxes)
+    static constexpr int SLOT = 2 * kTcTile * ROW;   // K then V rows of one tile (1024-byte multiple with boxes)
+    static constexpr int STAGES = PA_I8TC_STAGES;
     static constexpr int KSTEPS = D / 16;
     static constexpr int MT = D / 16;
-    static constexpr size_t kRing = (size_t)kI8TcWarps * STAGES * 2 * CODE_BYTES;
-    static constexpr size_t kStage = (size_t)kI8TcWarps * 2 * TILE_BYTES;
+    static constexpr int CPT = D / 64;               // 16-code K chunks per lane and row
+    static constexpr int DPT = D / 8;                // V codes per lane and token
+    static constexpr size_t kRing = (size_t)kI8TcWarps * STAGES * SLOT;
     static constexpr size_t kRedBytes = (size_t)kI8TcWarps * 16 * (D + 2) * 4;
-    static_assert(kRedBytes <= kRing + kStage, "the merge area reuses the tile buffers");
+    static constexpr size_t kArea = ((kRing > kRedBytes ? kRing : kRedBytes) + 15) & ~(size_t)15;
     static constexpr size_t kBars = (size_t)kI8TcWarps * STAGES * 8;
-    static constexpr size_t kFixed = kRing + kStage + kBars + 16;
+    static constexpr size_t kFixed = 1024 /*alignment slack*/ + kArea + kBars + 16;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 12; }   // ids, scale_K, scale_V
 };
 
-// 16 codes (one 16-byte chunk of a row) -> 16 exact fp16 values, written as
-// chunks 2*cc and 2*cc + 1 of row `row` of a swizzled tile.
-__device__ __forceinline__ void codes_to_f16_chunk(const uint4 &v, unsigned char *tile, int row, int cc) {
-    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-    const __half2 bias = __floats2half2_rn(1152.f, 1152.f);   // 1024 + 128
-    uint32_t h[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t lo = __byte_perm(w[i], 0x64646464u, 0x4140);   // 1024 + (c + 128), bytes 0 and 1
-        uint32_t hi = __byte_perm(w[i], 0x64646464u, 0x4342);   // bytes 2 and 3
-        __half2 a = __hsub2(*reinterpret_cast<__half2 *>(&lo), bias);
-        __half2 b = __hsub2(*reinterpret_cast<__half2 *>(&hi), bias);
-        h[2 * i] = *reinterpret_cast<uint32_t *>(&a);
-        h[2 * i + 1] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    *reinterpret_cast<uint4 *>(tile + swz(row, 2 * cc)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(tile + swz(row, 2 * cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+// Codes in bytes 0/1 (lo) or 2/3 (hi) of w, already biased by 128, as an
+// exact fp16 pair.
+__device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) {
+    uint32_t h = __byte_perm(w, 0x64646464u, 0x4140);   // 1024 + (c + 128)
+    __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&h), __floats2half2_rn(1152.f, 1152.f));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) {
+    uint32_t h = __byte_perm(w, 0x64646464u, 0x4342);
+    __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&h), __floats2half2_rn(1152.f, 1152.f));
+    return *reinterpret_cast<uint32_t *>(&r);
 }
 
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
-    decode_int8_tc_kernel(DecodeParams p, const float *kv_scales) {
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// DPT codes of one V token, as one 16-byte (head_dim 128) or 8-byte
+// (head_dim 64) load.
+template <int DPT>
+struct VCodes;
+template <>
+struct VCodes<16> {
+    uint4 v;
+    __device__ __forceinline__ void load(const unsigned char *p) { v = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ uint32_t word(int i) const { return word_of(v, i); }
+};
+template <>
+struct VCodes<8> {
+    uint2 v;
+    __device__ __forceinline__ void load(const unsigned char *p) { v = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ uint32_t word(int i) const { return i == 0 ? v.x : v.y; }
+};
+
+// Byte offset of 16-code chunk `c` of row `r` inside a K or V tile of the
+// ring (the tensor boxes' swizzle, or padded rows).
+template <int D, bool BOXES>
+__device__ __forceinline__ int code_off(int r, int c) {
+    if constexpr (!BOXES) return r * (D + 16) + (c << 4);
+    else if constexpr (D == 128) return r * 128 + ((c ^ (r & 7)) << 4);
+    else return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+template <typename T, int D, int NT, bool BOXES>
+__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
+    decode_int8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          DecodeParams p, const float *kv_scales, int box_rows) {
     grid_dependency_wait();
     allow_dependents();
-    using C = I8TcCfg<D>;
+    using C = I8TcCfg<D, BOXES>;
     constexpr int S = C::STAGES;
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *ring = smem;
-    unsigned char *stage = smem + C::kRing;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kRing + C::kStage);
-    int *flags = reinterpret_cast<int *>(smem + C::kRing + C::kStage + C::kBars);
-    int32_t *tbl = reinterpret_cast<int32_t *>(smem + C::kFixed);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // swizzled boxes need 1024-byte aligned destinations
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kArea);
+    int *flags = reinterpret_cast<int *>(smem + C::kArea + C::kBars);
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + C::kArea + C::kBars + 16);
     float *sk_tab = reinterpret_cast<float *>(tbl + p.table_cap);
     float *sv_tab = sk_tab + p.table_cap;
 
@@ -109,7 +152,13 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
     const int nblk = (len - 1) / p.bs + 1;
     const int ncache = min(nblk, p.table_cap);
     for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j];
-    if (threadIdx.x == 0) flags[0] = 0;
+    if (threadIdx.x == 0) {
+        flags[0] = 0;
+        if constexpr (BOXES) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+        }
+    }
     if (threadIdx.x < kI8TcWarps * S) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
     mbar_init_fence();
     __syncthreads();
@@ -129,45 +178,77 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
         const int32_t blk = trow[j];
         return good(blk) ? kv_scales[((int64_t)blk * 2 + kv) * p.Hkv + hk] : 0.f;
     };
+    unsigned char *wring = smem + (size_t)warp * S * C::SLOT;
 
-    // lane 0 fetches local tile k (codes of 16 tokens, one copy per block
-    // segment) into ring slot k % S
+    // Fetch local tile k into ring slot k % S (called by the whole warp).
+    // With boxes, lane 0 copies the tile's 8- or 16-row boxes of K and V;
+    // otherwise lane r < 16 copies K row r and lane 16 + r V row r.  Rows
+    // past the length are not fetched or belong to the last box: their codes
+    // are finite and get zero weight.
     auto issue = [&](int k) {
         const int t0 = (warp + k * kI8TcWarps) * kTcTile;
-        const int t1 = min(t0 + kTcTile, len);
+        if constexpr (BOXES) {
+            if (lane != 0) return;
+            const int slot = k % S;
+            const uint32_t bar = smem_u32(&bars[warp * S + slot]);
+            const uint32_t dst_k = smem_u32(wring + (size_t)slot * C::SLOT);
+            const uint32_t dst_v = dst_k + kTcTile * C::ROW;
+            const int subs = kTcTile / box_rows;
+            uint32_t nbytes = 0;
+            bool bad = false;
+            for (int sb = 0; sb < subs; ++sb) {
+                const int t = t0 + sb * box_rows;
+                if (t >= len) break;
+                if (good(lookup(blk_of(t)))) nbytes += (uint32_t)box_rows * D * 2;
+                else bad = true;
+            }
+            if (bad) {
+                flags[0] = 1;
+                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+            }
+            mbar_arrive_expect_tx(bar, nbytes);
+            for (int sb = 0; sb < subs; ++sb) {
+                const int t = t0 + sb * box_rows;
+                if (t >= len) break;
+                const int j = blk_of(t);
+                const int32_t blk = lookup(j);
+                if (!good(blk)) continue;
+                const int32_t y = blk * p.rows_per_block + hk * p.bs + (t - j * p.bs);
+                const uint32_t o = (uint32_t)(sb * box_rows * C::ROW);
+                tma_2d_g2s(dst_k + o, &kmap, 0, y, bar);
+                tma_2d_g2s(dst_v + o, &vmap, 0, y, bar);
+            }
+            return;
+        }
+        const int r = lane & 15, kv = lane >> 4;
+        const int t = t0 + r;
+        const bool live = t < len;
+        const int j = live ? blk_of(t) : 0;
+        const int32_t blk = live ? lookup(j) : -1;
+        const bool ok = live && good(blk);
+        const uint32_t nbytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, ok)) * D;
+        const bool bad = __any_sync(0xffffffffu, live && !ok);
         const int slot = k % S;
-        const uint32_t dst_k = smem_u32(ring + (size_t)((warp * S + slot) * 2) * C::CODE_BYTES);
-        const uint32_t dst_v = dst_k + C::CODE_BYTES;
         const uint32_t bar = smem_u32(&bars[warp * S + slot]);
-        uint32_t bytes = 0;
-        bool ok = true;
-        for (int t = t0, jj = blk_of(t0), e; t < t1; t = e, ++jj) {
-            e = min(t1, (jj + 1) * p.bs);
-            if (good(lookup(jj))) bytes += (uint32_t)(e - t) * D * 2;
-            else ok = false;
+        if (lane == 0) {
+            if (bad) {
+                flags[0] = 1;
+                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+            }
+            mbar_arrive_expect_tx(bar, nbytes);
         }
-        if (!ok) {
-            flags[0] = 1;
-            report(p.err_word, PA_DEVERR_BAD_BLOCK);
-        }
-        mbar_arrive_expect_tx(bar, bytes);
-        for (int t = t0, jj = blk_of(t0), e; t < t1; t = e, ++jj) {
-            e = min(t1, (jj + 1) * p.bs);
-            const int32_t blk = lookup(jj);
-            if (!good(blk)) continue;
-            const int64_t off = (int64_t)blk * p.block_stride_bytes + head_off + (int64_t)(t - jj * p.bs) * D;
-            const uint32_t n = (uint32_t)(e - t) * D;
-            const uint32_t so = (uint32_t)(t - t0) * D;
-            bulk_g2s(dst_k + so, p.k_pool + off, n, bar);
-            bulk_g2s(dst_v + so, p.v_pool + off, n, bar);
+        __syncwarp();
+        if (ok) {
+            const int64_t off = (int64_t)blk * p.block_stride_bytes + head_off + (int64_t)(t - j * p.bs) * D;
+            bulk_g2s(smem_u32(wring + (size_t)slot * C::SLOT + (size_t)(kv * kTcTile + r) * C::ROW),
+                     (kv ? p.v_pool : p.k_pool) + off, D, bar);
         }
     };
 
-    if (lane == 0)
-        for (int k = 0; k < min(S, my_tiles); ++k) issue(k);
+    for (int k = 0; k < min(S, my_tiles); ++k) issue(k);
 
-    // Q^T as fp16 MMA B fragments: column gid of head tile nt is head
-    // h0 + nt*8 + gid (zero past nh)
+    // Q^T as fp16 MMA B fragments in the K-step order above: column gid of
+    // head tile nt is head h0 + nt*8 + gid (zero past nh)
     uint32_t qb[C::KSTEPS][NT][2];
     {
         const T *qp = reinterpret_cast<const T *>(p.q);
@@ -177,11 +258,13 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
             const int64_t row = ((int64_t)b * p.H + h0 + (live ? nt * 8 + gid : 0)) * D;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                const int c0 = kk * 16 + 2 * tig;
-                __half2 a = __floats2half2_rn(Elem<T>::to_float(qp[row + c0]), Elem<T>::to_float(qp[row + c0 + 1]));
-                __half2 bq = __floats2half2_rn(Elem<T>::to_float(qp[row + c0 + 8]), Elem<T>::to_float(qp[row + c0 + 9]));
-                qb[kk][nt][0] = live ? *reinterpret_cast<uint32_t *>(&a) : 0u;
-                qb[kk][nt][1] = live ? *reinterpret_cast<uint32_t *>(&bq) : 0u;
+                const int d = 16 * (tig * C::CPT + kk / 4) + 4 * (kk % 4);
+                const __half2 lo =
+                    __floats2half2_rn(Elem<T>::to_float(qp[row + d]), Elem<T>::to_float(qp[row + d + 1]));
+                const __half2 hi =
+                    __floats2half2_rn(Elem<T>::to_float(qp[row + d + 2]), Elem<T>::to_float(qp[row + d + 3]));
+                qb[kk][nt][0] = live ? *reinterpret_cast<const uint32_t *>(&lo) : 0u;
+                qb[kk][nt][1] = live ? *reinterpret_cast<const uint32_t *>(&hi) : 0u;
             }
         }
     }
@@ -201,9 +284,6 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
             m_run[nt][j] = -INFINITY;
             l_run[nt][j] = 0.f;
         }
-    unsigned char *ks16 = stage + (size_t)warp * 2 * C::TILE_BYTES;
-    unsigned char *vs16 = ks16 + C::TILE_BYTES;
-    constexpr int kChunks = kTcTile * (D / 16);   // 16-code chunks per tile
 
     int k = 0;
     bool aborted = false;
@@ -213,27 +293,51 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
             aborted = true;
             break;
         }
-        const unsigned char *kc = ring + (size_t)((warp * S + slot) * 2) * C::CODE_BYTES;
-        const unsigned char *vc = kc + C::CODE_BYTES;
-        const int t0 = (warp + k * kI8TcWarps) * kTcTile;
-        const int nvalid = min(kTcTile, len - t0);
-        // codes -> fp16 tiles (rows past the valid length hold stale but
-        // finite values: their weight is 0)
-        for (int i = lane; i < kChunks; i += 32) {
-            const int row = i / (D / 16), cc = i % (D / 16);
-            codes_to_f16_chunk(*reinterpret_cast<const uint4 *>(kc + row * D + cc * 16), ks16, row, cc);
-            codes_to_f16_chunk(*reinterpret_cast<const uint4 *>(vc + row * D + cc * 16), vs16, row, cc);
-        }
-        __syncwarp();
-        // the code ring slot is free again: fetch the tile after next
+        const unsigned char *kc = wring + (size_t)slot * C::SLOT;
+        const unsigned char *vc = kc + kTcTile * C::ROW;
+        // this lane's codes: K rows gid and gid + 8 (CPT chunks each), V
+        // tokens 2tig, 2tig + 1, 2tig + 8, 2tig + 9 (DPT codes each)
+        uint4 kw[2][C::CPT];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int q = 0; q < C::CPT; ++q)
+                kw[rr][q] = *reinterpret_cast<const uint4 *>(kc + code_off<D, BOXES>(gid + 8 * rr, tig * C::CPT + q));
+        VCodes<C::DPT> vw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            vw[i].load(vc + code_off<D, BOXES>(2 * tig + (i & 1) + 8 * (i >> 1), C::DPT * gid / 16) +
+                       (C::DPT * gid) % 16);
+        // the ring slot is free again: fetch the tile after next
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && k + S < my_tiles) issue(k + S);
+        if (k + S < my_tiles) issue(k + S);
+
+        const int t0 = (warp + k * kI8TcWarps) * kTcTile;
+        const int nvalid = min(kTcTile, len - t0);
         const int j0r = blk_of(t0 + min(gid, nvalid - 1)), j1r = blk_of(t0 + min(gid + 8, nvalid - 1));
-        tc_tile_step<__half, D, NT, true>(smem_u32(ks16), smem_u32(vs16), 0, nvalid, qb, p.scale_log2, o_acc,
-                                          m_run, l_run, lane, make_float2(scale_of(j0r, 0), scale_of(j1r, 0)),
-                                          make_float2(scale_of(j0r, 1), scale_of(j1r, 1)));
-        __syncwarp();
+        tc_tile_step_frags<__half, D, NT, true>(
+            [&](int kk, uint32_t(&a)[4]) {
+                const uint32_t w0 = word_of(kw[0][kk / 4], kk % 4) ^ 0x80808080u;   // token gid
+                const uint32_t w1 = word_of(kw[1][kk / 4], kk % 4) ^ 0x80808080u;   // token gid + 8
+                a[0] = codes_lo_f16x2(w0);
+                a[1] = codes_lo_f16x2(w1);
+                a[2] = codes_hi_f16x2(w0);
+                a[3] = codes_hi_f16x2(w1);
+            },
+            [&](int mt, uint32_t(&a)[4]) {
+                // bytes 2mt and 2mt + 1 of each token's DPT codes, tokens
+                // (2tig, 2tig + 1) and (2tig + 8, 2tig + 9) interleaved
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t u01 = __byte_perm(vw[0].word(mt / 2), vw[1].word(mt / 2), sel) ^ 0x80808080u;
+                const uint32_t u23 = __byte_perm(vw[2].word(mt / 2), vw[3].word(mt / 2), sel) ^ 0x80808080u;
+                a[0] = codes_lo_f16x2(u01);   // row gid: head_dim DPT*gid + 2mt
+                a[1] = codes_hi_f16x2(u01);   // row gid + 8: head_dim DPT*gid + 2mt + 1
+                a[2] = codes_lo_f16x2(u23);
+                a[3] = codes_hi_f16x2(u23);
+            },
+            0, nvalid, qb, p.scale_log2, o_acc, m_run, l_run, lane,
+            make_float2(scale_of(j0r, 0), scale_of(j1r, 0)), make_float2(scale_of(j0r, 1), scale_of(j1r, 1)));
     }
     if (aborted) {
         if (lane == 0) {
@@ -253,7 +357,7 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
             l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], 16);
         }
 
-    // merge the warps through shared memory (reusing the tile buffers)
+    // merge the warps through shared memory (reusing the ring)
     __syncthreads();
     float *red_o = reinterpret_cast<float *>(smem);   // [W][16 heads][D]
     float *red_m = red_o + kI8TcWarps * 16 * D;       // [W][16]
@@ -265,7 +369,7 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hh = nt * 8 + 2 * tig + (e & 1);
-                const int d = mt * 16 + gid + (e >> 1) * 8;
+                const int d = C::DPT * gid + 2 * mt + (e >> 1);
                 red_o[(warp * 16 + hh) * D + d] = o_acc[mt][nt][e];
             }
     if (gid == 0) {
@@ -295,31 +399,42 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, kI8TcMinBlocks)
     }
 }
 
-template <typename T, int D, int NT>
-static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_scales, cudaStream_t stream) {
+template <typename T, int D, int NT, bool BOXES>
+static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_scales, const CUtensorMap &kmap,
+                                   const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
     DecodeParams p = params;
     p.table_cap = min(p.table_cap, kI8TcTableCap);
-    const size_t smem = I8TcCfg<D>::bytes(p.table_cap);
-    auto kern = decode_int8_tc_kernel<T, D, NT>;
+    const size_t smem = I8TcCfg<D, BOXES>::bytes(p.table_cap);
+    auto kern = decode_int8_tc_kernel<T, D, NT, BOXES>;
     static int configured[64] = {};   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;
     const int64_t grid = (int64_t)p.B * p.Hkv * ((g + 15) / 16);
     if (grid == 0) return cudaSuccess;
-    return launch_clustered(kern, grid, kI8TcWarps * 32, smem, 1, stream, p, kv_scales);
+    return launch_clustered(kern, grid, kI8TcWarps * 32, smem, 1, stream, kmap, vmap, p, kv_scales, box_rows);
+}
+
+template <typename T, int D, int NT>
+static cudaError_t launch_int8_tc_b(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
+                                    const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
+    if (kmap != nullptr && vmap != nullptr)
+        return launch_int8_tc_t<T, D, NT, true>(p, kv_scales, *kmap, *vmap, box_rows, stream);
+    const CUtensorMap none{};
+    return launch_int8_tc_t<T, D, NT, false>(p, kv_scales, none, none, box_rows, stream);
 }
 
 template <typename T>
-static cudaError_t launch_int8_tc_d(const DecodeParams &p, const float *kv_scales, cudaStream_t stream) {
+static cudaError_t launch_int8_tc_d(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
+                                    const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
     const bool one = p.H / p.Hkv <= 8;
     switch (p.D) {
         case 64:
-            return one ? launch_int8_tc_t<T, 64, 1>(p, kv_scales, stream)
-                       : launch_int8_tc_t<T, 64, 2>(p, kv_scales, stream);
+            return one ? launch_int8_tc_b<T, 64, 1>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 64, 2>(p, kv_scales, kmap, vmap, box_rows, stream);
         case 128:
-            return one ? launch_int8_tc_t<T, 128, 1>(p, kv_scales, stream)
-                       : launch_int8_tc_t<T, 128, 2>(p, kv_scales, stream);
+            return one ? launch_int8_tc_b<T, 128, 1>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 128, 2>(p, kv_scales, kmap, vmap, box_rows, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -329,9 +444,10 @@ bool int8_tc_supported(int dtype, int head_dim) {
 }
 
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                  const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16>(p, kv_scales, stream);
-    if (dtype == PA_F16) return launch_int8_tc_d<__half>(p, kv_scales, stream);
+    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16>(p, kv_scales, kmap, vmap, box_rows, stream);
+    if (dtype == PA_F16) return launch_int8_tc_d<__half>(p, kv_scales, kmap, vmap, box_rows, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -231,7 +231,10 @@ cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv
                                int head_dim, cudaStream_t stream);
 // grouped-query shapes of the int8 cache on the tensor cores
 bool int8_tc_supported(int dtype, int head_dim);
+// kmap/vmap: tensor maps of the int8 pools (boxes of box_rows rows, see
+// api.cu), or null to copy the tiles row by row (any block size).
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                  const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream);
 
 // Load-balanced persistent decode (final mode; plain, fused append or sliding

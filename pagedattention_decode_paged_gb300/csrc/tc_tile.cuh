@@ -35,13 +35,17 @@ __device__ __forceinline__ void tc_zero_v_rows(unsigned char *vs, int r0, int r1
 // One 16-token tile of grouped-query attention on the tensor cores:
 //     S^T[t][h] = sum_d K[t][d] Q[h][d]      (tokens x heads, reduced over D)
 //     O^T[d][h] += sum_t V[t][d] P^T[t][h]   (D x heads, reduced over tokens)
-// with the online softmax down each head column in the log2 domain.  ks_u /
-// vs_u address the tile's swizzled K and V (swz layout); rows outside
-// [lo, nvalid) get zero weight, and their V rows must hold finite values
-// (tc_zero_v_rows) so that 0 * V stays 0 inside the MMA.  qb holds Q^T as
-// MMA B fragments (column gid of head tile nt = head nt*8 + gid).
-// Accumulator layout: o_acc[mt][nt] regs 0/1 = head_dim row mt*16 + gid,
-// regs 2/3 = row + 8; even/odd = head column 2*tig / 2*tig + 1 of head tile
+// with the online softmax down each head column in the log2 domain.  The
+// operands come from two callables: kfrag(kk, a) yields the MMA A fragment
+// of K for K step kk (16 tokens x 16 head_dim entries), vfrag(mt, a) the A
+// fragment of V^T for M tile mt (16 head_dim rows x 16 tokens).  Which
+// head_dim entries a K step or an M tile covers is up to the caller, as
+// long as qb (Q^T as MMA B fragments: column gid of head tile nt = head
+// nt*8 + gid) uses the same K-step order and the caller reads o_acc rows in
+// its M-tile order.  Rows outside [lo, nvalid) get zero weight, and the V
+// values of those rows must be finite so that 0 * V stays 0 inside the MMA.
+// Accumulator layout: o_acc[mt][nt] regs 0/1 = row gid of M tile mt, regs
+// 2/3 = row gid + 8; even/odd = head column 2*tig / 2*tig + 1 of head tile
 // nt; m_run / l_run[nt][j] belong to head column nt*8 + 2*tig + j, and
 // l_run is this lane's share of the column sum (complete it over the 8 lanes
 // of a column group before use).
@@ -49,21 +53,16 @@ __device__ __forceinline__ void tc_zero_v_rows(unsigned char *vs, int r0, int r1
 // times row_k.x (row_k.y) and of V times row_v.x (row_v.y): the scores are
 // multiplied by the K factor, and the weights that meet V by the V factor
 // (the running sum keeps the weights themselves).
-template <typename T, int D, int NT, bool ROWSCALE = false>
-__device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int lo, int nvalid,
-                                             const uint32_t (&qb)[D / 16][NT][2], float scale_log2,
-                                             float (&o_acc)[D / 16][NT][4], float (&m_run)[NT][2],
-                                             float (&l_run)[NT][2], int lane,
-                                             float2 row_k = make_float2(1.f, 1.f),
-                                             float2 row_v = make_float2(1.f, 1.f)) {
+template <typename T, int D, int NT, bool ROWSCALE, typename KFrag, typename VFrag>
+__device__ __forceinline__ void tc_tile_step_frags(const KFrag &kfrag, const VFrag &vfrag, int lo, int nvalid,
+                                                   const uint32_t (&qb)[D / 16][NT][2], float scale_log2,
+                                                   float (&o_acc)[D / 16][NT][4], float (&m_run)[NT][2],
+                                                   float (&l_run)[NT][2], int lane, float2 row_k,
+                                                   float2 row_v) {
     constexpr int KSTEPS = D / 16;   // MMA K steps of K.Q^T
     constexpr int MT = D / 16;       // MMA M tiles of V^T.P^T
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
     const int gid = lane >> 2;
-    // ldmatrix lane roles (x4: lanes 8i..8i+7 address the rows of matrix i)
-    const int mi = lane >> 3, ri = lane & 7;
-    const int a_tok = (mi & 1) * 8 + ri, a_chunk = mi >> 1;  // K: {t0-7,t8-15} x {d lo, d hi}
-    const int v_tok = (mi >> 1) * 8 + ri, v_chunk = mi & 1;  // V^T: {d lo, d hi} x {t0-7,t8-15}
 
     // S^T = K Q^T: rows = tokens 0-15 of the tile, columns = heads
     float s[NT][4];
@@ -74,7 +73,7 @@ __device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int l
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
         uint32_t a[4];
-        ldsm_x4(ks_u + swz(a_tok, 2 * kk + a_chunk), a[0], a[1], a[2], a[3]);
+        kfrag(kk, a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(s[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
     }
@@ -148,17 +147,39 @@ __device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int l
         }
     }
 
-    // O^T += V^T P^T, one 16-row slab of head_dim per ldmatrix
+    // O^T += V^T P^T, one 16-row slab of head_dim per M tile
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         uint32_t a[4];
-        ldsm_x4_trans(vs_u + swz(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
+        vfrag(mt, a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             MmaOp<T>::run(o_acc[mt][nt], a, bhi[nt][0], bhi[nt][1]);
             if constexpr (kSplitP) MmaOp<T>::run(o_acc[mt][nt], a, blo[nt][0], blo[nt][1]);
         }
     }
+}
+
+// The tile step over a tile in shared memory in the swz layout (ks_u / vs_u:
+// the tile's K and V); K step kk covers head_dim 16*kk..16*kk+15 and M tile
+// mt head_dim rows 16*mt..16*mt+15, in order.
+template <typename T, int D, int NT, bool ROWSCALE = false>
+__device__ __forceinline__ void tc_tile_step(uint32_t ks_u, uint32_t vs_u, int lo, int nvalid,
+                                             const uint32_t (&qb)[D / 16][NT][2], float scale_log2,
+                                             float (&o_acc)[D / 16][NT][4], float (&m_run)[NT][2],
+                                             float (&l_run)[NT][2], int lane,
+                                             float2 row_k = make_float2(1.f, 1.f),
+                                             float2 row_v = make_float2(1.f, 1.f)) {
+    // ldmatrix lane roles (x4: lanes 8i..8i+7 address the rows of matrix i)
+    const int mi = lane >> 3, ri = lane & 7;
+    const int a_tok = (mi & 1) * 8 + ri, a_chunk = mi >> 1;  // K: {t0-7,t8-15} x {d lo, d hi}
+    const int v_tok = (mi >> 1) * 8 + ri, v_chunk = mi & 1;  // V^T: {d lo, d hi} x {t0-7,t8-15}
+    tc_tile_step_frags<T, D, NT, ROWSCALE>(
+        [&](int kk, uint32_t(&a)[4]) { ldsm_x4(ks_u + swz(a_tok, 2 * kk + a_chunk), a[0], a[1], a[2], a[3]); },
+        [&](int mt, uint32_t(&a)[4]) {
+            ldsm_x4_trans(vs_u + swz(v_tok, 2 * mt + v_chunk), a[0], a[1], a[2], a[3]);
+        },
+        lo, nvalid, qb, scale_log2, o_acc, m_run, l_run, lane, row_k, row_v);
 }
 
 }  // namespace pa

@@ -99,13 +99,24 @@ def test_int8_block_sizes(bs):
 
 @pytest.mark.parametrize("H,Hkv,dtype,D,bs", [(8, 2, BF16, 128, 16), (16, 1, BF16, 128, 16),
                                               (64, 8, BF16, 128, 16), (48, 2, F16, 128, 16),
-                                              (16, 2, F16, 64, 8), (8, 2, BF16, 128, 3),
-                                              (8, 2, F32, 128, 16)])
+                                              (16, 2, F16, 64, 8), (8, 1, F16, 64, 16),
+                                              (8, 2, BF16, 128, 3), (8, 2, F32, 128, 16)])
 def test_int8_grouped_query(H, Hkv, dtype, D, bs):
     """Tensor-core int8 path (16-bit queries, head_dim 64/128, any block
     size) and the CUDA-core one for fp32 queries."""
     w = workloads.to_int8(workloads.make_generic(B=len(LENS), H=H, Hkv=Hkv, D=D, bs=bs, dtype=dtype,
                                                  lens=LENS, seed=H + bs, poison=False), seed=H)
+    run_step8(w)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_int8_grouped_query_long_sequences(D):
+    """Sequences with more blocks than the tensor-core kernel stages in
+    shared memory (the rest of the table and its scales come from global
+    memory)."""
+    lens = [9000, 17, 8200]
+    w = workloads.to_int8(workloads.make_generic(B=len(lens), H=8, Hkv=2, D=D, bs=16, dtype=BF16,
+                                                 lens=lens, seed=D + 1, poison=False), seed=D)
     run_step8(w)
 
 
