@@ -494,6 +494,12 @@ def run_gpu(args) -> None:
     else:
         decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
         append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
+    # spread of the bracketed decode launches: p10 / median / p90 (us)
+    dsamples = sorted(e[1].elapsed_time(e[2]) * 1e3 for e in ev.values()) if graph is None else []
+    dspread = ({"p10": round(dsamples[len(dsamples) // 10], 3),
+                "median": round(statistics.median(dsamples), 3),
+                "p90": round(dsamples[(9 * len(dsamples)) // 10], 3), "samples": len(dsamples)}
+               if dsamples else None)
     total_ms = max_over_ranks(total_ms, dist, dev)
 
     # end to end through the C ABI with host buffers: H2D of the step's
@@ -565,6 +571,7 @@ def run_gpu(args) -> None:
             "tokens_per_s": round(world * w.B / (ms_step * 1e-3), 1),
             "us_per_layer_step": round(ms_step * 1e3, 3),
             "decode_us": round(decode_ms * 1e3, 3), "append_us": round(append_ms * 1e3, 3),
+            "decode_us_spread": dspread,
             "decode_bytes": dbytes, "kernel_bytes": kbytes,
             "logical_kv_bytes": logical_kv_bytes(w, lens_after),
             "decode_path": kernel, "fused_append": fused, "cuda_graph_steps": args.graph or None,
@@ -592,8 +599,10 @@ def run_gpu(args) -> None:
 # the CPU oracle, timed on the host cores
 # ---------------------------------------------------------------------------
 
-def _oracle_sample(w, lens_after, seqs):
-    """Oracle decode of the sequences `seqs` (all heads); returns bytes read."""
+def _oracle_sample(w, lens_after, seqs, threads=None):
+    """Oracle decode of the sequences `seqs` (all heads) on `threads` host
+    threads (default: every core); returns bytes read and seconds."""
+    threads = threads or os.cpu_count() or 1
     import oracle
     sub = torch.tensor(seqs, dtype=torch.long)
     q = w.q.index_select(0, sub).contiguous()
@@ -604,11 +613,11 @@ def _oracle_sample(w, lens_after, seqs):
     if getattr(w, "scales", None) is not None:
         oracle.attention_decode_i8(q, flat, flat[w.v_offset:], w.scales, table, lens, w.scale,
                                    num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
-                                   num_blocks=w.NB, threads=os.cpu_count() or 1)
+                                   num_blocks=w.NB, threads=threads)
     else:
         oracle.attention_decode(q, flat, flat[w.v_offset:], table, lens, w.scale,
                                 num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
-                                num_blocks=w.NB, threads=os.cpu_count() or 1)
+                                num_blocks=w.NB, threads=threads)
     dt = time.perf_counter() - t
     s = w.pool.element_size()
     sq = w.q.element_size()
@@ -618,18 +627,23 @@ def _oracle_sample(w, lens_after, seqs):
 
 
 def cpu_baseline(w, lens_after, budget_s=10.0) -> dict:
-    done_bytes, done_s, seqs = 0, 0.0, 0
-    b = 0
-    while done_s < budget_s:
-        nbytes, dt = _oracle_sample(w, lens_after, [b % w.B])
-        done_bytes += nbytes
-        done_s += dt
-        seqs += 1
-        b += 1
-    return {"value": round(done_bytes / done_s / 1e9, 4), "unit": UNIT,
+    def run(threads, budget):
+        done_bytes, done_s, seqs = 0, 0.0, 0
+        while done_s < budget:
+            nbytes, dt = _oracle_sample(w, lens_after, [seqs % w.B], threads)
+            done_bytes += nbytes
+            done_s += dt
+            seqs += 1
+        return done_bytes / done_s / 1e9, seqs, done_s
+
+    value, seqs, done_s = run(os.cpu_count() or 1, budget_s)
+    value1, seqs1, done1 = run(1, budget_s / 4)
+    return {"value": round(value, 4), "unit": UNIT,
             "cores": os.cpu_count() or 1, "kind": "oracle",
+            "value_1_thread": round(value1, 4),
             "sample": f"{seqs} sequence decodes (all {w.H} heads each) of the same workload, "
-                      f"fp64 C oracle with OpenMP over (sequence, kv head), {done_s:.1f} s"}
+                      f"fp64 C oracle with OpenMP over (sequence, kv head), {done_s:.1f} s; "
+                      f"one thread: {seqs1} decodes, {done1:.1f} s"}
 
 
 def run_reference(args) -> None:
