@@ -32,7 +32,10 @@
 
 namespace pa {
 
-constexpr int kI8Warps = 4;
+#ifndef PA_I8_WARPS
+#define PA_I8_WARPS 3
+#endif
+constexpr int kI8Warps = PA_I8_WARPS;
 constexpr int kI8Stages = 2;
 constexpr int kI8TableCap = 1024;   // table entries (and scales) staged per CTA
 
@@ -65,7 +68,7 @@ struct I8Smem {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kI8Warps * 32, 3) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
+__global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
     grid_dependency_wait();
     allow_dependents();
     using C = I8Cfg<D>;

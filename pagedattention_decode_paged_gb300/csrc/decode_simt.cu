@@ -32,13 +32,15 @@
 
 namespace pa {
 
-// Tiles in flight per warp.  Two stages keep the CTA at 72 KB of shared
-// memory so three CTAs (12 warps) share an SM.
+// Tiles in flight per warp, and warps per CTA.  Two stages of 3 warps keep
+// the CTA at about 54 KB of shared memory, so four CTAs (12 warps) share an
+// SM; three warps per unit (rather than four) shorten the per-CTA start and
+// merge on short sequences and make the last wave of a launch finer.
 #ifndef PA_SIMT_STAGES
 #define PA_SIMT_STAGES 2
 #endif
 #ifndef PA_SIMT_WARPS
-#define PA_SIMT_WARPS 4
+#define PA_SIMT_WARPS 3
 #endif
 constexpr int kSimtWarps = PA_SIMT_WARPS;
 constexpr int kSimtStages = PA_SIMT_STAGES;
