@@ -171,15 +171,8 @@ pa::DecodeParams base_params(const pa_shape *s, const void *q, const void *k_poo
 }
 
 [[maybe_unused]] int sm_count() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
+    int n = 0;
+    return pa::device_sm_count(&n) == cudaSuccess ? n : 0;
 }
 
 // CTAs per work unit for the single-pass decode.  When the launch has fewer

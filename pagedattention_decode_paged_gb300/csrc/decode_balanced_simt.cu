@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kBalWarps * 32, kBalSimtMinBlocks)
 
 template <typename T, int D>
 struct BalSimtLaunch {
-    static int configured[64];
+    static std::atomic<int> configured[64];
     static int64_t occupancy[64][2];
 
     static cudaError_t plan(int batch, int64_t max_tiles_total, BalancedPlan *plan) {
@@ -339,7 +339,7 @@ struct BalSimtLaunch {
                                 1, stream, p);
     }
 };
-template <typename T, int D> int BalSimtLaunch<T, D>::configured[64] = {};
+template <typename T, int D> std::atomic<int> BalSimtLaunch<T, D>::configured[64];
 template <typename T, int D> int64_t BalSimtLaunch<T, D>::occupancy[64][2] = {};
 
 // Run F<T, D> for the (dtype, head_dim) pair; cudaErrorInvalidValue if the

@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kBalWarps * 32, 2)
 
 template <typename T, int D, int NT>
 struct BalTcLaunch {
-    static int configured[64];
+    static std::atomic<int> configured[64];
     static int64_t occupancy[64][2];
 
     static cudaError_t plan(int batch, int64_t max_tiles_total, BalancedPlan *plan) {
@@ -489,7 +489,7 @@ struct BalTcLaunch {
                                 stream, kmap, vmap, p, box_rows);
     }
 };
-template <typename T, int D, int NT> int BalTcLaunch<T, D, NT>::configured[64] = {};
+template <typename T, int D, int NT> std::atomic<int> BalTcLaunch<T, D, NT>::configured[64];
 template <typename T, int D, int NT> int64_t BalTcLaunch<T, D, NT>::occupancy[64][2] = {};
 
 // Run F<T, D, NT> for (dtype, head_dim, group); cudaErrorInvalidValue when

@@ -414,7 +414,7 @@ static cudaError_t launch_tc_t(const DecodeParams &params, const CUtensorMap &km
     p.table_cap = min(p.table_cap, kTcTableCap);
     const size_t smem = TcCfg<D>::bytes(p.table_cap);
     auto kern = decode_gqa_tc_kernel<T, D, NT, SPLIT>;
-    static int configured[64] = {};   // per template instance of this launcher
+    static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;

@@ -419,7 +419,7 @@ static cudaError_t launch_int8_t(const DecodeParams &params, const float *kv_sca
     p.table_cap = min(p.table_cap, kI8TableCap);
     const size_t smem = I8Smem<D>::bytes(p.table_cap);
     auto kern = decode_int8_kernel<T, D>;
-    static int configured[64] = {};   // per template instance of this launcher
+    static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)p.B * p.H;

@@ -406,7 +406,7 @@ static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_
     p.table_cap = min(p.table_cap, kI8TcTableCap);
     const size_t smem = I8TcCfg<D, BOXES>::bytes(p.table_cap);
     auto kern = decode_int8_tc_kernel<T, D, NT, BOXES>;
-    static int configured[64] = {};   // per template instance of this launcher
+    static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;

@@ -314,7 +314,7 @@ static cudaError_t launch_prefix_t(const DecodeParams &params, const CUtensorMap
     p.table_cap = min(p.table_cap, 1024);
     const size_t smem = PfxCfg<D>::bytes(p.table_cap);
     auto kern = decode_prefix_tc_kernel<T, D, NT>;
-    static int configured[64] = {};   // per template instance of this launcher
+    static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     int64_t grid = 0;

@@ -390,7 +390,7 @@ static cudaError_t launch_simt_t(const DecodeParams &params, cudaStream_t stream
     p.table_cap = min(p.table_cap, kSimtTableCap);
     const size_t smem = SimtSmem<T, D>::bytes(p.table_cap);
     auto kern = decode_simt_kernel<T, D, SPLIT>;
-    static int configured[64] = {};   // per template instance of this launcher
+    static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
     const int cluster = SPLIT ? 1 : max(1, p.cluster);

@@ -2,6 +2,8 @@
 // the C-ABI layer (api.cu) and the kernel translation units.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -121,29 +123,34 @@ struct ReduceParams {
 // kernels of one signature share a function-pointer type, so the record
 // cannot live in this template.
 template <typename Kern>
-inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, int (&configured)[64]) {
+inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, std::atomic<int> (&configured)[64]) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && configured[dev] >= (int)bytes) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && configured[dev].load(std::memory_order_relaxed) >= (int)bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess && dev >= 0 && dev < 64 && configured[dev] < (int)bytes)
-        configured[dev] = (int)bytes;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) {
+        int cur = configured[dev].load(std::memory_order_relaxed);
+        while (cur < (int)bytes && !configured[dev].compare_exchange_weak(cur, (int)bytes)) {
+        }
+    }
     return e;
 }
 
 // Number of SMs of the current device (cached per device).
 inline cudaError_t device_sm_count(int *count) {
-    static int counts[64] = {};
+    static std::atomic<int> counts[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (counts[dev] == 0) {
-        e = cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        counts[dev].store(n, std::memory_order_relaxed);
     }
-    *count = counts[dev];
+    *count = n;
     return cudaSuccess;
 }
 
