@@ -359,10 +359,14 @@ def run_gpu(args) -> None:
         fused = False
     kflat, vflat = w.k_flat(), w.v_flat()
 
-    def make_calls(prepared: bool):
-        """The step's C-ABI calls.  Prepared calls marshal their arguments
-        once (a serving loop reuses its buffers every step) and are bound to
-        the bench stream; graph capture needs calls on the capture stream."""
+    def make_calls(prepared: bool, t=None):
+        """The step's C-ABI calls on the tensors `t` (default: the workload's
+        own q, k_new, v_new, block_table, positions, lens_after and out).
+        Prepared calls marshal their arguments once (a serving loop reuses
+        its buffers every step) and are bound to the bench stream; graph
+        capture needs calls on the capture stream."""
+        t = t or dict(q=w.q, k_new=w.k_new, v_new=w.v_new, block_table=w.block_table,
+                      positions=positions, lens_after=lens_after, out=out)
         o = dict(err_word=err, prepare=prepared,
                  stream=stream.cuda_stream if prepared else None)
 
@@ -376,45 +380,45 @@ def run_gpu(args) -> None:
                               w.block_table, prefill["start"], w.lens, **kw))
             return calls, []
         if args.shared_prefix:
-            calls.append(bind(pa.paged_attention_decode_shared_prefix, out, w.q, kflat, vflat,
-                              w.block_table, lens_after, w.scale, ptok, ws,
+            calls.append(bind(pa.paged_attention_decode_shared_prefix, t["out"], t["q"], kflat, vflat,
+                              t["block_table"], t["lens_after"], w.scale, ptok, ws,
                               group_first=groups["first"], shared_tokens=groups["shared"],
                               num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table,
-                                positions, **kw)]
+            return calls, [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
+                                t["positions"], **kw)]
         if args.int8:
-            calls.append(bind(pa.paged_attention_decode_int8, out, w.q, kflat, vflat, w.scales,
-                              w.block_table, lens_after, w.scale, num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append_int8, w.k_new, w.v_new, kflat, vflat, w.scales,
-                                w.block_table, positions, **kw)]
+            calls.append(bind(pa.paged_attention_decode_int8, t["out"], t["q"], kflat, vflat, w.scales,
+                              t["block_table"], t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
+            return calls, [bind(pa.paged_kv_append_int8, t["k_new"], t["v_new"], kflat, vflat, w.scales,
+                                t["block_table"], t["positions"], **kw)]
         if balanced:
             if fused:
-                calls.append(bind(pa.paged_attention_decode_balanced, out, w.q, kflat, vflat,
-                                  w.block_table, w.scale, bws, positions=positions, k_new=w.k_new,
-                                  v_new=w.v_new, window=window, num_kv_heads=w.Hkv, **kw))
+                calls.append(bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
+                                  t["block_table"], w.scale, bws, positions=t["positions"], k_new=t["k_new"],
+                                  v_new=t["v_new"], window=window, num_kv_heads=w.Hkv, **kw))
                 return calls, []
-            calls.append(bind(pa.paged_attention_decode_balanced, out, w.q, kflat, vflat,
-                              w.block_table, w.scale, bws, seq_lens=lens_after, window=window,
+            calls.append(bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
+                              t["block_table"], w.scale, bws, seq_lens=t["lens_after"], window=window,
                               num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table,
-                                positions, **kw)]
+            return calls, [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
+                                t["positions"], **kw)]
         if fused:
-            calls.append(bind(pa.paged_attention_decode_append, out, w.q, w.k_new, w.v_new, kflat,
-                              vflat, w.block_table, positions, w.scale, num_kv_heads=w.Hkv, **kw))
+            calls.append(bind(pa.paged_attention_decode_append, t["out"], t["q"], t["k_new"], t["v_new"], kflat,
+                              vflat, t["block_table"], t["positions"], w.scale, num_kv_heads=w.Hkv, **kw))
             return calls, []
-        app = [bind(pa.paged_kv_append, w.k_new, w.v_new, kflat, vflat, w.block_table, positions,
+        app = [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"], t["positions"],
                     **kw)]
         if window:
-            calls.append(bind(pa.paged_attention_decode_window, out, w.q, kflat, vflat,
-                              w.block_table, lens_after, w.scale, window, num_kv_heads=w.Hkv, **kw))
+            calls.append(bind(pa.paged_attention_decode_window, t["out"], t["q"], kflat, vflat,
+                              t["block_table"], t["lens_after"], w.scale, window, num_kv_heads=w.Hkv, **kw))
         elif ptok:
-            calls.append(bind(pa.paged_attention_decode_partial, w.q, kflat, vflat, w.block_table,
-                              lens_after, w.scale, ptok, ws, num_kv_heads=w.Hkv, **kw))
-            calls.append(bind(pa.paged_attention_decode_reduce, out, ws, lens_after, ptok,
+            calls.append(bind(pa.paged_attention_decode_partial, t["q"], kflat, vflat, t["block_table"],
+                              t["lens_after"], w.scale, ptok, ws, num_kv_heads=w.Hkv, **kw))
+            calls.append(bind(pa.paged_attention_decode_reduce, t["out"], ws, t["lens_after"], ptok,
                               num_kv_heads=w.Hkv, max_blocks_per_seq=w.MB, **kw))
         else:
-            calls.append(bind(pa.paged_attention_decode, out, w.q, kflat, vflat, w.block_table,
-                              lens_after, w.scale, num_kv_heads=w.Hkv, **kw))
+            calls.append(bind(pa.paged_attention_decode, t["out"], t["q"], kflat, vflat, t["block_table"],
+                              t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
         return calls, app
 
     main_calls, app_calls = make_calls(prepared=True)
@@ -502,40 +506,93 @@ def run_gpu(args) -> None:
                if dsamples else None)
     total_ms = max_over_ranks(total_ms, dist, dev)
 
-    # end to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, append + decode, D2H of the output
-    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "block_table")}
-    host["positions"] = positions.cpu().pin_memory()
-    host["lens_after"] = lens_after.cpu().pin_memory()
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    # end to end through the C ABI with host buffers: every step copies its
+    # inputs (q, k_new, v_new, block_table, positions, lengths) from pinned
+    # host memory, runs the step and reads the output back.  The inputs sit
+    # in one pinned buffer and one device buffer per slot (one copy each
+    # way), and two slots are double-buffered on two copy streams: the H2D
+    # of step i+1 and the D2H of step i-1 overlap step i, the pipelining a
+    # serving loop would use.  Graph and prefill runs copy in line.
+    names = ("q", "k_new", "v_new", "block_table", "positions", "lens_after")
+    src = dict(q=w.q, k_new=w.k_new, v_new=w.v_new, block_table=w.block_table,
+               positions=positions, lens_after=lens_after)
+    offs, total = {}, 0
+    for n in names:
+        offs[n] = total
+        total += -(-src[n].numel() * src[n].element_size() // 256) * 256
+    h2d = sum(src[n].numel() * src[n].element_size() for n in names)
+    d2h = out.numel() * out.element_size()
+    host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for n in names:
+        nb = src[n].numel() * src[n].element_size()
+        host_in[offs[n]:offs[n] + nb].copy_(src[n].contiguous().view(-1).view(torch.uint8).cpu())
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     Ke = max(3, min(K, 2000))
+    pipelined = graph is None and prefill is None
+    if pipelined:
+        dev_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        slots = []
+        for buf in dev_in:
+            t = {n: buf[offs[n]:offs[n] + src[n].numel() * src[n].element_size()]
+                 .view(src[n].dtype).view(src[n].shape) for n in names}
+            t["out"] = torch.empty_like(out)
+            slots.append((buf, t, make_calls(prepared=True, t=t)))
+        h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+        done = [torch.cuda.Event() for _ in range(2)]      # step in slot b finished
+        loaded = [torch.cuda.Event() for _ in range(2)]    # inputs of slot b copied
+        read = [torch.cuda.Event() for _ in range(2)]      # output of slot b copied back
+        for b in range(2):
+            done[b].record(stream)
+            read[b].record(stream)
 
-    def e2e_step():
-        w.q.copy_(host["q"], non_blocking=True)
-        w.k_new.copy_(host["k_new"], non_blocking=True)
-        w.v_new.copy_(host["v_new"], non_blocking=True)
-        w.block_table.copy_(host["block_table"], non_blocking=True)
-        positions.copy_(host["positions"], non_blocking=True)
-        lens_after.copy_(host["lens_after"], non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
+        def e2e_run(n):
+            for i in range(n):
+                b = i % 2
+                buf, t, (m_calls, a_calls) = slots[b]
+                h2d_stream.wait_event(done[b])
+                with torch.cuda.stream(h2d_stream):
+                    buf.copy_(host_in, non_blocking=True)
+                loaded[b].record(h2d_stream)
+                stream.wait_event(loaded[b])
+                stream.wait_event(read[b])
+                for c in a_calls + m_calls:
+                    c()
+                done[b].record(stream)
+                d2h_stream.wait_event(done[b])
+                with torch.cuda.stream(d2h_stream):
+                    host_out[b].copy_(t["out"], non_blocking=True)
+                read[b].record(d2h_stream)
+            for b in range(2):
+                stream.wait_event(read[b])
+    else:
+        host_views = {n: host_in[offs[n]:offs[n] + src[n].numel() * src[n].element_size()]
+                      .view(src[n].dtype).view(src[n].shape) for n in names}
 
-    for _ in range(3):
-        e2e_step()
+        def e2e_run(n):
+            for _ in range(n):
+                for name in names:
+                    src[name].copy_(host_views[name], non_blocking=True)
+                step()
+                host_out[0].copy_(out, non_blocking=True)
+
+    e2e_run(3)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(Ke):
-        e2e_step()
+    if pipelined:
+        h2d_stream.wait_event(e0)
+    e2e_run(Ke)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    # the copies really landed: the last output read back equals the step's
+    # (a prefill run writes no output)
+    out_checked = (None if prefill is not None else
+                   bool(torch.equal(host_out[(Ke - 1) % 2 if pipelined else 0].to(dev), out)))
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())} during timing")
 
@@ -585,7 +642,10 @@ def run_gpu(args) -> None:
                          "kernel_timing": "graph step" if graph is not None else "events"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": Ke,
-                    "ms_per_step": round(e2e_ms / Ke, 6)},
+                    "ms_per_step": round(e2e_ms / Ke, 6),
+                    "copies": ("one H2D and one D2H per step, double-buffered on two copy streams"
+                               if pipelined else "in line with the step"),
+                    "output_read_back_matches": out_checked},
             "gpu_launches": K * launches_per_step,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
