@@ -98,6 +98,22 @@ def _lib():
             lib.pao_kv_append.restype = i32
             lib.pao_kv_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, i32,
                                           vp, vp, vp, vp, vp, vp, vp]
+            lib.pao_e4m3_value.restype = dbl
+            lib.pao_e4m3_value.argtypes = [ctypes.c_ubyte]
+            lib.pao_e4m3_encode.restype = ctypes.c_ubyte
+            lib.pao_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.pao_quantize_fp8.restype = ctypes.c_ubyte
+            lib.pao_quantize_fp8.argtypes = [ctypes.c_float, ctypes.c_float]
+            lib.pao_quantize_fp8_array.restype = None
+            lib.pao_quantize_fp8_array.argtypes = [vp, i64, ctypes.c_float, vp]
+            lib.pao_kv_append_fp8.restype = i32
+            lib.pao_kv_append_fp8.argtypes = [i32, i32, i32, i32, i32, i64, i64, i32,
+                                              vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.pao_gather_fp8.restype = None
+            lib.pao_gather_fp8.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, i32, i64, vp, vp]
+            lib.pao_attention_decode_fp8.restype = i32
+            lib.pao_attention_decode_fp8.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, i32,
+                                                     vp, vp, vp, vp, vp, vp, dbl, vp, vp, i32]
             _handle = lib
     return _handle
 
@@ -361,4 +377,81 @@ def attention_decode_i8(q, k_pool, v_pool, kv_scales, block_table, seq_lens, sca
                                    block_stride, _dtype_code(q), _ptr(q), _ptr(k_pool),
                                    _ptr(v_pool), sc.ctypes.data, bt.ctypes.data, sl.ctypes.data,
                                    float(scale), out.ctypes.data, err.ctypes.data, int(threads))
+    return out, err
+
+
+# ---------------------------------------------------------------------------
+# fp8 (E4M3) cache blocks with per-(block, kv head) scales
+# ---------------------------------------------------------------------------
+# The second reading of quantised blocks implemented in pa_oracle.c: a code
+# is an OCP FP8 E4M3 byte (bias 7, 3 mantissa bits, subnormals m * 2^-9, no
+# infinities, 0x7F / 0xFF NaN, largest finite 448) standing for value(c) * s,
+# scales laid out as for int8; writing x stores the code of the binary32
+# quotient x / s, nearest value, ties to the even code, magnitudes beyond 448
+# saturating to 448 (a NaN quotient stores 0x7F).
+
+def e4m3_value(code: int) -> float:
+    """The value an E4M3 code stands for."""
+    return float(_lib().pao_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """The E4M3 code of a binary32 value (nearest, ties to even, saturating)."""
+    return int(_lib().pao_e4m3_encode(float(np.float32(x))))
+
+
+def quantize_fp8(x, scale: float) -> np.ndarray:
+    """E4M3 codes (uint8) of the float32 values x under one scale."""
+    xs = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(xs.shape, dtype=np.uint8)
+    _lib().pao_quantize_fp8_array(xs.ctypes.data, xs.size, float(np.float32(scale)), out.ctypes.data)
+    return out
+
+
+def kv_append_fp8(k_new, v_new, k_pool, v_pool, kv_scales, block_table, positions, *,
+                  block_size: int, block_stride: int, num_blocks: int):
+    """Append one token per (sequence, kv head) into fp8 pools, quantising
+    with the scales of the target block (in place; returns seq_err)."""
+    B, Hkv, D = (int(s) for s in k_new.shape)
+    bt = _i32(block_table)
+    pos = _i32(positions)
+    sc = _f32(kv_scales)
+    MB = bt.shape[1]
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_kv_append_fp8(B, Hkv, D, block_size, MB, num_blocks, block_stride,
+                             _dtype_code(k_new), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                             _ptr(v_pool), sc.ctypes.data, bt.ctypes.data, pos.ctypes.data,
+                             err.ctypes.data)
+    return err
+
+
+def gather_fp8(k_pool, v_pool, kv_scales, table_row, kv_head: int, length: int, *,
+               block_size: int, head_dim: int, num_kv_heads: int, block_stride: int):
+    """Contiguous [length][head_dim] dequantised K and V of one kv head."""
+    row = _i32(table_row)
+    sc = _f32(kv_scales)
+    Kc = np.empty((max(length, 1), head_dim), dtype=np.float64)
+    Vc = np.empty_like(Kc)
+    _lib().pao_gather_fp8(head_dim, block_size, num_kv_heads, block_stride, _ptr(k_pool),
+                          _ptr(v_pool), sc.ctypes.data, row.ctypes.data, kv_head, length,
+                          Kc.ctypes.data, Vc.ctypes.data)
+    return Kc[:length], Vc[:length]
+
+
+def attention_decode_fp8(q, k_pool, v_pool, kv_scales, block_table, seq_lens, scale: float, *,
+                         num_kv_heads: int, block_size: int, block_stride: int,
+                         num_blocks: int, threads: int = 0):
+    """Decode attention over an fp8 cache (the values the codes stand for),
+    masked to seq_lens.  Returns (out float64 [B][H][D], seq_err int32 [B])."""
+    B, H, D = (int(s) for s in q.shape)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    sc = _f32(kv_scales)
+    MB = bt.shape[1]
+    out = np.empty((B, H, D), dtype=np.float64)
+    err = np.zeros(B, dtype=np.int32)
+    _lib().pao_attention_decode_fp8(B, H, num_kv_heads, D, block_size, MB, num_blocks,
+                                    block_stride, _dtype_code(q), _ptr(q), _ptr(k_pool),
+                                    _ptr(v_pool), sc.ctypes.data, bt.ctypes.data, sl.ctypes.data,
+                                    float(scale), out.ctypes.data, err.ctypes.data, int(threads))
     return out, err

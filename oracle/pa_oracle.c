@@ -656,3 +656,177 @@ int pao_attention_decode_i8(int B, int H, int Hkv, int D, int bs, int MB,
     }
     return any;
 }
+
+/* ------------------------------------------------------------------------ */
+/* fp8 (E4M3) cache blocks with per-block scales                             */
+/* ------------------------------------------------------------------------ */
+
+/* The second reading of "quantised blocks with per-block scales": a cached
+ * element is an 8-bit floating-point code in the OCP FP8 E4M3 format (sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
+ * the subnormals m * 2^-9; no infinities; 0x7F and 0xFF are NaN, so the
+ * largest finite magnitude is 448) that stands for value(c) * s, with the
+ * scales laid out as for int8.  Writing a value x gives the code of x / s
+ * (the division in IEEE binary32) rounded to the nearest E4M3 value, ties to
+ * the even code, magnitudes beyond 448 saturating to 448 (infinities
+ * included); a NaN quotient gives the NaN code 0x7F. */
+
+/* The value an E4M3 code stands for. */
+double pao_e4m3_value(unsigned char c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* The E4M3 code of a binary32 value: nearest, ties to even, saturating. */
+unsigned char pao_e4m3_encode(float x)
+{
+    unsigned char sign;
+    double a, r;
+    int e2, E;
+    if (x != x)
+        return 0x7F;
+    sign = signbit(x) ? 0x80 : 0x00;
+    a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest
+         * normal, code 0x08, so the code is the multiple itself */
+        r = nearbyint(a / ldexp(1.0, -9));   /* exact quotient; ties to even */
+        return sign | (unsigned char)r;
+    }
+    frexp(a, &e2);          /* a in [2^(e2-1), 2^e2) */
+    E = e2 - 1;             /* a in [2^E, 2^(E+1)), E in [-6, 8] */
+    r = nearbyint(a / ldexp(1.0, E - 3));   /* in [8, 16]: 8 + mantissa */
+    if (r == 16.0) {        /* rounded up to the next power of two */
+        r = 8.0;
+        E += 1;
+    }
+    return sign | (unsigned char)(((E + 7) << 3) | ((int)r - 8));
+}
+
+unsigned char pao_quantize_fp8(float x, float s)
+{
+    volatile float q = x / s;   /* binary32 division, round to nearest even */
+    return pao_e4m3_encode(q);
+}
+
+void pao_quantize_fp8_array(const float *x, int64_t n, float s, unsigned char *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = pao_quantize_fp8(x[i], s);
+}
+
+/* As pao_kv_append_i8, with E4M3 codes. */
+int pao_kv_append_fp8(int B, int Hkv, int D, int bs, int MB, int64_t NB,
+                      int64_t block_stride, int dtype, const void *k_new,
+                      const void *v_new, unsigned char *k_pool, unsigned char *v_pool,
+                      const float *kv_scales, const int32_t *block_table,
+                      const int32_t *positions, int32_t *seq_err)
+{
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t pos = positions[b];
+        seq_err[b] = 0;
+        if (pos < 0 || pos >= (int64_t)MB * bs) {
+            seq_err[b] = PAO_SEQ_BAD_POS;
+            any |= seq_err[b];
+            continue;
+        }
+        int64_t blk = block_table[(int64_t)b * MB + pos / bs];
+        if (blk < 0 || blk >= NB) {
+            seq_err[b] = PAO_SEQ_BAD_BLOCK;
+            any |= seq_err[b];
+            continue;
+        }
+        for (int hk = 0; hk < Hkv; ++hk) {
+            int64_t dst = blk * block_stride + (int64_t)hk * bs * D + (pos % bs) * D;
+            int64_t src = ((int64_t)b * Hkv + hk) * D;
+            float sk = kv_scales[(blk * 2 + 0) * Hkv + hk];
+            float sv = kv_scales[(blk * 2 + 1) * Hkv + hk];
+            for (int d = 0; d < D; ++d) {
+                k_pool[dst + d] = pao_quantize_fp8((float)pao_element(k_new, src + d, dtype), sk);
+                v_pool[dst + d] = pao_quantize_fp8((float)pao_element(v_new, src + d, dtype), sv);
+            }
+        }
+    }
+    return any;
+}
+
+/* Gather of an fp8 cache: the values value(c) * s of kv head hk, tokens
+ * [0, len). */
+void pao_gather_fp8(int D, int bs, int Hkv, int64_t block_stride,
+                    const unsigned char *k_pool, const unsigned char *v_pool,
+                    const float *kv_scales, const int32_t *table_row, int hk,
+                    int64_t len, double *Kc, double *Vc)
+{
+    for (int64_t t = 0; t < len; ++t) {
+        int64_t blk = table_row[t / bs];
+        int64_t base = blk * block_stride + (int64_t)hk * bs * D + (t % bs) * D;
+        double sk = kv_scales[(blk * 2 + 0) * Hkv + hk];
+        double sv = kv_scales[(blk * 2 + 1) * Hkv + hk];
+        for (int d = 0; d < D; ++d) {
+            Kc[t * D + d] = pao_e4m3_value(k_pool[base + d]) * sk;
+            Vc[t * D + d] = pao_e4m3_value(v_pool[base + d]) * sv;
+        }
+    }
+}
+
+/* Decode attention over an fp8 cache: the textbook attention of
+ * pao_attention_decode over the values the codes stand for. */
+int pao_attention_decode_fp8(int B, int H, int Hkv, int D, int bs, int MB,
+                             int64_t NB, int64_t block_stride, int dtype,
+                             const void *q, const unsigned char *k_pool,
+                             const unsigned char *v_pool, const float *kv_scales,
+                             const int32_t *block_table, const int32_t *seq_lens,
+                             double scale, double *out, int32_t *seq_err,
+                             int nthreads)
+{
+    int group = H / Hkv;
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        seq_err[b] = validate_sequence(seq_lens[b], bs, MB, NB,
+                                       block_table + (int64_t)b * MB);
+        any |= seq_err[b];
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+        int b = (int)(u / Hkv);
+        int hk = (int)(u % Hkv);
+        int64_t len = seq_lens[b];
+        if (seq_err[b]) {
+            for (int h = hk * group; h < (hk + 1) * group; ++h)
+                for (int d = 0; d < D; ++d)
+                    out[((int64_t)b * H + h) * D + d] = 0.0;
+            continue;
+        }
+        size_t n = (size_t)(len > 0 ? len : 1) * D;
+        double *Kc = (double *)malloc(n * sizeof(double));
+        double *Vc = (double *)malloc(n * sizeof(double));
+        double *qd = (double *)malloc((size_t)D * sizeof(double));
+        pao_gather_fp8(D, bs, Hkv, block_stride, k_pool, v_pool, kv_scales,
+                       block_table + (int64_t)b * MB, hk, len, Kc, Vc);
+        for (int h = hk * group; h < (hk + 1) * group; ++h) {
+            for (int d = 0; d < D; ++d)
+                qd[d] = pao_element(q, ((int64_t)b * H + h) * D + d, dtype);
+            pao_attention_contiguous(len, D, qd, Kc, Vc, scale,
+                                     out + ((int64_t)b * H + h) * D);
+        }
+        free(Kc);
+        free(Vc);
+        free(qd);
+    }
+    return any;
+}

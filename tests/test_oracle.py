@@ -737,6 +737,151 @@ def test_i8_append_writes_the_codes_of_its_block_scale():
 
 
 # ---------------------------------------------------------------------------
+# fp8 (E4M3) cache: the format pinned to torch's float8_e4m3fn (a library
+# routine) and to values worked by hand, the decode to brute force
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_values():
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_value_of_every_code_matches_torch():
+    ref = _torch_e4m3_values()
+    got = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert list(np.nonzero(np.isnan(got))[0]) == [0x7F, 0xFF]
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ref[fin], got[fin])
+    # by hand: the largest finite, the smallest normal and subnormal, one
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0xFE) == -448.0
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6 and oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0x80) == 0.0
+
+
+def test_e4m3_encode_pins():
+    vals = _torch_e4m3_values()
+    # every finite code round-trips (both zeros included)
+    for c in range(256):
+        if not np.isnan(vals[c]):
+            assert oracle.e4m3_encode(np.float32(vals[c])) == c, c
+    # midpoints between neighbours go to the even code; one ulp off decides
+    pos = [(c, vals[c]) for c in range(0x7F)]
+    for (c0, v0), (c1, v1) in zip(pos, pos[1:]):
+        mid = np.float32((v0 + v1) / 2)
+        assert float(mid) == (v0 + v1) / 2
+        assert oracle.e4m3_encode(mid) == (c0 if c0 % 2 == 0 else c1), (c0, c1)
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(np.inf))) == c1
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(0))) == c0
+        assert oracle.e4m3_encode(-mid) == 0x80 | oracle.e4m3_encode(mid)
+    # worked by hand: subnormal ties, saturation beyond 448, NaN
+    cases = [(2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (5 * 2.0 ** -10, 0x02), (1.0625, 0x38),
+             (1.1875, 0x3A), (449.0, 0x7E), (463.9, 0x7E), (464.0, 0x7E), (1e30, 0x7E),
+             (float("inf"), 0x7E), (-500.0, 0xFE), (float("-inf"), 0xFE), (float("nan"), 0x7F)]
+    for x, c in cases:
+        assert oracle.e4m3_encode(x) == c, (x, c)
+    # inside the finite range it is torch's rounding
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.uniform(-463.0, 463.0, 50000), rng.normal(0.0, 0.05, 50000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.quantize_fp8(x, 1.0), ref)
+
+
+def test_quantize_fp8_divides_in_binary32():
+    # the quotient is taken in binary32 before rounding to E4M3
+    rng = np.random.default_rng(10)
+    x = rng.normal(0.0, 3.0, 20000).astype(np.float32)
+    sc = np.float32(0.0137)
+    q = (x / sc).astype(np.float32)
+    ref = torch.from_numpy(np.clip(q, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.quantize_fp8(x, sc), ref)
+
+
+def _fp8_case(seed, B=3, H=4, Hkv=2, D=16, bs=4, lens=(0, 5, 11)):
+    c = _i8_case(seed, B=B, H=H, Hkv=Hkv, D=D, bs=bs, lens=lens)
+    rng = np.random.default_rng(seed + 100)
+    codes = rng.integers(0, 256, size=c["pool"].shape).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C   # no NaN codes in the cache
+    c["pool"] = codes
+    return c
+
+
+def _fp8_values(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_fp8_decode_brute_force():
+    """Tiny case against per-token Python loops over the dequantised values
+    (codes read by torch's float8_e4m3fn)."""
+    c = _fp8_case(21)
+    flat = c["pool"].reshape(-1)
+    out, err = oracle.attention_decode_fp8(c["q"], flat, flat[c["Hkv"] * c["bs"] * c["D"]:],
+                                           c["scales"], c["table"], c["lens"], 0.05,
+                                           num_kv_heads=c["Hkv"], block_size=c["bs"],
+                                           block_stride=c["stride"], num_blocks=c["NB"])
+    assert not err.any()
+    deq = _fp8_values(c["pool"])
+    g = c["H"] // c["Hkv"]
+    for b in range(c["B"]):
+        for h in range(c["H"]):
+            hk = h // g
+            L = int(c["lens"][b])
+            if L == 0:
+                assert not out[b, h].any()
+                continue
+            K = np.empty((L, c["D"]))
+            V = np.empty((L, c["D"]))
+            for t in range(L):
+                blk = c["table"][b, t // c["bs"]]
+                K[t] = deq[blk, 0, hk, t % c["bs"]] * float(c["scales"][blk, 0, hk])
+                V[t] = deq[blk, 1, hk, t % c["bs"]] * float(c["scales"][blk, 1, hk])
+            x = 0.05 * (K @ c["q"][b, h].astype(np.float64))
+            w = np.exp(x - x.max())
+            np.testing.assert_allclose(out[b, h], (w[:, None] * V).sum(0) / w.sum(), rtol=0, atol=1e-12)
+
+
+def test_fp8_append_writes_the_codes_of_its_block_scale():
+    c = _fp8_case(23, B=3, H=4, Hkv=2, D=16, bs=4, lens=(3, 8, 9))
+    NB, Hkv, D, bs = c["NB"], c["Hkv"], c["D"], c["bs"]
+    used = set(int(x) for x in c["table"].ravel() if x >= 0)
+    free = [i for i in range(NB) if i not in used]
+    for b in range(c["B"]):
+        for j in range(-(-(int(c["lens"][b]) + 1) // bs)):
+            if c["table"][b, j] < 0:
+                c["table"][b, j] = free.pop()
+    gen = torch.Generator().manual_seed(24)
+    kn = torch.randn((c["B"], Hkv, D), generator=gen).to(torch.float16)
+    vn = torch.randn((c["B"], Hkv, D), generator=gen).to(torch.float16)
+    pool = c["pool"].copy()
+    flat = pool.reshape(-1)
+    err = oracle.kv_append_fp8(kn, vn, flat, flat[Hkv * bs * D:], c["scales"], c["table"], c["lens"],
+                               block_size=bs, block_stride=c["stride"], num_blocks=NB)
+    assert not err.any()
+    want = c["pool"].copy()
+
+    def codes(x, s):
+        q = (x.float().numpy() / np.float32(s)).astype(np.float32)
+        return torch.from_numpy(np.clip(q, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    for b in range(c["B"]):
+        pos = int(c["lens"][b])
+        blk = c["table"][b, pos // bs]
+        for hk in range(Hkv):
+            want[blk, 0, hk, pos % bs] = codes(kn[b, hk], c["scales"][blk, 0, hk])
+            want[blk, 1, hk, pos % bs] = codes(vn[b, hk], c["scales"][blk, 1, hk])
+    assert np.array_equal(pool, want)
+    # a position past the row and a hole in the table are skipped and flagged
+    pos = c["lens"].copy()
+    pos[0] = c["MB"] * bs
+    tab = c["table"].copy()
+    tab[1, int(c["lens"][1]) // bs] = -1
+    pool2 = c["pool"].copy()
+    f2 = pool2.reshape(-1)
+    err = oracle.kv_append_fp8(kn, vn, f2, f2[Hkv * bs * D:], c["scales"], tab, pos,
+                               block_size=bs, block_stride=c["stride"], num_blocks=NB)
+    assert list(err) == [oracle.SEQ_BAD_POS, oracle.SEQ_BAD_BLOCK, 0]
+
+
+# ---------------------------------------------------------------------------
 # the battery catches plausible mistakes planted in a copy of the oracle
 # ---------------------------------------------------------------------------
 
@@ -765,6 +910,14 @@ MUTANTS = {
                                         "double sv = kv_scales[((t / bs) * 2 + 1) * Hkv + hk];"),
     "int8 append with the V scale": ("float sk = kv_scales[(blk * 2 + 0) * Hkv + hk];",
                                      "float sk = kv_scales[(blk * 2 + 1) * Hkv + hk];"),
+    "fp8 exponent bias off by one": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 9);"),
+    "fp8 subnormals as normals": ("v = ldexp((double)m, -9);", "v = ldexp((double)(8 + m), -10);"),
+    "fp8 ties away from zero": ("r = nearbyint(a / ldexp(1.0, E - 3));", "r = round(a / ldexp(1.0, E - 3));"),
+    "fp8 truncated": ("r = nearbyint(a / ldexp(1.0, -9));", "r = floor(a / ldexp(1.0, -9));"),
+    "fp8 no saturation": ("    if (a >= 448.0)\n        return sign | 0x7E;\n", ""),
+    "fp8 carry into the exponent lost": ("        r = 8.0;\n        E += 1;", "        r = 15.0;"),
+    "fp8 V read with the K scale": ("            Vc[t * D + d] = pao_e4m3_value(v_pool[base + d]) * sv;",
+                                    "            Vc[t * D + d] = pao_e4m3_value(v_pool[base + d]) * sk;"),
 }
 
 
@@ -782,7 +935,11 @@ def _battery(lib) -> bool:
                  lambda: test_multi_token_append_equals_token_by_token("f32"),
                  test_quantize_i8_pins,
                  test_i8_decode_brute_force,
-                 test_i8_append_writes_the_codes_of_its_block_scale]
+                 test_i8_append_writes_the_codes_of_its_block_scale,
+                 test_e4m3_value_of_every_code_matches_torch,
+                 test_e4m3_encode_pins,
+                 test_fp8_decode_brute_force,
+                 test_fp8_append_writes_the_codes_of_its_block_scale]
         for t in tests:
             try:
                 t()
@@ -800,7 +957,9 @@ def _load_like_real(path):
                "pao_attention_contiguous", "pao_attention_decode", "pao_attention_partial",
                "pao_merge_partials", "pao_kv_append", "pao_kv_append_tokens",
                "pao_attention_decode_window", "pao_quantize_i8", "pao_quantize_i8_array",
-               "pao_kv_append_i8", "pao_gather_i8", "pao_attention_decode_i8"):
+               "pao_kv_append_i8", "pao_gather_i8", "pao_attention_decode_i8",
+               "pao_e4m3_value", "pao_e4m3_encode", "pao_quantize_fp8", "pao_quantize_fp8_array",
+               "pao_kv_append_fp8", "pao_gather_fp8", "pao_attention_decode_fp8"):
         getattr(lib, fn).restype = getattr(real, fn).restype
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
     return lib
