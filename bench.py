@@ -52,6 +52,7 @@ KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_
                   "decode_tc_balanced": "decode_balanced_tc.cu",
                   "decode_int8": "decode_int8.cu",
                   "decode_int8_tc": "decode_int8_tc.cu",
+                  "decode_fp8_tc": "decode_int8_tc.cu",
                   "decode_prefix_tc": "decode_prefix_tc.cu",
                   "append_tokens": "append.cu"}
 
@@ -67,7 +68,7 @@ def decode_bytes(w, lens_after, window: int = 0) -> int:
     HBM once).  With a sliding window only the last `window` rows count.
     """
     s = w.q.element_size()
-    s_kv = w.pool.element_size()           # 1 for an int8 cache
+    s_kv = w.pool.element_size()           # 1 for an int8 or fp8 cache
     lens = [int(x) for x in lens_after]
     tab = w.block_table.cpu()
     row_bytes = w.Hkv * w.D * s_kv         # one token, all kv heads, K or V
@@ -83,7 +84,7 @@ def decode_bytes(w, lens_after, window: int = 0) -> int:
             cur = rows.get(blk)
             rows[blk] = (a, e) if cur is None else (min(cur[0], a), max(cur[1], e))
     kv = 2 * row_bytes * sum(e - a for a, e in rows.values())
-    # an int8 cache also reads the K and V scales of every block it touches
+    # a quantised cache also reads the K and V scales of every block it touches
     scales = 2 * 4 * w.Hkv * len(rows) if getattr(w, "scales", None) is not None else 0
     return kv + scales + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
 
@@ -105,7 +106,7 @@ def logical_kv_bytes(w, lens_after) -> int:
 
 
 def append_bytes(w) -> int:
-    """Read the new K/V rows, write them into the pool (as codes for an int8
+    """Read the new K/V rows, write them into the pool (as codes for a quantised
     cache, which also reads the target blocks' scales), plus positions and
     table entries."""
     s = w.k_new.element_size()
@@ -293,11 +294,13 @@ def run_gpu(args) -> None:
     if args.long_seq:
         w = workloads.with_long_sequence(w, args.long_seq, seed=7 + rank, device=dev)
         workload_key += f"_long{args.long_seq}"
-    if args.int8:
+    if args.int8 and args.fp8:
+        raise SystemExit("--int8 and --fp8 are two cache formats: pick one")
+    if args.int8 or args.fp8:
         if args.prefill or args.window or args.balanced or args.graph:
-            raise SystemExit("--int8 times the int8 append + decode pair only")
-        w = workloads.to_int8(w, seed=17 + rank).to(dev)
-        workload_key += "_int8"
+            raise SystemExit("--int8 / --fp8 time the quantising append + decode pair only")
+        w = (workloads.to_fp8(w, seed=19 + rank) if args.fp8 else workloads.to_int8(w, seed=17 + rank)).to(dev)
+        workload_key += "_fp8" if args.fp8 else "_int8"
     kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
     shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
                           block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
@@ -309,6 +312,8 @@ def run_gpu(args) -> None:
         # the tensor cores (the rule of paged_attention_decode_int8)
         tc8 = w.H // w.Hkv >= 2 and w.D in (64, 128) and w.dtype in (torch.float16, torch.bfloat16)
         kernel = "decode_int8_tc" if tc8 else "decode_int8"
+    if args.fp8:
+        kernel = "decode_fp8_tc"
     if args.prefill:
         kernel = "append_tokens"
     ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
@@ -320,18 +325,19 @@ def run_gpu(args) -> None:
           if ptok else None)
     stream = torch.cuda.current_stream()
 
-    fused = not ptok and not args.unfused and not args.int8
+    quant = args.int8 or args.fp8
+    fused = not ptok and not args.unfused and not quant
 
     window = args.window or 0
     balanced = args.balanced
     if window and not balanced:
         fused = False
     bws = None
-    if args.int8:
+    if quant:
         ptok = None
     groups = None
     if args.shared_prefix is None:
-        args.shared_prefix = args.workload in SHARED_PREFIX and not args.int8 and not args.balanced \
+        args.shared_prefix = args.workload in SHARED_PREFIX and not quant and not args.balanced \
             and not args.long_seq and not args.prefill and not window
     if args.shared_prefix:
         if "shared_blocks" not in w.meta:
@@ -386,6 +392,11 @@ def run_gpu(args) -> None:
                               num_kv_heads=w.Hkv, **kw))
             return calls, [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
                                 t["positions"], **kw)]
+        if args.fp8:
+            calls.append(bind(pa.paged_attention_decode_fp8, t["out"], t["q"], kflat, vflat, w.scales,
+                              t["block_table"], t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
+            return calls, [bind(pa.paged_kv_append_fp8, t["k_new"], t["v_new"], kflat, vflat, w.scales,
+                                t["block_table"], t["positions"], **kw)]
         if args.int8:
             calls.append(bind(pa.paged_attention_decode_int8, t["out"], t["q"], kflat, vflat, w.scales,
                               t["block_table"], t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
@@ -670,7 +681,11 @@ def _oracle_sample(w, lens_after, seqs, threads=None):
     lens = lens_after.index_select(0, sub).contiguous()
     flat = w.pool.view(-1)
     t = time.perf_counter()
-    if getattr(w, "scales", None) is not None:
+    if getattr(w, "scales", None) is not None and w.pool.dtype == torch.uint8:
+        oracle.attention_decode_fp8(q, flat, flat[w.v_offset:], w.scales, table, lens, w.scale,
+                                    num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
+                                    num_blocks=w.NB, threads=threads)
+    elif getattr(w, "scales", None) is not None:
         oracle.attention_decode_i8(q, flat, flat[w.v_offset:], w.scales, table, lens, w.scale,
                                    num_kv_heads=w.Hkv, block_size=w.bs, block_stride=w.block_stride,
                                    num_blocks=w.NB, threads=threads)
@@ -717,6 +732,8 @@ def run_reference(args) -> None:
         w = workloads.with_long_sequence(w, args.long_seq)
     if args.int8:
         w = workloads.to_int8(w)
+    if args.fp8:
+        w = workloads.to_fp8(w)
     lens_after = w.lens + 1
     for i in range(args.warmup):
         _oracle_sample(w, lens_after, [i % w.B])
@@ -767,6 +784,9 @@ def main() -> None:
     ap.add_argument("--shared-prefix", action=argparse.BooleanOptionalAction, default=None,
                     help="paged_attention_decode_shared_prefix (shared blocks read once per "
                          "group; the default for workload 5)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="fp8 (E4M3) cache with per-block scales (paged_kv_append_fp8 + "
+                         "paged_attention_decode_fp8)")
     ap.add_argument("--int8", action="store_true",
                     help="int8 cache with per-block scales (paged_kv_append_int8 + "
                          "paged_attention_decode_int8)")

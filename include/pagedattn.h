@@ -16,6 +16,8 @@
  *                                   equal work per warp (mixed lengths)
  *   paged_kv_append_int8,           the same write and attention over an
  *   paged_attention_decode_int8     int8 cache with per-block scales
+ *   paged_kv_append_fp8,            ... over an fp8 (E4M3) cache with
+ *   paged_attention_decode_fp8      per-block scales
  *
  * Sources (web pages on paged KV caches), cited by title and section:
  *   "KV Cache and BlockManager" (dpshk.com/news/5906718)            [BM]
@@ -409,8 +411,8 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
  * codes stand for ([PG] s2.2): x_t = scale * s_K * <q, c_t>, weights w_t as
  * there, out = sum_t w_t s_V c_t / sum_t w_t.  Same device checks, zeros and
  * PA_DEVERR_* bits.  Grouped-query shapes with 16-bit q and head_dim 64 or
- * 128 run on the tensor cores (codes turned into exact fp16 in shared
- * memory, queries rounded to fp16); the rest on the CUDA cores.
+ * 128 run on the tensor cores (codes turned into exact fp16 in registers,
+ * queries rounded to fp16); the rest on the CUDA cores.
  */
 pa_status paged_kv_append_int8(const pa_shape *shape, const void *k_new, const void *v_new,
                                int8_t *k_pool, int8_t *v_pool, const float *kv_scales,
@@ -422,6 +424,43 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
                                       const float *kv_scales, const int32_t *block_table,
                                       const int32_t *seq_lens, float scale, int32_t *err_word,
                                       pa_stream_t stream);
+
+/*
+ * fp8 KV cache: E4M3 blocks with per-block scales.
+ *
+ * The second scheme for the quantised blocks the sources name ([BM] s6.3,
+ * s3) without fixing one: a pool element is an 8-bit floating-point code in
+ * the OCP FP8 E4M3 format (sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 holds the subnormals m * 2^-9; no
+ * infinities; 0x7F and 0xFF are NaN; largest finite magnitude 448) standing
+ * for value(c) * s, with the scales laid out and owned exactly as for the
+ * int8 cache above.  The pools have the same byte layout; shape->dtype is
+ * the element type of q, out, k_new and v_new (fp32, fp16 or bf16); head_dim
+ * must be 64 or 128 (other head_dims: PA_ERR_UNSUPPORTED).
+ *
+ * paged_kv_append_fp8 writes each value x as the E4M3 code of x / s (the
+ * quotient in IEEE binary32) nearest to it, ties to the even code,
+ * magnitudes beyond 448 saturating to 448 (a NaN quotient gives the NaN code
+ * 0x7F).
+ *
+ * paged_attention_decode_fp8 is paged_attention_decode over the values the
+ * codes stand for ([PG] s2.2): x_t = scale * s_K * <q, value(c_t)>, out =
+ * sum_t w_t s_V value(c_t) / sum_t w_t.  Same device checks, zeros and
+ * PA_DEVERR_* bits.  Every group size runs on the tensor cores: codes are
+ * converted to exact fp16 in registers and queries are rounded to fp16
+ * (held to the 16-bit tolerance whatever q's dtype).  Codes that are NaN
+ * make the outputs of their (sequence, kv head) NaN.
+ */
+pa_status paged_kv_append_fp8(const pa_shape *shape, const void *k_new, const void *v_new,
+                              uint8_t *k_pool, uint8_t *v_pool, const float *kv_scales,
+                              const int32_t *block_table, const int32_t *positions,
+                              int32_t *err_word, pa_stream_t stream);
+
+pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const void *q,
+                                     const uint8_t *k_pool, const uint8_t *v_pool,
+                                     const float *kv_scales, const int32_t *block_table,
+                                     const int32_t *seq_lens, float scale, int32_t *err_word,
+                                     pa_stream_t stream);
 
 /*
  * paged_attention_decode_split_static -- the split-KV pair without any

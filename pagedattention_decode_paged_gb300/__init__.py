@@ -13,7 +13,9 @@ paged_attention_partial_workspace, paged_attention_decode_partial,
 paged_attention_decode_reduce, paged_attention_decode_path,
 paged_attention_balanced_workspace, paged_attention_decode_balanced
 (persistent load-balanced schedule), paged_kv_append_int8,
-paged_attention_decode_int8 (int8 cache with per-block scales).
+paged_attention_decode_int8 (int8 cache with per-block scales),
+paged_kv_append_fp8, paged_attention_decode_fp8 (fp8 E4M3 cache with
+per-block scales).
 """
 from __future__ import annotations
 
@@ -38,6 +40,7 @@ EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attentio
             "paged_attention_decode_partial", "paged_attention_decode_reduce",
             "paged_attention_balanced_workspace", "paged_attention_decode_balanced",
             "paged_kv_append_int8", "paged_attention_decode_int8",
+            "paged_kv_append_fp8", "paged_attention_decode_fp8",
             "paged_attention_decode_shared_prefix")
 
 
@@ -103,6 +106,10 @@ def load() -> ctypes.CDLL:
             lib.paged_kv_append_int8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.paged_attention_decode_int8.restype = ctypes.c_int
             lib.paged_attention_decode_int8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
+            lib.paged_kv_append_fp8.restype = ctypes.c_int
+            lib.paged_kv_append_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.paged_attention_decode_fp8.restype = ctypes.c_int
+            lib.paged_attention_decode_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
             lib.paged_attention_balanced_workspace.restype = sz
             lib.paged_attention_balanced_workspace.argtypes = [sp]
             lib.paged_attention_decode_balanced.restype = ctypes.c_int
@@ -364,6 +371,33 @@ def paged_attention_decode_int8(out, q, k_pool, v_pool, kv_scales, block_table, 
     args = (ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_scales),
             _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(err_word), _stream(stream))
     return _issue(load().paged_attention_decode_int8, args, "paged_attention_decode_int8", prepare,
+                  (shape,))
+
+
+def paged_kv_append_fp8(k_new, v_new, k_pool, v_pool, kv_scales, block_table, positions, *,
+                        block_size, num_blocks, block_stride, err_word=None, stream=None,
+                        prepare=False):
+    """Quantising append of k_new/v_new [B][Hkv][D] into fp8 (E4M3) pools
+    (codes of the target block's scales)."""
+    B, Hkv, D = k_new.shape
+    shape = make_shape(batch=B, num_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=block_size,
+                       max_blocks_per_seq=block_table.shape[1], num_blocks=num_blocks,
+                       block_stride=block_stride, dtype=k_new.dtype)
+    args = (ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+            _ptr(kv_scales), _ptr(block_table), _ptr(positions), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_kv_append_fp8, args, "paged_kv_append_fp8", prepare, (shape,))
+
+
+def paged_attention_decode_fp8(out, q, k_pool, v_pool, kv_scales, block_table, seq_lens, scale, *,
+                               num_kv_heads, block_size, num_blocks, block_stride, err_word=None,
+                               stream=None, prepare=False):
+    """Decode attention over an fp8 (E4M3) cache with per-(block, kv head)
+    scales."""
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    args = (ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_scales),
+            _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(err_word), _stream(stream))
+    return _issue(load().paged_attention_decode_fp8, args, "paged_attention_decode_fp8", prepare,
                   (shape,))
 
 

@@ -681,6 +681,14 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
 
 // Shape checks of the int8 entry points: pools of one byte per element whose
 // rows (head_dim bytes) and blocks start on 16-byte boundaries.
+static pa_status check_fp8_shape(const pa_shape *s) {
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (!pa::fp8_supported(s->dtype, s->head_dim)) return PA_ERR_UNSUPPORTED;
+    if (s->block_stride % 16 != 0) return PA_ERR_MISALIGNED;
+    return PA_OK;
+}
+
 static pa_status check_int8_shape(const pa_shape *s) {
     pa_status st = check_shape(s);
     if (st != PA_OK) return st;
@@ -716,8 +724,8 @@ pa_status paged_kv_append_int8(const pa_shape *shape, const void *k_new, const v
     p.MB = shape->max_blocks_per_seq;
     p.bs = shape->block_size;
     p.row_bytes = shape->head_dim;
-    return pa::launch_append_int8(shape->dtype, p, kv_scales, shape->head_dim,
-                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    return pa::launch_append_codes(shape->dtype, false, p, kv_scales, shape->head_dim,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }
@@ -753,6 +761,70 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
         return PA_ERR_CUDA;
     const cudaError_t e = pa::launch_decode_int8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
                                                     boxes ? &vmap : nullptr, box_rows_for(shape), s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_kv_append_fp8(const pa_shape *shape, const void *k_new, const void *v_new,
+                               uint8_t *k_pool, uint8_t *v_pool, const float *kv_scales,
+                               const int32_t *block_table, const int32_t *positions,
+                               int32_t *err_word, pa_stream_t stream) {
+    pa_status st = check_fp8_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        kv_scales == nullptr || block_table == nullptr || positions == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(kv_scales) & 3u) != 0) return PA_ERR_MISALIGNED;
+    pa::AppendParams p{};
+    p.k_new = static_cast<const char *>(k_new);
+    p.v_new = static_cast<const char *>(v_new);
+    p.k_pool = reinterpret_cast<char *>(k_pool);
+    p.v_pool = reinterpret_cast<char *>(v_pool);
+    p.block_table = block_table;
+    p.positions = positions;
+    p.err_word = err_word;
+    p.num_blocks = shape->num_blocks;
+    p.block_stride_bytes = shape->block_stride;
+    p.B = shape->batch;
+    p.Hkv = shape->num_kv_heads;
+    p.MB = shape->max_blocks_per_seq;
+    p.bs = shape->block_size;
+    p.row_bytes = shape->head_dim;
+    return pa::launch_append_codes(shape->dtype, true, p, kv_scales, shape->head_dim,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const void *q,
+                                      const uint8_t *k_pool, const uint8_t *v_pool,
+                                      const float *kv_scales, const int32_t *block_table,
+                                      const int32_t *seq_lens, float scale, int32_t *err_word,
+                                      pa_stream_t stream) {
+    pa_status st = check_fp8_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (out == nullptr || q == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        kv_scales == nullptr || block_table == nullptr || seq_lens == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(kv_scales) & 3u) != 0) return PA_ERR_MISALIGNED;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.block_stride_bytes = shape->block_stride;   // one byte per element
+    p.out = out;
+    p.partition_tokens = 0;
+    p.num_partitions = 1;
+    p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap kmap{}, vmap{};
+    const bool boxes = int8_tc_boxes_ok(shape);
+    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
+        return PA_ERR_CUDA;
+    const cudaError_t e = pa::launch_decode_fp8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
+                                                   boxes ? &vmap : nullptr, box_rows_for(shape), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -24,6 +24,7 @@
 // (relative error of the largest weight below 2^-14), and meets the V codes
 // in dp2a as well, two tokens per instruction.  Both scales of every block
 // of the sequence are staged in shared memory next to its block-table row.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "pa_device.cuh"
@@ -363,8 +364,40 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
 // quantising append: one thread per 16 codes of a new row
 // ---------------------------------------------------------------------------
 
-template <typename T>
-__global__ void __launch_bounds__(256) append_int8_kernel(AppendParams p, const float *kv_scales, int D) {
+// The codes of a new row's 16 elements src[0..15] under scale s: int8 codes
+// (binary32 quotient, nearest integer with ties to even, NaN -> 0, clamped
+// to the symmetric code range) or E4M3 codes (the same quotient, nearest
+// E4M3 value with ties to even, saturating at +-448, by the hardware
+// conversion with .satfinite).
+template <typename T, bool FP8>
+__device__ __forceinline__ uint4 row_codes16(const T *src, float s) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+        if constexpr (FP8) {
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const float2 x = make_float2(__fdiv_rn(Elem<T>::to_float(src[q * 4 + e]), s),
+                                             __fdiv_rn(Elem<T>::to_float(src[q * 4 + e + 1]), s));
+                const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+                word |= (uint32_t)two << (8 * e);   // element e in the lower byte
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int c = __float2int_rn(__fdiv_rn(Elem<T>::to_float(src[q * 4 + e]), s));
+                c = max(-127, min(127, c));
+                word |= (uint32_t)(c & 0xff) << (8 * e);
+            }
+        }
+        w[q] = word;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T, bool FP8>
+__device__ __forceinline__ void append_codes(const AppendParams &p, const float *kv_scales, int D) {
     grid_dependency_wait();
     allow_dependents();
     const int vecs = D / 16;
@@ -391,22 +424,18 @@ __global__ void __launch_bounds__(256) append_int8_kernel(AppendParams p, const 
     }
     const float s = kv_scales[((int64_t)blk * 2 + kv) * p.Hkv + h];
     const T *src = reinterpret_cast<const T *>(kv ? p.v_new : p.k_new) + ((int64_t)b * p.Hkv + h) * D + v * 16;
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            // binary32 quotient, nearest integer with ties to even (NaN -> 0),
-            // clamped to the symmetric code range
-            int c = __float2int_rn(__fdiv_rn(Elem<T>::to_float(src[q * 4 + e]), s));
-            c = max(-127, min(127, c));
-            word |= (uint32_t)(c & 0xff) << (8 * e);
-        }
-        w[q] = word;
-    }
     const int64_t dst = (int64_t)blk * p.block_stride_bytes + ((int64_t)h * p.bs + pos % p.bs) * D + v * 16;
-    *reinterpret_cast<uint4 *>((kv ? p.v_pool : p.k_pool) + dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>((kv ? p.v_pool : p.k_pool) + dst) = row_codes16<T, FP8>(src, s);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_int8_kernel(AppendParams p, const float *kv_scales, int D) {
+    append_codes<T, false>(p, kv_scales, D);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_fp8_kernel(AppendParams p, const float *kv_scales, int D) {
+    append_codes<T, true>(p, kv_scales, D);
 }
 
 // ---------------------------------------------------------------------------
@@ -452,20 +481,22 @@ cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv_scales, int head_dim,
-                               cudaStream_t stream) {
+cudaError_t launch_append_codes(int dtype, bool fp8, const AppendParams &p, const float *kv_scales,
+                                int head_dim, cudaStream_t stream) {
     const int64_t total = (int64_t)p.B * p.Hkv * 2 * (head_dim / 16);
     if (total == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
     switch (dtype) {
         case PA_F32:
-            return launch_clustered(append_int8_kernel<float>, blocks, threads, 0, 1, stream, p, kv_scales, head_dim);
+            return launch_clustered(fp8 ? append_fp8_kernel<float> : append_int8_kernel<float>, blocks, threads, 0,
+                                    1, stream, p, kv_scales, head_dim);
         case PA_F16:
-            return launch_clustered(append_int8_kernel<__half>, blocks, threads, 0, 1, stream, p, kv_scales, head_dim);
+            return launch_clustered(fp8 ? append_fp8_kernel<__half> : append_int8_kernel<__half>, blocks, threads,
+                                    0, 1, stream, p, kv_scales, head_dim);
         case PA_BF16:
-            return launch_clustered(append_int8_kernel<__nv_bfloat16>, blocks, threads, 0, 1, stream, p, kv_scales,
-                                    head_dim);
+            return launch_clustered(fp8 ? append_fp8_kernel<__nv_bfloat16> : append_int8_kernel<__nv_bfloat16>,
+                                    blocks, threads, 0, 1, stream, p, kv_scales, head_dim);
     }
     return cudaErrorInvalidValue;
 }

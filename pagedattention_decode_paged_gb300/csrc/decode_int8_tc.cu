@@ -28,6 +28,7 @@
 //   consecutive codes of each of its 4 tokens.
 // The K scale of each row's block multiplies its scores and the V scale its
 // weights (the ROWSCALE tile step); queries are rounded to fp16.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "pa_device.cuh"
@@ -87,12 +88,14 @@ template <>
 struct VCodes<16> {
     uint4 v;
     __device__ __forceinline__ void load(const unsigned char *p) { v = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void clear() { v = make_uint4(0, 0, 0, 0); }
     __device__ __forceinline__ uint32_t word(int i) const { return word_of(v, i); }
 };
 template <>
 struct VCodes<8> {
     uint2 v;
     __device__ __forceinline__ void load(const unsigned char *p) { v = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ void clear() { v = make_uint2(0, 0); }
     __device__ __forceinline__ uint32_t word(int i) const { return i == 0 ? v.x : v.y; }
 };
 
@@ -105,10 +108,17 @@ __device__ __forceinline__ int code_off(int r, int c) {
     else return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
 }
 
-template <typename T, int D, int NT, bool BOXES>
-__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
-    decode_int8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                          DecodeParams p, const float *kv_scales, int box_rows) {
+// Two E4M3 codes (bytes 0 and 1 of v) as the exact fp16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// The kernel body, for int8 codes or (FP8) E4M3 codes: the two differ only
+// in how a word of four codes becomes two fp16 pairs.
+template <typename T, int D, int NT, bool BOXES, bool FP8>
+__device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                              const DecodeParams &p, const float *kv_scales, int box_rows) {
     grid_dependency_wait();
     allow_dependents();
     using C = I8TcCfg<D, BOXES>;
@@ -315,26 +325,49 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWar
 
         const int t0 = (warp + k * kI8TcWarps) * kTcTile;
         const int nvalid = min(kTcTile, len - t0);
+        if constexpr (FP8) {
+            // rows past the length hold stale or unwritten bytes, which may be
+            // NaN codes: clear them so that their zero weights meet zeros
+            if (nvalid < kTcTile) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (2 * tig + (i & 1) + 8 * (i >> 1) >= nvalid) vw[i].clear();
+            }
+        }
         const int j0r = blk_of(t0 + min(gid, nvalid - 1)), j1r = blk_of(t0 + min(gid + 8, nvalid - 1));
         tc_tile_step_frags<__half, D, NT, true>(
             [&](int kk, uint32_t(&a)[4]) {
-                const uint32_t w0 = word_of(kw[0][kk / 4], kk % 4) ^ 0x80808080u;   // token gid
-                const uint32_t w1 = word_of(kw[1][kk / 4], kk % 4) ^ 0x80808080u;   // token gid + 8
-                a[0] = codes_lo_f16x2(w0);
-                a[1] = codes_lo_f16x2(w1);
-                a[2] = codes_hi_f16x2(w0);
-                a[3] = codes_hi_f16x2(w1);
+                const uint32_t w0 = word_of(kw[0][kk / 4], kk % 4);   // token gid
+                const uint32_t w1 = word_of(kw[1][kk / 4], kk % 4);   // token gid + 8
+                if constexpr (FP8) {
+                    a[0] = e4m3x2_f16x2(w0);
+                    a[1] = e4m3x2_f16x2(w1);
+                    a[2] = e4m3x2_f16x2(w0 >> 16);
+                    a[3] = e4m3x2_f16x2(w1 >> 16);
+                } else {
+                    a[0] = codes_lo_f16x2(w0 ^ 0x80808080u);
+                    a[1] = codes_lo_f16x2(w1 ^ 0x80808080u);
+                    a[2] = codes_hi_f16x2(w0 ^ 0x80808080u);
+                    a[3] = codes_hi_f16x2(w1 ^ 0x80808080u);
+                }
             },
             [&](int mt, uint32_t(&a)[4]) {
                 // bytes 2mt and 2mt + 1 of each token's DPT codes, tokens
                 // (2tig, 2tig + 1) and (2tig + 8, 2tig + 9) interleaved
                 const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t u01 = __byte_perm(vw[0].word(mt / 2), vw[1].word(mt / 2), sel) ^ 0x80808080u;
-                const uint32_t u23 = __byte_perm(vw[2].word(mt / 2), vw[3].word(mt / 2), sel) ^ 0x80808080u;
-                a[0] = codes_lo_f16x2(u01);   // row gid: head_dim DPT*gid + 2mt
-                a[1] = codes_hi_f16x2(u01);   // row gid + 8: head_dim DPT*gid + 2mt + 1
-                a[2] = codes_lo_f16x2(u23);
-                a[3] = codes_hi_f16x2(u23);
+                const uint32_t u01 = __byte_perm(vw[0].word(mt / 2), vw[1].word(mt / 2), sel);
+                const uint32_t u23 = __byte_perm(vw[2].word(mt / 2), vw[3].word(mt / 2), sel);
+                if constexpr (FP8) {
+                    a[0] = e4m3x2_f16x2(u01);         // row gid: head_dim DPT*gid + 2mt
+                    a[1] = e4m3x2_f16x2(u01 >> 16);   // row gid + 8: head_dim DPT*gid + 2mt + 1
+                    a[2] = e4m3x2_f16x2(u23);
+                    a[3] = e4m3x2_f16x2(u23 >> 16);
+                } else {
+                    a[0] = codes_lo_f16x2(u01 ^ 0x80808080u);
+                    a[1] = codes_hi_f16x2(u01 ^ 0x80808080u);
+                    a[2] = codes_lo_f16x2(u23 ^ 0x80808080u);
+                    a[3] = codes_hi_f16x2(u23 ^ 0x80808080u);
+                }
             },
             0, nvalid, qb, p.scale_log2, o_acc, m_run, l_run, lane,
             make_float2(scale_of(j0r, 0), scale_of(j1r, 0)), make_float2(scale_of(j0r, 1), scale_of(j1r, 1)));
@@ -400,12 +433,26 @@ __global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWar
 }
 
 template <typename T, int D, int NT, bool BOXES>
+__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
+    decode_int8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          DecodeParams p, const float *kv_scales, int box_rows) {
+    codes_tc_body<T, D, NT, BOXES, false>(kmap, vmap, p, kv_scales, box_rows);
+}
+
+template <typename T, int D, int NT, bool BOXES>
+__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
+    decode_fp8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                         DecodeParams p, const float *kv_scales, int box_rows) {
+    codes_tc_body<T, D, NT, BOXES, true>(kmap, vmap, p, kv_scales, box_rows);
+}
+
+template <typename T, int D, int NT, bool BOXES, bool FP8>
 static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_scales, const CUtensorMap &kmap,
                                    const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
     DecodeParams p = params;
     p.table_cap = min(p.table_cap, kI8TcTableCap);
     const size_t smem = I8TcCfg<D, BOXES>::bytes(p.table_cap);
-    auto kern = decode_int8_tc_kernel<T, D, NT, BOXES>;
+    auto kern = FP8 ? decode_fp8_tc_kernel<T, D, NT, BOXES> : decode_int8_tc_kernel<T, D, NT, BOXES>;
     static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
@@ -415,26 +462,26 @@ static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_
     return launch_clustered(kern, grid, kI8TcWarps * 32, smem, 1, stream, kmap, vmap, p, kv_scales, box_rows);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool FP8>
 static cudaError_t launch_int8_tc_b(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
                                     const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
     if (kmap != nullptr && vmap != nullptr)
-        return launch_int8_tc_t<T, D, NT, true>(p, kv_scales, *kmap, *vmap, box_rows, stream);
+        return launch_int8_tc_t<T, D, NT, true, FP8>(p, kv_scales, *kmap, *vmap, box_rows, stream);
     const CUtensorMap none{};
-    return launch_int8_tc_t<T, D, NT, false>(p, kv_scales, none, none, box_rows, stream);
+    return launch_int8_tc_t<T, D, NT, false, FP8>(p, kv_scales, none, none, box_rows, stream);
 }
 
-template <typename T>
+template <typename T, bool FP8>
 static cudaError_t launch_int8_tc_d(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
                                     const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
     const bool one = p.H / p.Hkv <= 8;
     switch (p.D) {
         case 64:
-            return one ? launch_int8_tc_b<T, 64, 1>(p, kv_scales, kmap, vmap, box_rows, stream)
-                       : launch_int8_tc_b<T, 64, 2>(p, kv_scales, kmap, vmap, box_rows, stream);
+            return one ? launch_int8_tc_b<T, 64, 1, FP8>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 64, 2, FP8>(p, kv_scales, kmap, vmap, box_rows, stream);
         case 128:
-            return one ? launch_int8_tc_b<T, 128, 1>(p, kv_scales, kmap, vmap, box_rows, stream)
-                       : launch_int8_tc_b<T, 128, 2>(p, kv_scales, kmap, vmap, box_rows, stream);
+            return one ? launch_int8_tc_b<T, 128, 1, FP8>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 128, 2, FP8>(p, kv_scales, kmap, vmap, box_rows, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -443,11 +490,24 @@ bool int8_tc_supported(int dtype, int head_dim) {
     return (dtype == PA_F16 || dtype == PA_BF16) && (head_dim == 64 || head_dim == 128);
 }
 
+bool fp8_supported(int dtype, int head_dim) {
+    return (dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16) && (head_dim == 64 || head_dim == 128);
+}
+
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16>(p, kv_scales, kmap, vmap, box_rows, stream);
-    if (dtype == PA_F16) return launch_int8_tc_d<__half>(p, kv_scales, kmap, vmap, box_rows, stream);
+    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16, false>(p, kv_scales, kmap, vmap, box_rows, stream);
+    if (dtype == PA_F16) return launch_int8_tc_d<__half, false>(p, kv_scales, kmap, vmap, box_rows, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_fp8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                 const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
+                                 cudaStream_t stream) {
+    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16, true>(p, kv_scales, kmap, vmap, box_rows, stream);
+    if (dtype == PA_F16) return launch_int8_tc_d<__half, true>(p, kv_scales, kmap, vmap, box_rows, stream);
+    if (dtype == PA_F32) return launch_int8_tc_d<float, true>(p, kv_scales, kmap, vmap, box_rows, stream);
     return cudaErrorInvalidValue;
 }
 

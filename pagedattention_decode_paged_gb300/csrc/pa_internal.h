@@ -234,8 +234,10 @@ cudaError_t launch_prefix_tc(int dtype, const DecodeParams &p, const CUtensorMap
 bool int8_supported(int dtype, int head_dim);
 cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv_scales,
                                cudaStream_t stream);
-cudaError_t launch_append_int8(int dtype, const AppendParams &p, const float *kv_scales,
-                               int head_dim, cudaStream_t stream);
+// The quantising append of one token per (sequence, kv head): int8 codes,
+// or E4M3 codes when fp8.
+cudaError_t launch_append_codes(int dtype, bool fp8, const AppendParams &p, const float *kv_scales,
+                                int head_dim, cudaStream_t stream);
 // grouped-query shapes of the int8 cache on the tensor cores
 bool int8_tc_supported(int dtype, int head_dim);
 // kmap/vmap: tensor maps of the int8 pools (boxes of box_rows rows, see
@@ -243,6 +245,12 @@ bool int8_tc_supported(int dtype, int head_dim);
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream);
+// The fp8 (E4M3) cache: every group size, head_dim 64/128, queries of any
+// of the three dtypes, on the tensor-core code kernel.
+bool fp8_supported(int dtype, int head_dim);
+cudaError_t launch_decode_fp8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                 const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
+                                 cudaStream_t stream);
 
 // Load-balanced persistent decode (final mode; plain, fused append or sliding
 // window as DecodeParams says).  A plan fixes the grid for a shape on the

@@ -204,6 +204,33 @@ def test_int8_rejects_bad_arguments(lib):
         == pa.PA_ERR_UNSUPPORTED
 
 
+def test_fp8_rejects_bad_arguments(lib):
+    s8 = base_shape(block_stride=2 * 2 * 16 * 128)   # bytes: one per element
+    dec = lib.paged_attention_decode_fp8
+    app = lib.paged_kv_append_fp8
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # out, q, k_pool, v_pool, scales, table, lens
+    assert dec(None, *ok, 0.1, None, None) == pa.PA_ERR_INVALID_ARG
+    # head_dim 64 and 128 only (256 runs on the int8 path but not here)
+    for D in (32, 96, 256):
+        assert dec(ctypes.byref(base_shape(head_dim=D, block_stride=2 * 2 * 16 * D)), *ok, 0.1, None, None) \
+            == pa.PA_ERR_UNSUPPORTED
+        assert app(ctypes.byref(base_shape(head_dim=D, block_stride=2 * 2 * 16 * D)), *ok, None, None) \
+            == pa.PA_ERR_UNSUPPORTED
+    assert dec(ctypes.byref(base_shape(block_stride=2 * 2 * 16 * 128 + 8)), *ok, 0.1, None, None) \
+        == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), *ok[:4], None, *ok[5:], 0.1, None, None) == pa.PA_ERR_INVALID_ARG
+    assert dec(ctypes.byref(s8), *ok[:4], FAKE + 2, *ok[5:], 0.1, None, None) == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), FAKE, FAKE, FAKE + 8, *ok[3:], 0.1, None, None) == pa.PA_ERR_MISALIGNED
+    assert dec(ctypes.byref(s8), *ok, float("nan"), None, None) == pa.PA_ERR_INVALID_ARG
+    assert dec(ctypes.byref(base_shape(batch=0)), *ok, 0.1, None, None) == pa.PA_OK
+    ok_a = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)  # k_new, v_new, k_pool, v_pool, scales, table, pos
+    assert app(ctypes.byref(s8), *ok_a[:4], None, *ok_a[5:], None, None) == pa.PA_ERR_INVALID_ARG
+    assert app(ctypes.byref(s8), *ok_a[:2], FAKE + 4, *ok_a[3:], None, None) == pa.PA_ERR_MISALIGNED
+    # fp32 queries and rows are accepted (the shape check passes; no device here)
+    assert app(ctypes.byref(base_shape(batch=0, dtype=pa.PA_F32, block_stride=2 * 2 * 16 * 128)), *ok_a,
+               None, None) == pa.PA_OK
+
+
 def test_shared_prefix_rejects_bad_arguments(lib):
     f = lib.paged_attention_decode_shared_prefix
     s = base_shape()

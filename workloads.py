@@ -341,9 +341,10 @@ def with_long_sequence(w: Workload, length: int, *, seed: int = 7, device="cpu")
 
 @dataclass
 class Int8Workload:
-    """An int8 cache in the layout of `Workload`: pool [NB][2][Hkv][bs][D] of
-    codes, scales [NB][2][Hkv] fp32 (K, V per block and kv head), q and the
-    new rows in `dtype`."""
+    """A quantised cache in the layout of `Workload`: pool [NB][2][Hkv][bs][D]
+    of one-byte codes (int8, or uint8 E4M3 codes for an fp8 cache), scales
+    [NB][2][Hkv] fp32 (K, V per block and kv head), q and the new rows in
+    `dtype`."""
     name: str
     B: int
     H: int
@@ -396,6 +397,24 @@ def to_int8(w: Workload, *, seed: int = 17, scale_range=(0.004, 0.012)) -> Int8W
     return Int8Workload(w.name + "-int8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
                         cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
                         cpu(w.v_new), w.scale, dict(w.meta, int8_seed=seed))
+
+
+def to_fp8(w: Workload, *, seed: int = 19, scale_range=(0.002, 0.006)) -> Int8Workload:
+    """The fp8 (E4M3) counterpart of workload `w` (same shape, table,
+    lengths, q and new rows): seeded uniform bytes over the finite E4M3 codes
+    (the two NaN codes are redrawn as zero) and per-(block, K|V, kv head)
+    scales drawn uniformly from scale_range, so that the values the codes
+    stand for stay within a few units.  The pool is uint8."""
+    gen = torch.Generator().manual_seed(seed)
+    pool = torch.randint(0, 256, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.int32)
+    pool[(pool & 0x7F) == 0x7F] = 0
+    pool = pool.to(torch.uint8)
+    lo, hi = scale_range
+    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32) * (hi - lo) + lo)
+    cpu = lambda t: t.cpu() if isinstance(t, torch.Tensor) else t
+    return Int8Workload(w.name + "-fp8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
+                        cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
+                        cpu(w.v_new), w.scale, dict(w.meta, fp8_seed=seed))
 
 
 def make_prefix_groups(*, group_sizes, shared_blocks, tails, H, Hkv, D, bs, dtype, seed=0,
