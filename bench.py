@@ -53,6 +53,7 @@ KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_
                   "decode_int8": "decode_int8.cu",
                   "decode_int8_tc": "decode_int8_tc.cu",
                   "decode_fp8_tc": "decode_int8_tc.cu",
+                  "decode_fp8": "decode_int8.cu",
                   "decode_prefix_tc": "decode_prefix_tc.cu",
                   "append_tokens": "append.cu"}
 
@@ -313,7 +314,9 @@ def run_gpu(args) -> None:
         tc8 = w.H // w.Hkv >= 2 and w.D in (64, 128) and w.dtype in (torch.float16, torch.bfloat16)
         kernel = "decode_int8_tc" if tc8 else "decode_int8"
     if args.fp8:
-        kernel = "decode_fp8_tc"
+        # grouped-query shapes at head_dim 64/128 on the tensor cores, the
+        # rest on the CUDA cores (the rule of paged_attention_decode_fp8)
+        kernel = "decode_fp8_tc" if w.H // w.Hkv >= 2 and w.D in (64, 128) else "decode_fp8"
     if args.prefill:
         kernel = "append_tokens"
     ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)

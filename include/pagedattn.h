@@ -436,7 +436,7 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
  * for value(c) * s, with the scales laid out and owned exactly as for the
  * int8 cache above.  The pools have the same byte layout; shape->dtype is
  * the element type of q, out, k_new and v_new (fp32, fp16 or bf16); head_dim
- * must be 64 or 128 (other head_dims: PA_ERR_UNSUPPORTED).
+ * must be 64, 128 or 256 (others: PA_ERR_UNSUPPORTED).
  *
  * paged_kv_append_fp8 writes each value x as the E4M3 code of x / s (the
  * quotient in IEEE binary32) nearest to it, ties to the even code,
@@ -446,10 +446,11 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
  * paged_attention_decode_fp8 is paged_attention_decode over the values the
  * codes stand for ([PG] s2.2): x_t = scale * s_K * <q, value(c_t)>, out =
  * sum_t w_t s_V value(c_t) / sum_t w_t.  Same device checks, zeros and
- * PA_DEVERR_* bits.  Every group size runs on the tensor cores: codes are
- * converted to exact fp16 in registers and queries are rounded to fp16
- * (held to the 16-bit tolerance whatever q's dtype).  Codes that are NaN
- * make the outputs of their (sequence, kv head) NaN.
+ * PA_DEVERR_* bits.  Grouped-query shapes at head_dim 64 or 128 run on the
+ * tensor cores (codes converted to exact fp16 in registers, queries rounded
+ * to fp16); the rest on the CUDA cores in fp32.  Results are held to the
+ * 16-bit tolerance whatever q's dtype.  A NaN code inside the attended
+ * length makes the outputs it meets NaN.
  */
 pa_status paged_kv_append_fp8(const pa_shape *shape, const void *k_new, const void *v_new,
                               uint8_t *k_pool, uint8_t *v_pool, const float *kv_scales,

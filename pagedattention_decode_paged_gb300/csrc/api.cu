@@ -819,6 +819,9 @@ pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const voi
     p.num_partitions = 1;
     p.table_cap = shape->max_blocks_per_seq < kTableCap ? shape->max_blocks_per_seq : kTableCap;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = shape->num_heads / shape->num_kv_heads >= 2 &&
+                    (shape->head_dim == 64 || shape->head_dim == 128);
+    if (!tc) return pa::launch_decode_fp8_simt(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
     if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))

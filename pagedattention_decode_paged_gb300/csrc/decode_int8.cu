@@ -68,8 +68,19 @@ struct I8Smem {
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 12; }   // ids, scale_K, scale_V
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
+// Two E4M3 codes (bytes 0 and 1 of v) as floats.
+__device__ __forceinline__ float2 e4m3x2_float2(uint32_t v) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xFFFFu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+// The kernel body for int8 codes or (FP8) E4M3 codes.  The E4M3 variant
+// keeps the query in fp32 and turns each code into fp32 (two codes per
+// conversion to an exact fp16 pair), then uses the packed fp32 FMAs of the
+// 16-bit kernel for both contractions; rows past the length are skipped in
+// P.V, since their stale bytes may be NaN codes.
+template <typename T, int D, bool FP8>
+__device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const float *kv_scales) {
     grid_dependency_wait();
     allow_dependents();
     using C = I8Cfg<D>;
@@ -177,7 +188,14 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
     // products (dp2a), exact, with one conversion per row of 16 codes
     uint32_t qpk[C::VEC / 2];
     float q_unit;
-    {
+    float2 qf2[C::VEC / 2];   // the query as fp32 pairs (FP8)
+    if constexpr (FP8) {
+        const T *qrow = reinterpret_cast<const T *>(p.q) + bh * D + c * C::VEC;
+#pragma unroll
+        for (int e = 0; e < C::VEC / 2; ++e)
+            qf2[e] = make_float2(Elem<T>::to_float(qrow[2 * e]), Elem<T>::to_float(qrow[2 * e + 1]));
+        q_unit = 1.f;
+    } else {
         const T *qrow = reinterpret_cast<const T *>(p.q) + bh * D + c * C::VEC;
         float qf[C::VEC];
         float qmax = 0.f;
@@ -225,14 +243,25 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
 #pragma unroll
         for (int j = 0; j < C::NVALS; ++j) {
             const uint4 kv = *reinterpret_cast<const uint4 *>(ks + (j * C::RPW + r) * C::ROWB + c * 16);
-            const int w[4] = {(int)kv.x, (int)kv.y, (int)kv.z, (int)kv.w};
-            int a = 0;
+            if constexpr (FP8) {
+                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+                float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                a = __dp2a_lo((int)qpk[2 * e], w[e], a);
-                a = __dp2a_hi((int)qpk[2 * e + 1], w[e], a);
+                for (int e = 0; e < 4; ++e) {
+                    a2 = __ffma2_rn(qf2[2 * e], e4m3x2_float2(w[e]), a2);
+                    a2 = __ffma2_rn(qf2[2 * e + 1], e4m3x2_float2(w[e] >> 16), a2);
+                }
+                v[j] = a2.x + a2.y;
+            } else {
+                const int w[4] = {(int)kv.x, (int)kv.y, (int)kv.z, (int)kv.w};
+                int a = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a = __dp2a_lo((int)qpk[2 * e], w[e], a);
+                    a = __dp2a_hi((int)qpk[2 * e + 1], w[e], a);
+                }
+                v[j] = (float)a * q_unit;
             }
-            v[j] = (float)a * q_unit;
         }
         Butterfly<C::NVALS, C::LPT / 2>::run(v, lane);
 
@@ -264,6 +293,25 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
             pj[j] = f.x; pj[j + 1] = f.y; pj[j + 2] = f.z; pj[j + 3] = f.w;
             pjs[j] = g.x; pjs[j + 1] = g.y; pjs[j + 2] = g.z; pjs[j + 3] = g.w;
         }
+        if constexpr (FP8) {
+            // P.V in fp32: each row's codes as fp32 pairs, times its weight
+            // (times the V scale of its block); rows past the length skipped
+            const float2 corr2 = make_float2(corr, corr);
+#pragma unroll
+            for (int e = 0; e < C::VEC / 2; ++e) acc2[e] = __fmul2_rn(acc2[e], corr2);
+#pragma unroll
+            for (int j = 0; j < C::NVALS; ++j) {
+                if (j * C::RPW + r >= nrows) continue;
+                const uint4 vv = *reinterpret_cast<const uint4 *>(vs + (j * C::RPW + r) * C::ROWB + c * 16);
+                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+                const float2 p2 = make_float2(pjs[j], pjs[j]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc2[2 * e] = __ffma2_rn(p2, e4m3x2_float2(w[e]), acc2[2 * e]);
+                    acc2[2 * e + 1] = __ffma2_rn(p2, e4m3x2_float2(w[e] >> 16), acc2[2 * e + 1]);
+                }
+            }
+        } else {
         // P.V in integers: the weights times the V scales of their blocks
         // become int16 with one power-free step per tile (largest = 16383),
         // two tokens' codes of each column are interleaved by a byte
@@ -300,6 +348,7 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
         for (int e = 0; e < C::VEC / 2; ++e)
             acc2[e] = __ffma2_rn(acc2[e], corr2,
                                  make_float2((float)acc_i[2 * e] * from_int, (float)acc_i[2 * e + 1] * from_int));
+        }
         float psum = 0.f;
 #pragma unroll
         for (int j = 0; j < C::NVALS; ++j) psum += pj[j];
@@ -358,6 +407,16 @@ __global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kern
         for (int w = 0; w < kI8Warps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
         out[bh * D + d] = Elem<T>::from_float(bad ? 0.f : a * inv);
     }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_int8_kernel(DecodeParams p, const float *kv_scales) {
+    codes_simt_body<T, D, false>(p, kv_scales);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kI8Warps * 32, 12 / kI8Warps) decode_fp8_kernel(DecodeParams p, const float *kv_scales) {
+    codes_simt_body<T, D, true>(p, kv_scales);
 }
 
 // ---------------------------------------------------------------------------
@@ -442,12 +501,12 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(AppendParams p, const f
 // host side
 // ---------------------------------------------------------------------------
 
-template <typename T, int D>
+template <typename T, int D, bool FP8>
 static cudaError_t launch_int8_t(const DecodeParams &params, const float *kv_scales, cudaStream_t stream) {
     DecodeParams p = params;
     p.table_cap = min(p.table_cap, kI8TableCap);
     const size_t smem = I8Smem<D>::bytes(p.table_cap);
-    auto kern = decode_int8_kernel<T, D>;
+    auto kern = FP8 ? decode_fp8_kernel<T, D> : decode_int8_kernel<T, D>;
     static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
@@ -456,12 +515,12 @@ static cudaError_t launch_int8_t(const DecodeParams &params, const float *kv_sca
     return launch_clustered(kern, grid, kI8Warps * 32, smem, 1, stream, p, kv_scales);
 }
 
-template <typename T>
+template <typename T, bool FP8>
 static cudaError_t launch_int8_d(const DecodeParams &p, const float *kv_scales, cudaStream_t stream) {
     switch (p.D) {
-        case 64: return launch_int8_t<T, 64>(p, kv_scales, stream);
-        case 128: return launch_int8_t<T, 128>(p, kv_scales, stream);
-        case 256: return launch_int8_t<T, 256>(p, kv_scales, stream);
+        case 64: return launch_int8_t<T, 64, FP8>(p, kv_scales, stream);
+        case 128: return launch_int8_t<T, 128, FP8>(p, kv_scales, stream);
+        case 256: return launch_int8_t<T, 256, FP8>(p, kv_scales, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -474,9 +533,19 @@ bool int8_supported(int dtype, int head_dim) {
 cudaError_t launch_decode_int8(int dtype, const DecodeParams &p, const float *kv_scales,
                                cudaStream_t stream) {
     switch (dtype) {
-        case PA_F32: return launch_int8_d<float>(p, kv_scales, stream);
-        case PA_F16: return launch_int8_d<__half>(p, kv_scales, stream);
-        case PA_BF16: return launch_int8_d<__nv_bfloat16>(p, kv_scales, stream);
+        case PA_F32: return launch_int8_d<float, false>(p, kv_scales, stream);
+        case PA_F16: return launch_int8_d<__half, false>(p, kv_scales, stream);
+        case PA_BF16: return launch_int8_d<__nv_bfloat16, false>(p, kv_scales, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_fp8_simt(int dtype, const DecodeParams &p, const float *kv_scales,
+                                   cudaStream_t stream) {
+    switch (dtype) {
+        case PA_F32: return launch_int8_d<float, true>(p, kv_scales, stream);
+        case PA_F16: return launch_int8_d<__half, true>(p, kv_scales, stream);
+        case PA_BF16: return launch_int8_d<__nv_bfloat16, true>(p, kv_scales, stream);
     }
     return cudaErrorInvalidValue;
 }

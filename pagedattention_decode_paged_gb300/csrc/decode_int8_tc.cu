@@ -491,7 +491,8 @@ bool int8_tc_supported(int dtype, int head_dim) {
 }
 
 bool fp8_supported(int dtype, int head_dim) {
-    return (dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16) && (head_dim == 64 || head_dim == 128);
+    return (dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16) &&
+           (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
 
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,

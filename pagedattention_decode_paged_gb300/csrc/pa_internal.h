@@ -245,9 +245,12 @@ bool int8_tc_supported(int dtype, int head_dim);
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream);
-// The fp8 (E4M3) cache: every group size, head_dim 64/128, queries of any
-// of the three dtypes, on the tensor-core code kernel.
+// The fp8 (E4M3) cache: head_dim 64/128/256, queries of any of the three
+// dtypes; grouped-query shapes at head_dim 64/128 on the tensor-core code
+// kernel, the rest on the CUDA-core code kernel.
 bool fp8_supported(int dtype, int head_dim);
+cudaError_t launch_decode_fp8_simt(int dtype, const DecodeParams &p, const float *kv_scales,
+                                   cudaStream_t stream);
 cudaError_t launch_decode_fp8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                  const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                  cudaStream_t stream);

@@ -3,9 +3,10 @@ scales) against the CPU oracle: the quantising append is compared code for
 code (the rounding rule decides the codes, so it must be bit-exact,
 including ties, subnormals and saturated values), and decode attention over
 the codes within the 16-bit tolerance, on the five workloads' shapes,
-ragged lengths, both head_dims, every query dtype and group size, odd block
-sizes (row-by-row copies), long sequences and the device-side error
-handling."""
+ragged lengths, every head_dim and query dtype, both kernels (tensor cores
+for grouped queries, CUDA cores for MHA and head_dim 256), odd block sizes
+(row-by-row copies), NaN codes past the length, long sequences and the
+device-side error handling."""
 import numpy as np
 import pytest
 import torch
@@ -84,7 +85,7 @@ LENS = [0, 1, 15, 16, 17, 31, 33, 64, 100, 257]
 
 
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_fp8_every_head_dim_and_query_dtype(dtype, D):
     w = workloads.to_fp8(workloads.make_generic(B=len(LENS), H=3, Hkv=3, D=D, bs=16, dtype=dtype,
                                                 lens=LENS, seed=D, poison=False), seed=D)
@@ -101,18 +102,19 @@ def test_fp8_block_sizes(bs):
 @pytest.mark.parametrize("H,Hkv,dtype,D,bs", [(8, 2, BF16, 128, 16), (16, 1, BF16, 128, 16),
                                               (64, 8, BF16, 128, 16), (48, 2, F16, 128, 16),
                                               (16, 2, F16, 64, 8), (8, 1, F16, 64, 16),
-                                              (8, 2, BF16, 128, 3), (8, 2, F32, 128, 16)])
+                                              (8, 2, BF16, 128, 3), (8, 2, F32, 128, 16),
+                                              (8, 2, BF16, 256, 16)])
 def test_fp8_grouped_query(H, Hkv, dtype, D, bs):
     w = workloads.to_fp8(workloads.make_generic(B=len(LENS), H=H, Hkv=Hkv, D=D, bs=bs, dtype=dtype,
                                                 lens=LENS, seed=H + bs, poison=False), seed=H)
     run_step(w)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_fp8_long_sequences(D):
-    """More blocks than the kernel stages in shared memory."""
+@pytest.mark.parametrize("D,H,Hkv", [(64, 8, 2), (128, 8, 2), (128, 2, 2)])
+def test_fp8_long_sequences(D, H, Hkv):
+    """More blocks than the kernels stage in shared memory."""
     lens = [9000, 17, 8200]
-    w = workloads.to_fp8(workloads.make_generic(B=len(lens), H=8, Hkv=2, D=D, bs=16, dtype=BF16,
+    w = workloads.to_fp8(workloads.make_generic(B=len(lens), H=H, Hkv=Hkv, D=D, bs=16, dtype=BF16,
                                                 lens=lens, seed=D + 1, poison=False), seed=D)
     run_step(w)
 
@@ -204,7 +206,7 @@ def test_fp8_equals_16bit_decode_on_exactly_representable_values():
     hz.assert_close(a, b.double().cpu().numpy(), BF16, "fp8 vs bf16 path")
 
 
-@pytest.mark.parametrize("bs,H,Hkv", [(16, 4, 4), (8, 8, 2), (3, 8, 2), (32, 16, 2)])
+@pytest.mark.parametrize("bs,H,Hkv", [(16, 4, 4), (8, 8, 2), (3, 8, 2), (32, 16, 2), (8, 4, 4), (3, 2, 2)])
 def test_fp8_nan_codes_past_the_length_are_ignored(bs, H, Hkv):
     """Slots past each sequence's length (in its last block, and in blocks
     nobody owns) hold NaN codes, as an unwritten pool may: they are never

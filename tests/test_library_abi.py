@@ -210,8 +210,8 @@ def test_fp8_rejects_bad_arguments(lib):
     app = lib.paged_kv_append_fp8
     ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # out, q, k_pool, v_pool, scales, table, lens
     assert dec(None, *ok, 0.1, None, None) == pa.PA_ERR_INVALID_ARG
-    # head_dim 64 and 128 only (256 runs on the int8 path but not here)
-    for D in (32, 96, 256):
+    # head_dim 64, 128 and 256 only
+    for D in (32, 96, 512):
         assert dec(ctypes.byref(base_shape(head_dim=D, block_stride=2 * 2 * 16 * D)), *ok, 0.1, None, None) \
             == pa.PA_ERR_UNSUPPORTED
         assert app(ctypes.byref(base_shape(head_dim=D, block_stride=2 * 2 * 16 * D)), *ok, None, None) \
