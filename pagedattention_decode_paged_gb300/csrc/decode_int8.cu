@@ -1,4 +1,5 @@
-// decode_int8.cu -- the int8 KV cache: quantising append and decode attention.
+// decode_int8.cu -- the int8 KV cache (and the fp8 E4M3 cache): quantising
+// append and decode attention on the CUDA cores.
 //
 // The pages name int8-quantised cache blocks ("KV Cache and BlockManager",
 // dpshk.com/news/5906718, s6.3; the "quantized" element size in its s3
@@ -24,6 +25,12 @@
 // (relative error of the largest weight below 2^-14), and meets the V codes
 // in dp2a as well, two tokens per instruction.  Both scales of every block
 // of the sequence are staged in shared memory next to its block-table row.
+//
+// The fp8 cache (OCP FP8 E4M3 codes with the same scales) shares the append
+// (hardware conversion with saturation instead of rounding to integers) and
+// this kernel's structure (decode_fp8_kernel): there the query stays fp32,
+// codes become fp32 through exact fp16 pairs, and both contractions use the
+// packed fp32 FMAs.
 #include <cuda_fp8.h>
 #include <math.h>
 

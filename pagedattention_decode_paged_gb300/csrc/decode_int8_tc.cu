@@ -1,5 +1,5 @@
-// decode_int8_tc.cu -- grouped-query decode over the int8 cache on the tensor
-// cores.
+// decode_int8_tc.cu -- grouped-query decode over the int8 cache (and the fp8
+// E4M3 cache) on the tensor cores.
 //
 // The int8 cache of decode_int8.cu (codes c in [-127, 127] standing for
 // c * s, one fp32 scale per (block, kv head) for K and one for V) read by one
@@ -28,6 +28,12 @@
 //   consecutive codes of each of its 4 tokens.
 // The K scale of each row's block multiplies its scores and the V scale its
 // weights (the ROWSCALE tile step); queries are rounded to fp16.
+//
+// decode_fp8_tc_kernel is the same body over E4M3 codes: the hardware
+// conversion cvt.rn.f16x2.e4m3x2 turns two codes into an exact fp16 pair
+// (bytes 0 and 1 of a word, then bytes 2 and 3), so the fragment layout and
+// the query order are those above with no bias.  Rows past the length are
+// cleared before P.V, since unwritten pool bytes may be NaN codes.
 #include <cuda_fp8.h>
 #include <math.h>
 
