@@ -681,6 +681,15 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
 
 // Shape checks of the int8 entry points: pools of one byte per element whose
 // rows (head_dim bytes) and blocks start on 16-byte boundaries.
+// CTAs per (sequence, head) for the CUDA-core code kernels (int8, fp8): the
+// rule of the 16-bit single pass, on their 4 KB tiles of codes.
+static int code_simt_cluster(const pa_shape *s) {
+    const int64_t units = (int64_t)s->batch * s->num_heads;
+    const int tile = 4096 / s->head_dim;
+    const int64_t max_tiles = ((int64_t)s->max_blocks_per_seq * s->block_size + tile - 1) / tile;
+    return choose_cluster(units, max_tiles);
+}
+
 static pa_status check_fp8_shape(const pa_shape *s) {
     pa_status st = check_shape(s);
     if (st != PA_OK) return st;
@@ -754,7 +763,10 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tc = shape->num_heads / shape->num_kv_heads >= 2 &&
                     pa::int8_tc_supported(shape->dtype, shape->head_dim);
-    if (!tc) return pa::launch_decode_int8(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (!tc) {
+        p.cluster = code_simt_cluster(shape);
+        return pa::launch_decode_int8(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
     if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
@@ -821,7 +833,10 @@ pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const voi
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tc = shape->num_heads / shape->num_kv_heads >= 2 &&
                     (shape->head_dim == 64 || shape->head_dim == 128);
-    if (!tc) return pa::launch_decode_fp8_simt(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (!tc) {
+        p.cluster = code_simt_cluster(shape);
+        return pa::launch_decode_fp8_simt(shape->dtype, p, kv_scales, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
     if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))

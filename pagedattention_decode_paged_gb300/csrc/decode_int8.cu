@@ -71,7 +71,8 @@ struct I8Smem {
     static constexpr size_t kP = (size_t)kI8Warps * C::TILE * 4 * 2;   // weights, and weights * scale_V
     static constexpr size_t kRed = (size_t)kI8Warps * (D + 2) * 4;
     static constexpr size_t kFlags = 16;
-    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags;
+    static constexpr size_t kXchg = (size_t)(D + 4) * 4;   // CTA result read by the cluster leader
+    static constexpr size_t kFixed = kStages + kBars + kP + kRed + kFlags + kXchg;
     static size_t bytes(int table_cap) { return kFixed + (size_t)table_cap * 12; }   // ids, scale_K, scale_V
 };
 
@@ -101,14 +102,24 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
     float *red_l = red_m + kI8Warps;
     float *red_acc = red_l + kI8Warps;
     int *flags = reinterpret_cast<int *>(smem + L::kStages + L::kBars + L::kP + L::kRed);
+    float *xchg = reinterpret_cast<float *>(smem + L::kStages + L::kBars + L::kP + L::kRed + L::kFlags);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kFixed);
     float *sk_tab = reinterpret_cast<float *>(tbl + p.table_cap);
     float *sv_tab = sk_tab + p.table_cap;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x % p.B;
-    const int h = blockIdx.x / p.B;
+    // a unit (sequence, head) may be spread over the CTAs of a thread-block
+    // cluster when the launch has fewer units than SMs; its tiles then go
+    // round-robin to all the cluster's warps and the leader merges the CTAs'
+    // states through distributed shared memory
+    const int csize = (int)cluster_size();
+    const int crank = (int)cluster_rank();
+    const int vwarp = crank * kI8Warps + warp;
+    const int nvw = csize * kI8Warps;
+    const int unit = blockIdx.x / csize;
+    const int b = unit % p.B;
+    const int h = unit / p.B;
     const int hk = h / (p.H / p.Hkv);
     const int64_t bh = (int64_t)b * p.H + h;
     T *out = reinterpret_cast<T *>(p.out);
@@ -143,7 +154,7 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
     __syncthreads();
 
     const int ntiles = (len + C::TILE - 1) / C::TILE;
-    const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kI8Warps + 1 : 0;
+    const int my_tiles = vwarp < ntiles ? (ntiles - 1 - vwarp) / nvw + 1 : 0;
     const int r = lane / C::LPT;   // row group
     const int c = lane % C::LPT;   // 16-byte column
     const int64_t head_off = (int64_t)hk * p.bs * C::ROWB;
@@ -157,7 +168,7 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
 
     // lane 0 of the warp fetches local tile k into ring slot k % S
     auto issue = [&](int k) {
-        const int t0 = (warp + k * kI8Warps) * C::TILE;
+        const int t0 = (vwarp + k * nvw) * C::TILE;
         const int t1 = min(t0 + C::TILE, len);
         const int slot = k % S;
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * S + slot) * 2) * kTileBytes);
@@ -241,7 +252,7 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
         }
         const unsigned char *ks = stages + (size_t)((warp * S + slot) * 2) * kTileBytes;
         const unsigned char *vs = ks + kTileBytes;
-        const int t0 = (warp + k * kI8Warps) * C::TILE;
+        const int t0 = (vwarp + k * nvw) * C::TILE;
         const int nrows = min(C::TILE, len - t0);
 
         // scores: partial dot products of 8 rows (integer, exact), then the
@@ -407,6 +418,44 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
         wsc[w] = merge_weight(red_m[w], M);
         lsum = fmaf(red_l[w], wsc[w], lsum);
     }
+    if (csize > 1) {
+        // publish this CTA's state, then the leader merges the cluster
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kI8Warps; ++w) a = fmaf(red_acc[w * D + d], wsc[w], a);
+            xchg[d] = a;
+        }
+        if (threadIdx.x == 0) {
+            xchg[D] = M;
+            xchg[D + 1] = lsum;
+            xchg[D + 2] = bad ? 1.f : 0.f;
+        }
+        cluster_sync();
+        if (crank == 0) {
+            float Mc = -INFINITY;
+            bool badc = false;
+            for (int r = 0; r < csize; ++r) {
+                Mc = fmaxf(Mc, dsmem_ld_f32(dsmem_addr(&xchg[D], r)));
+                badc |= dsmem_ld_f32(dsmem_addr(&xchg[D + 2], r)) != 0.f;
+            }
+            float lc = 0.f;
+            for (int r = 0; r < csize; ++r)
+                lc = fmaf(dsmem_ld_f32(dsmem_addr(&xchg[D + 1], r)),
+                          merge_weight(dsmem_ld_f32(dsmem_addr(&xchg[D], r)), Mc), lc);
+            const float invc = 1.f / lc;
+            for (int d = threadIdx.x; d < D; d += blockDim.x) {
+                float a = 0.f;
+                for (int r = 0; r < csize; ++r)
+                    a = fmaf(dsmem_ld_f32(dsmem_addr(&xchg[d], r)),
+                             merge_weight(dsmem_ld_f32(dsmem_addr(&xchg[D], r)), Mc), a);
+                out[bh * D + d] = Elem<T>::from_float(badc ? 0.f : a * invc);
+            }
+        }
+        // keep every CTA's shared memory alive until the leader has read it
+        cluster_sync();
+        return;
+    }
     const float inv = 1.f / lsum;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float a = 0.f;
@@ -517,9 +566,10 @@ static cudaError_t launch_int8_t(const DecodeParams &params, const float *kv_sca
     static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)p.B * p.H;
+    const int cluster = max(1, p.cluster);
+    const int64_t grid = (int64_t)p.B * p.H * cluster;
     if (grid == 0) return cudaSuccess;
-    return launch_clustered(kern, grid, kI8Warps * 32, smem, 1, stream, p, kv_scales);
+    return launch_clustered(kern, grid, kI8Warps * 32, smem, cluster, stream, p, kv_scales);
 }
 
 template <typename T, bool FP8>

@@ -110,7 +110,7 @@ def test_fp8_grouped_query(H, Hkv, dtype, D, bs):
     run_step(w)
 
 
-@pytest.mark.parametrize("D,H,Hkv", [(64, 8, 2), (128, 8, 2), (128, 2, 2)])
+@pytest.mark.parametrize("D,H,Hkv", [(64, 8, 2), (128, 8, 2), (128, 2, 2), (256, 3, 3), (64, 2, 2)])
 def test_fp8_long_sequences(D, H, Hkv):
     """More blocks than the kernels stage in shared memory."""
     lens = [9000, 17, 8200]

@@ -109,13 +109,14 @@ def test_int8_grouped_query(H, Hkv, dtype, D, bs):
     run_step8(w)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_int8_grouped_query_long_sequences(D):
-    """Sequences with more blocks than the tensor-core kernel stages in
-    shared memory (the rest of the table and its scales come from global
-    memory)."""
+@pytest.mark.parametrize("D,H,Hkv", [(64, 8, 2), (128, 8, 2), (128, 2, 2), (256, 3, 3)])
+def test_int8_grouped_query_long_sequences(D, H, Hkv):
+    """Sequences with more blocks than the kernels stage in shared memory
+    (the rest of the table and its scales come from global memory); with
+    few (sequence, head) units the CUDA-core kernel spreads each over a
+    thread-block cluster."""
     lens = [9000, 17, 8200]
-    w = workloads.to_int8(workloads.make_generic(B=len(lens), H=8, Hkv=2, D=D, bs=16, dtype=BF16,
+    w = workloads.to_int8(workloads.make_generic(B=len(lens), H=H, Hkv=Hkv, D=D, bs=16, dtype=BF16,
                                                  lens=lens, seed=D + 1, poison=False), seed=D)
     run_step8(w)
 
