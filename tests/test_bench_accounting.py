@@ -1,0 +1,78 @@
+"""The host-side accounting of bench.py, on CPU: the algorithmic byte
+counts that the roofline fraction divides by (valid rows only, shared
+blocks once, the window's rows, the scales of a quantised cache), and the
+lookup of DRAM traffic from the committed ncu summaries, which must refuse a
+summary whose kernel sources have changed."""
+import bench
+import workloads
+
+
+def _tiny(lens, bs=4, H=4, Hkv=2, D=16):
+    return workloads.make_generic(B=len(lens), H=H, Hkv=Hkv, D=D, bs=bs, dtype=workloads.torch.float16,
+                                  lens=lens, seed=1, poison=False)
+
+
+def test_decode_bytes_counts_valid_rows_tables_and_q_out():
+    w = _tiny([5, 0, 9])
+    lens = [5, 0, 9]
+    s = 2   # fp16
+    kv = 2 * w.Hkv * w.D * s * sum(lens)
+    tables = sum(-(-L // w.bs) for L in lens)
+    want = kv + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
+    assert bench.decode_bytes(w, lens) == want
+    assert bench.logical_kv_bytes(w, lens) == kv
+
+
+def test_decode_bytes_window_counts_only_the_last_rows():
+    w = _tiny([9, 3])
+    # window 4 over lengths 9 and 3: rows 5..8 of sequence 0 (blocks 1 and 2),
+    # rows 0..2 of sequence 1 (block 0)
+    s = 2
+    rows = 4 + 3
+    tables = 2 + 1
+    want = 2 * w.Hkv * w.D * s * rows + 4 * tables + 4 * w.B + 2 * w.B * w.H * w.D * s
+    assert bench.decode_bytes(w, [9, 3], window=4) == want
+
+
+def test_decode_bytes_reads_shared_blocks_once():
+    w = _tiny([8, 8])
+    w.block_table[1, :2] = w.block_table[0, :2]   # both sequences share their two blocks
+    s = 2
+    want = 2 * w.Hkv * w.D * s * 8 + 4 * 4 + 4 * w.B + 2 * w.B * w.H * w.D * s
+    assert bench.decode_bytes(w, [8, 8]) == want
+
+
+def test_quantised_cache_counts_one_byte_per_element_and_the_scales():
+    for conv in (workloads.to_int8, workloads.to_fp8):
+        w = conv(_tiny([5, 9]))
+        lens = [5, 9]
+        blocks = sum(-(-L // w.bs) for L in lens)
+        kv = 2 * w.Hkv * w.D * 1 * sum(lens)
+        want = kv + 2 * 4 * w.Hkv * blocks + 4 * blocks + 4 * w.B + 2 * w.B * w.H * w.D * 2
+        assert bench.decode_bytes(w, lens) == want
+        # the append reads the 16-bit rows and their block's two scales and
+        # writes one byte per element
+        assert bench.append_bytes(w) == 2 * w.B * w.Hkv * w.D * (2 + 1) + 2 * 4 * w.B * w.Hkv + 8 * w.B
+
+
+def test_kernel_traffic_refuses_a_stale_summary(tmp_path, monkeypatch):
+    digest = bench.source_digest(bench.KERNEL_SOURCES["decode_simt"])
+    good = tmp_path / "decode_simt__tiny_w9_fused.md"
+    good.write_text(f"source_sha256: {digest}\ndram_bytes_per_launch: 1234\n")
+    stale = tmp_path / "decode_simt__tiny_w8_fused.md"
+    stale.write_text("source_sha256: " + "0" * 64 + "\ndram_bytes_per_launch: 999\n")
+    monkeypatch.setattr(bench, "PROFILE_DIR", tmp_path)
+    assert bench.kernel_traffic("decode_simt", "w9", fused=True) == 1234
+    assert bench.kernel_traffic("decode_simt", "w9", fused=False) is None   # no unfused summary
+    assert bench.kernel_traffic("decode_simt", "w8", fused=True) is None    # sources changed since
+
+
+def test_every_profiled_kernel_has_a_source():
+    """Each kernel bench.py can name maps to a source file whose digest can
+    be taken, and every committed summary names a known kernel."""
+    for name, src in bench.KERNEL_SOURCES.items():
+        assert (bench.ROOT / "pagedattention_decode_paged_gb300" / "csrc" / src).exists(), name
+        assert len(bench.source_digest(src)) == 64
+    for f in bench.PROFILE_DIR.glob("*.md"):
+        kernel = f.name.split("__")[0]
+        assert kernel == "launches" or kernel in bench.KERNEL_SOURCES, f.name
