@@ -174,6 +174,33 @@ __device__ __forceinline__ void codes_simt_body(const DecodeParams &p, const flo
         const uint32_t dst_k = smem_u32(stages + (size_t)((warp * S + slot) * 2) * kTileBytes);
         const uint32_t dst_v = dst_k + kTileBytes;
         const uint32_t bar = smem_u32(&bars[warp * S + slot]);
+        const int j = blk_of(t0);
+        const int in_blk = t0 - j * p.bs;
+        if (in_blk + (t1 - t0) <= 2 * p.bs) {
+            // one or two block segments (a 32-token tile at block_size 16):
+            // both entries are read at once
+            const bool two = in_blk + (t1 - t0) > p.bs;
+            const int32_t b0 = lookup(j), b1 = two ? lookup(j + 1) : 0;
+            const int e0 = two ? (j + 1) * p.bs : t1;   // end of the first segment
+            const uint32_t n0 = (uint32_t)(e0 - t0) * C::ROWB, n1 = (uint32_t)(t1 - e0) * C::ROWB;
+            const bool g0 = good(b0), g1 = !two || good(b1);
+            if (!g0 || !g1) {
+                flags[0] = 1;
+                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+            }
+            mbar_arrive_expect_tx(bar, 2 * ((g0 ? n0 : 0u) + (two && g1 ? n1 : 0u)));
+            if (g0) {
+                const int64_t off = (int64_t)b0 * p.block_stride_bytes + head_off + (int64_t)in_blk * C::ROWB;
+                bulk_g2s(dst_k, p.k_pool + off, n0, bar);
+                bulk_g2s(dst_v, p.v_pool + off, n0, bar);
+            }
+            if (two && g1) {
+                const int64_t off = (int64_t)b1 * p.block_stride_bytes + head_off;
+                bulk_g2s(dst_k + n0, p.k_pool + off, n1, bar);
+                bulk_g2s(dst_v + n0, p.v_pool + off, n1, bar);
+            }
+            return;
+        }
         uint32_t bytes = 0;
         bool ok = true;
         for (int t = t0, jj = blk_of(t0), e; t < t1; t = e, ++jj) {

@@ -186,7 +186,28 @@ __global__ void __launch_bounds__(kSimtWarps * 32, kSimtMinBlocks) decode_simt_k
             bulk_g2s(dst_v, p.v_pool + off, n, bar);
             return;
         }
-        // the tile crosses block boundaries: one copy per block segment
+        if (in_blk + (t1 - t0) <= 2 * p.bs) {
+            // two block segments (block_size 8, or a tile cut by a block
+            // boundary): both entries are read at once, then four copies
+            const int32_t b0 = lookup(j), b1 = lookup(j + 1);
+            const int e0 = (j + 1) * p.bs;   // first token of the second block
+            const uint32_t n0 = (uint32_t)(e0 - t0) * C::ROWB, n1 = (uint32_t)(t1 - e0) * C::ROWB;
+            const bool g0 = good(b0), g1 = good(b1);
+            if (!g0 || !g1) bad_block();
+            mbar_arrive_expect_tx(bar, 2 * ((g0 ? n0 : 0u) + (g1 ? n1 : 0u)));
+            if (g0) {
+                const int64_t off = (int64_t)b0 * p.block_stride_bytes + head_off + (int64_t)in_blk * C::ROWB;
+                bulk_g2s(dst_k, p.k_pool + off, n0, bar);
+                bulk_g2s(dst_v, p.v_pool + off, n0, bar);
+            }
+            if (g1) {
+                const int64_t off = (int64_t)b1 * p.block_stride_bytes + head_off;
+                bulk_g2s(dst_k + n0, p.k_pool + off, n1, bar);
+                bulk_g2s(dst_v + n0, p.v_pool + off, n1, bar);
+            }
+            return;
+        }
+        // more block segments: one copy each
         uint32_t bytes = 0;
         bool ok = true;
         for (int t = t0, jj = j, e; t < t1; t = e, ++jj) {
