@@ -9,15 +9,23 @@
  *   paged_attention_decode          attention of each query head over the
  *                                   sequence's valid tokens, reading K/V
  *                                   through block_table
+ *   paged_attention_decode_append   both in one launch (the usual step)
  *   paged_attention_decode_partial  the same over fixed token partitions,
  *   paged_attention_decode_reduce   then a log-sum-exp merge (split-KV, for
  *                                   long contexts or few sequences)
+ *   paged_attention_decode_split_static  the pair with library-owned scratch
+ *   paged_attention_decode_shared_prefix split-KV that reads blocks shared
+ *                                   by a group of sequences once per group
  *   paged_attention_decode_balanced the same step on a persistent grid with
  *                                   equal work per warp (mixed lengths)
+ *   paged_attention_decode_window   attention over the last W tokens only
+ *   paged_kv_append_tokens          the prompt write (several tokens per
+ *                                   sequence, valid rows only)
  *   paged_kv_append_int8,           the same write and attention over an
  *   paged_attention_decode_int8     int8 cache with per-block scales
  *   paged_kv_append_fp8,            ... over an fp8 (E4M3) cache with
  *   paged_attention_decode_fp8      per-block scales
+ *   *_workspace, pa_status_string   sizes of caller workspaces, messages
  *
  * Sources (web pages on paged KV caches), cited by title and section:
  *   "KV Cache and BlockManager" (dpshk.com/news/5906718)            [BM]
