@@ -41,7 +41,7 @@
 namespace pa {
 
 #ifndef PA_I8_WARPS
-#define PA_I8_WARPS 3
+#define PA_I8_WARPS 2
 #endif
 constexpr int kI8Warps = PA_I8_WARPS;
 constexpr int kI8Stages = 2;
