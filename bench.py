@@ -46,6 +46,7 @@ UNIT = "GB/s"
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 SPLIT_PTOK = {5: 1024}          # workloads timed through split-KV partitions
 SHARED_PREFIX = {5: 4096}       # ... or with the shared prefix read once per group (partition)
+SHARED_PREFIX_CODES = {5: 2048}  # the same over an int8 / fp8 cache (measured best of 1024-4096)
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
                   "decode_simt_balanced": "decode_balanced_simt.cu",
@@ -55,6 +56,8 @@ KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_
                   "decode_fp8_tc": "decode_int8_tc.cu",
                   "decode_fp8": "decode_int8.cu",
                   "decode_prefix_tc": "decode_prefix_tc.cu",
+                  "decode_prefix_int8_tc": "decode_int8_tc.cu",
+                  "decode_prefix_fp8_tc": "decode_int8_tc.cu",
                   "append_tokens": "append.cu"}
 
 
@@ -340,16 +343,16 @@ def run_gpu(args) -> None:
         ptok = None
     groups = None
     if args.shared_prefix is None:
-        args.shared_prefix = args.workload in SHARED_PREFIX and not quant and not args.balanced \
+        args.shared_prefix = args.workload in SHARED_PREFIX and not args.balanced \
             and not args.long_seq and not args.prefill and not window
     if args.shared_prefix:
         if "shared_blocks" not in w.meta:
             raise SystemExit("--shared-prefix needs a workload with a shared prefix (workload 5)")
         groups = {"first": [0, w.B], "shared": [w.meta["shared_blocks"] * w.bs]}
-        ptok = args.split_tokens or SHARED_PREFIX.get(args.workload, 4096)
+        ptok = args.split_tokens or (SHARED_PREFIX_CODES if quant else SHARED_PREFIX).get(args.workload, 4096)
         ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
         fused = False
-        kernel = "decode_prefix_tc"
+        kernel = "decode_prefix_fp8_tc" if args.fp8 else "decode_prefix_int8_tc" if args.int8 else "decode_prefix_tc"
     if balanced:
         ptok = None
         fused = not args.unfused
@@ -388,6 +391,15 @@ def run_gpu(args) -> None:
             calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
                               w.block_table, prefill["start"], w.lens, **kw))
             return calls, []
+        if args.shared_prefix and quant:
+            fn = (pa.paged_attention_decode_shared_prefix_fp8 if args.fp8
+                  else pa.paged_attention_decode_shared_prefix_int8)
+            calls.append(bind(fn, t["out"], t["q"], kflat, vflat, w.scales, t["block_table"], t["lens_after"],
+                              w.scale, ptok, ws, group_first=groups["first"], shared_tokens=groups["shared"],
+                              num_kv_heads=w.Hkv, **kw))
+            app_fn = pa.paged_kv_append_fp8 if args.fp8 else pa.paged_kv_append_int8
+            return calls, [bind(app_fn, t["k_new"], t["v_new"], kflat, vflat, w.scales, t["block_table"],
+                                t["positions"], **kw)]
         if args.shared_prefix:
             calls.append(bind(pa.paged_attention_decode_shared_prefix, t["out"], t["q"], kflat, vflat,
                               t["block_table"], t["lens_after"], w.scale, ptok, ws,

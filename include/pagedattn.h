@@ -25,6 +25,8 @@
  *   paged_attention_decode_int8     int8 cache with per-block scales
  *   paged_kv_append_fp8,            ... over an fp8 (E4M3) cache with
  *   paged_attention_decode_fp8      per-block scales
+ *   paged_attention_decode_shared_prefix_int8, _fp8  the shared-prefix
+ *                                   split-KV over those two caches
  *   *_workspace, pa_status_string   sizes of caller workspaces, messages
  *
  * Sources (web pages on paged KV caches), cited by title and section:
@@ -470,6 +472,45 @@ pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const voi
                                      const float *kv_scales, const int32_t *block_table,
                                      const int32_t *seq_lens, float scale, int32_t *err_word,
                                      pa_stream_t stream);
+
+/*
+ * paged_attention_decode_shared_prefix_int8 / _fp8 -- the shared-prefix
+ * split-KV pair of paged_attention_decode_shared_prefix over the int8 or fp8
+ * cache above ([KB] s3.4 for the sharing, [PG] s2.2 for the per-block
+ * decomposition and its merge).
+ *
+ * Groups, partitions, workspace (paged_attention_partial_workspace), device
+ * checks, PA_DEVERR_BAD_PREFIX and the merge are exactly those of
+ * paged_attention_decode_shared_prefix; the per-token arithmetic is that of
+ * paged_attention_decode_int8 / _fp8 on their tensor-core kernel (codes
+ * turned into exact fp16 in registers, queries rounded to fp16), for every
+ * unit, with one query column per (member, query head of the kv head), at
+ * most 16.  The result is paged_attention_decode_int8's / _fp8's up to
+ * rounding order and held to the same tolerance.  Shapes: head_dim 64 or
+ * 128; q of fp16 or bf16 (int8), or fp32, fp16 or bf16 (fp8); any block size
+ * (tensor boxes where it is 8 or a multiple of 16, row copies otherwise);
+ * num_heads/num_kv_heads <= 16.  Others give PA_ERR_UNSUPPORTED.  Two
+ * launches on `stream`.
+ */
+pa_status paged_attention_decode_shared_prefix_int8(const pa_shape *shape, void *out, const void *q,
+                                                    const int8_t *k_pool, const int8_t *v_pool,
+                                                    const float *kv_scales, const int32_t *block_table,
+                                                    const int32_t *seq_lens, int32_t num_groups,
+                                                    const int32_t *group_first,
+                                                    const int32_t *shared_tokens, float scale,
+                                                    int32_t partition_tokens, void *workspace,
+                                                    size_t workspace_bytes, int32_t *err_word,
+                                                    pa_stream_t stream);
+
+pa_status paged_attention_decode_shared_prefix_fp8(const pa_shape *shape, void *out, const void *q,
+                                                   const uint8_t *k_pool, const uint8_t *v_pool,
+                                                   const float *kv_scales, const int32_t *block_table,
+                                                   const int32_t *seq_lens, int32_t num_groups,
+                                                   const int32_t *group_first,
+                                                   const int32_t *shared_tokens, float scale,
+                                                   int32_t partition_tokens, void *workspace,
+                                                   size_t workspace_bytes, int32_t *err_word,
+                                                   pa_stream_t stream);
 
 /*
  * paged_attention_decode_split_static -- the split-KV pair without any

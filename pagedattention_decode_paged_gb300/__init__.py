@@ -41,7 +41,8 @@ EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attentio
             "paged_attention_balanced_workspace", "paged_attention_decode_balanced",
             "paged_kv_append_int8", "paged_attention_decode_int8",
             "paged_kv_append_fp8", "paged_attention_decode_fp8",
-            "paged_attention_decode_shared_prefix")
+            "paged_attention_decode_shared_prefix", "paged_attention_decode_shared_prefix_int8",
+            "paged_attention_decode_shared_prefix_fp8")
 
 
 class PagedAttnError(RuntimeError):
@@ -102,6 +103,10 @@ def load() -> ctypes.CDLL:
             lib.paged_attention_decode_shared_prefix.restype = ctypes.c_int
             lib.paged_attention_decode_shared_prefix.argtypes = [sp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
                                                                  f32, i32, vp, sz, vp, vp]
+            for name in ("paged_attention_decode_shared_prefix_int8", "paged_attention_decode_shared_prefix_fp8"):
+                fn = getattr(lib, name)
+                fn.restype = ctypes.c_int
+                fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, f32, i32, vp, sz, vp, vp]
             lib.paged_kv_append_int8.restype = ctypes.c_int
             lib.paged_kv_append_int8.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.paged_attention_decode_int8.restype = ctypes.c_int
@@ -420,3 +425,43 @@ def paged_attention_decode_shared_prefix(out, q, k_pool, v_pool, block_table, se
             _stream(stream))
     return _issue(load().paged_attention_decode_shared_prefix, args,
                   "paged_attention_decode_shared_prefix", prepare, (shape, first, shared))
+
+
+def _shared_prefix_codes(name, out, q, k_pool, v_pool, kv_scales, block_table, seq_lens, scale,
+                         partition_tokens, workspace, group_first, shared_tokens, num_kv_heads,
+                         block_size, num_blocks, block_stride, err_word, stream, prepare):
+    shape = decode_shape(q, block_table, num_kv_heads=num_kv_heads, block_size=block_size,
+                         num_blocks=num_blocks, block_stride=block_stride)
+    n = len(shared_tokens)
+    first = (ctypes.c_int32 * (n + 1))(*[int(x) for x in group_first])
+    shared = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in shared_tokens])
+    nbytes = workspace.numel() * workspace.element_size()
+    args = (ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_scales),
+            _ptr(block_table), _ptr(seq_lens), n, ctypes.cast(first, ctypes.c_void_p),
+            ctypes.cast(shared, ctypes.c_void_p), float(scale), int(partition_tokens), _ptr(workspace),
+            nbytes, _ptr(err_word), _stream(stream))
+    return _issue(getattr(load(), name), args, name, prepare, (shape, first, shared))
+
+
+def paged_attention_decode_shared_prefix_int8(out, q, k_pool, v_pool, kv_scales, block_table, seq_lens,
+                                              scale, partition_tokens, workspace, *, group_first,
+                                              shared_tokens, num_kv_heads, block_size, num_blocks,
+                                              block_stride, err_word=None, stream=None, prepare=False):
+    """paged_attention_decode_shared_prefix over an int8 cache with
+    per-(block, kv head) scales (host group lists)."""
+    return _shared_prefix_codes("paged_attention_decode_shared_prefix_int8", out, q, k_pool, v_pool,
+                                kv_scales, block_table, seq_lens, scale, partition_tokens, workspace,
+                                group_first, shared_tokens, num_kv_heads, block_size, num_blocks,
+                                block_stride, err_word, stream, prepare)
+
+
+def paged_attention_decode_shared_prefix_fp8(out, q, k_pool, v_pool, kv_scales, block_table, seq_lens,
+                                             scale, partition_tokens, workspace, *, group_first,
+                                             shared_tokens, num_kv_heads, block_size, num_blocks,
+                                             block_stride, err_word=None, stream=None, prepare=False):
+    """paged_attention_decode_shared_prefix over an fp8 (E4M3) cache with
+    per-(block, kv head) scales (host group lists)."""
+    return _shared_prefix_codes("paged_attention_decode_shared_prefix_fp8", out, q, k_pool, v_pool,
+                                kv_scales, block_table, seq_lens, scale, partition_tokens, workspace,
+                                group_first, shared_tokens, num_kv_heads, block_size, num_blocks,
+                                block_stride, err_word, stream, prepare)

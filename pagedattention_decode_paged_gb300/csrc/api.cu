@@ -597,23 +597,26 @@ pa_status paged_attention_decode_balanced(const pa_shape *shape, void *out, cons
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out, const void *q,
-                                               const void *k_pool, const void *v_pool,
-                                               const int32_t *block_table,
-                                               const int32_t *seq_lens, int32_t num_groups,
-                                               const int32_t *group_first,
-                                               const int32_t *shared_tokens, float scale,
-                                               int32_t partition_tokens, void *workspace,
-                                               size_t workspace_bytes, int32_t *err_word,
-                                               pa_stream_t stream) {
-    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
-    if (st != PA_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// Checks of the shared-prefix arguments that come before any pointer check.
+pa_status prefix_args(int32_t num_groups, const int32_t *group_first, const int32_t *shared_tokens,
+                      float scale, int32_t partition_tokens) {
     if (partition_tokens <= 0 || partition_tokens % 16 != 0) return PA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (num_groups < 0 || num_groups > pa::kMaxPrefixGroups) return PA_ERR_INVALID_ARG;
     if (num_groups > 0 && (group_first == nullptr || shared_tokens == nullptr)) return PA_ERR_INVALID_ARG;
-    if (shape->batch == 0) return PA_OK;
-    if (!tc_layout_ok(shape)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// The part of a shared-prefix call that does not depend on the cache format:
+// the workspace slots, the partitions and the groups (into p), and the widest
+// unit's query columns.
+pa_status prefix_plan(const pa_shape *shape, void *out, int32_t num_groups, const int32_t *group_first,
+                      const int32_t *shared_tokens, int32_t partition_tokens, void *workspace,
+                      size_t workspace_bytes, pa::DecodeParams *p, int *widest_out) {
     if (out == nullptr || workspace == nullptr) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(workspace)) return PA_ERR_MISALIGNED;
     const int64_t P = num_partitions(shape, partition_tokens);
@@ -640,24 +643,22 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
     }
     if (num_groups > 0) groups.first[num_groups] = group_first[num_groups];
 
-    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
     char *ws = static_cast<char *>(workspace);
-    p.ws_m = reinterpret_cast<float *>(ws + w.off_m);
-    p.ws_l = reinterpret_cast<float *>(ws + w.off_l);
-    p.ws_acc = reinterpret_cast<float *>(ws + w.off_acc);
-    p.partition_tokens = partition_tokens;
-    p.num_partitions = (int32_t)P;
+    p->ws_m = reinterpret_cast<float *>(ws + w.off_m);
+    p->ws_l = reinterpret_cast<float *>(ws + w.off_l);
+    p->ws_acc = reinterpret_cast<float *>(ws + w.off_acc);
+    p->partition_tokens = partition_tokens;
+    p->num_partitions = (int32_t)P;
     const int64_t need = partition_tokens / shape->block_size + 2;
-    p.table_cap = (int)(need < kTableCap ? need : kTableCap);
-    p.groups = groups;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    p->table_cap = (int)(need < kTableCap ? need : kTableCap);
+    p->groups = groups;
+    *widest_out = widest;
+    return PA_OK;
+}
 
-    // 1. the shared partitions once per group, every other one per sequence
-    CUtensorMap kmap, vmap;
-    if (!cached_pool_map(&kmap, shape, k_pool) || !cached_pool_map(&vmap, shape, v_pool)) return PA_ERR_CUDA;
-    if (pa::launch_prefix_tc(shape->dtype, p, kmap, vmap, box_rows_for(shape), widest, s) != cudaSuccess)
-        return PA_ERR_CUDA;
-    // 2. the merge
+// The log-sum-exp merge of the partials of a shared-prefix call into out.
+pa_status prefix_reduce(const pa_shape *shape, void *out, const pa::DecodeParams &p, const int32_t *seq_lens,
+                        int32_t *err_word, cudaStream_t s) {
     pa::ReduceParams r{};
     r.out = out;
     r.ws_m = p.ws_m;
@@ -670,9 +671,44 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
     r.D = shape->head_dim;
     r.MB = shape->max_blocks_per_seq;
     r.bs = shape->block_size;
-    r.partition_tokens = partition_tokens;
-    r.num_partitions = (int32_t)P;
+    r.partition_tokens = p.partition_tokens;
+    r.num_partitions = p.num_partitions;
     return pa::launch_reduce(shape->dtype, r, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out, const void *q,
+                                               const void *k_pool, const void *v_pool,
+                                               const int32_t *block_table,
+                                               const int32_t *seq_lens, int32_t num_groups,
+                                               const int32_t *group_first,
+                                               const int32_t *shared_tokens, float scale,
+                                               int32_t partition_tokens, void *workspace,
+                                               size_t workspace_bytes, int32_t *err_word,
+                                               pa_stream_t stream) {
+    pa_status st = check_decode_args(shape, q, k_pool, v_pool, block_table, seq_lens);
+    if (st != PA_OK) return st;
+    st = prefix_args(num_groups, group_first, shared_tokens, scale, partition_tokens);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (!tc_layout_ok(shape)) return PA_ERR_UNSUPPORTED;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    int widest = 0;
+    st = prefix_plan(shape, out, num_groups, group_first, shared_tokens, partition_tokens, workspace,
+                     workspace_bytes, &p, &widest);
+    if (st != PA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // 1. the shared partitions once per group, every other one per sequence
+    CUtensorMap kmap, vmap;
+    if (!cached_pool_map(&kmap, shape, k_pool) || !cached_pool_map(&vmap, shape, v_pool)) return PA_ERR_CUDA;
+    if (pa::launch_prefix_tc(shape->dtype, p, kmap, vmap, box_rows_for(shape), widest, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // 2. the merge
+    return prefix_reduce(shape, out, p, seq_lens, err_word, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -844,6 +880,73 @@ pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const voi
     const cudaError_t e = pa::launch_decode_fp8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
                                                    boxes ? &vmap : nullptr, box_rows_for(shape), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// The shared-prefix pair over an int8 (fp8 false) or fp8 cache: the
+// partials on the tensor-core code kernel, then the 16-bit path's reduce.
+static pa_status shared_prefix_codes(bool fp8, const pa_shape *shape, void *out, const void *q,
+                                     const void *k_pool, const void *v_pool, const float *kv_scales,
+                                     const int32_t *block_table, const int32_t *seq_lens,
+                                     int32_t num_groups, const int32_t *group_first,
+                                     const int32_t *shared_tokens, float scale, int32_t partition_tokens,
+                                     void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                     pa_stream_t stream) {
+    pa_status st = fp8 ? check_fp8_shape(shape) : check_int8_shape(shape);
+    if (st != PA_OK) return st;
+    st = prefix_args(num_groups, group_first, shared_tokens, scale, partition_tokens);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    // the tensor-core code kernel: head_dim 64/128, 16-bit queries for int8
+    if (shape->head_dim != 64 && shape->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!fp8 && !pa::int8_tc_supported(shape->dtype, shape->head_dim)) return PA_ERR_UNSUPPORTED;
+    if (q == nullptr || k_pool == nullptr || v_pool == nullptr || kv_scales == nullptr ||
+        block_table == nullptr || seq_lens == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(kv_scales) & 3u) != 0) return PA_ERR_MISALIGNED;
+    pa::DecodeParams p = base_params(shape, q, k_pool, v_pool, block_table, seq_lens, scale, err_word);
+    p.block_stride_bytes = shape->block_stride;   // one byte per element
+    int widest = 0;
+    st = prefix_plan(shape, out, num_groups, group_first, shared_tokens, partition_tokens, workspace,
+                     workspace_bytes, &p, &widest);
+    if (st != PA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap kmap{}, vmap{};
+    const bool boxes = int8_tc_boxes_ok(shape);
+    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
+        return PA_ERR_CUDA;
+    if (pa::launch_prefix_codes_tc(shape->dtype, fp8, p, kv_scales, boxes ? &kmap : nullptr,
+                                   boxes ? &vmap : nullptr, box_rows_for(shape), widest, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return prefix_reduce(shape, out, p, seq_lens, err_word, s);
+}
+
+pa_status paged_attention_decode_shared_prefix_int8(const pa_shape *shape, void *out, const void *q,
+                                                    const int8_t *k_pool, const int8_t *v_pool,
+                                                    const float *kv_scales, const int32_t *block_table,
+                                                    const int32_t *seq_lens, int32_t num_groups,
+                                                    const int32_t *group_first,
+                                                    const int32_t *shared_tokens, float scale,
+                                                    int32_t partition_tokens, void *workspace,
+                                                    size_t workspace_bytes, int32_t *err_word,
+                                                    pa_stream_t stream) {
+    return shared_prefix_codes(false, shape, out, q, k_pool, v_pool, kv_scales, block_table, seq_lens,
+                               num_groups, group_first, shared_tokens, scale, partition_tokens, workspace,
+                               workspace_bytes, err_word, stream);
+}
+
+pa_status paged_attention_decode_shared_prefix_fp8(const pa_shape *shape, void *out, const void *q,
+                                                   const uint8_t *k_pool, const uint8_t *v_pool,
+                                                   const float *kv_scales, const int32_t *block_table,
+                                                   const int32_t *seq_lens, int32_t num_groups,
+                                                   const int32_t *group_first,
+                                                   const int32_t *shared_tokens, float scale,
+                                                   int32_t partition_tokens, void *workspace,
+                                                   size_t workspace_bytes, int32_t *err_word,
+                                                   pa_stream_t stream) {
+    return shared_prefix_codes(true, shape, out, q, k_pool, v_pool, kv_scales, block_table, seq_lens,
+                               num_groups, group_first, shared_tokens, scale, partition_tokens, workspace,
+                               workspace_bytes, err_word, stream);
 }
 
 }  // extern "C"

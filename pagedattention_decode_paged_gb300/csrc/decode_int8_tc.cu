@@ -34,6 +34,16 @@
 // (bytes 0 and 1 of a word, then bytes 2 and 3), so the fragment layout and
 // the query order are those above with no bias.  Rows past the length are
 // cleared before P.V, since unwritten pool bytes may be NaN codes.
+//
+// decode_prefix_int8_tc_kernel / decode_prefix_fp8_tc_kernel run the same
+// body over the units of the shared-prefix split-KV pair of
+// decode_prefix_tc.cu: sequences forked from one prompt name the same blocks
+// for their common prefix ("KV Block design", vLLM memory-management course,
+// ch. 3, s3.4), so a partition inside a group's shared prefix is read once
+// and contracted with the queries of every member (the MMA columns are then
+// (member, query head)); every other partition is a unit of one sequence.
+// Each unit writes its columns' split-KV workspace slots, which the 16-bit
+// path's reduce merges.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -122,7 +132,16 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v) {
 
 // The kernel body, for int8 codes or (FP8) E4M3 codes: the two differ only
 // in how a word of four codes becomes two fp16 pairs.
-template <typename T, int D, int NT, bool BOXES, bool FP8>
+//
+// A unit is a token range [t_begin, t_end) of one table row attended by up
+// to 16 query columns.  Plain decode (PFX false): one CTA per (sequence, kv
+// head, group of up to 16 query heads) over the whole sequence, writing out.
+// Shared prefix (PFX true): first one CTA per (group, kv head, partition
+// wholly inside the group's shared prefix), whose columns are (member,
+// query head of the kv head) so that each shared tile is read once for the
+// whole group; then one CTA per (sequence, kv head, later partition); each
+// writes the split-KV workspace slot (m, l, acc) of its columns.
+template <typename T, int D, int NT, bool BOXES, bool FP8, bool PFX>
 __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                               const DecodeParams &p, const float *kv_scales, int box_rows) {
     grid_dependency_wait();
@@ -143,31 +162,81 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
     const int gid = lane >> 2;
     const int tig = lane & 3;
     const int g = p.H / p.Hkv;
-    const int ngroups = (g + 15) / 16;
-    int unit = blockIdx.x;
-    const int b = unit % p.B;
-    unit /= p.B;
-    const int hg = unit % ngroups;
-    const int hk = unit / ngroups;
-    const int h0 = hk * g + hg * 16;
-    const int nh = min(16, g - hg * 16);
     T *out = reinterpret_cast<T *>(p.out);
-    const int32_t *trow = p.block_table + (int64_t)b * p.MB;
 
-    const int nspec = min(min(p.MB, p.table_cap), 64);
-    for (int j = threadIdx.x; j < nspec; j += blockDim.x) tbl[j] = trow[j];
-    const int32_t len = p.seq_lens[b];
-    if (len <= 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
-        if (len != 0 && threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
-        for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
-            out[((int64_t)b * p.H + h0) * D + i] = Elem<T>::from_float(0.f);
-        return;
+    int b0, hk, hbase, ncols, t_begin, t_end;
+    int part = 0, nmem = 1, nstaged = 0;
+    bool shared_unit = false;
+    const int32_t *trow;   // the unit's table row
+    if constexpr (PFX) {
+        int n_shared = 0;
+        for (int i = 0; i < p.groups.n; ++i) n_shared += p.groups.parts[i] * p.Hkv;
+        shared_unit = (int)blockIdx.x < n_shared;
+        if (shared_unit) {
+            int unit = blockIdx.x;
+            int grp = 0;
+            while (unit >= p.groups.parts[grp] * p.Hkv) {
+                unit -= p.groups.parts[grp] * p.Hkv;
+                ++grp;
+            }
+            hk = unit % p.Hkv;
+            part = unit / p.Hkv;
+            b0 = p.groups.first[grp];
+            nmem = p.groups.first[grp + 1] - b0;
+            t_begin = part * p.partition_tokens;
+            t_end = t_begin + p.partition_tokens;
+        } else {
+            int unit = blockIdx.x - n_shared;
+            b0 = unit % p.B;
+            unit /= p.B;
+            hk = unit % p.Hkv;
+            part = prefix_parts_of(p.groups, b0) + unit / p.Hkv;
+            const int32_t len = p.seq_lens[b0];
+            // a bad length is the reduce's to report; a partition past the
+            // end is never read by it
+            if (len < 0 || (int64_t)len > (int64_t)p.MB * p.bs) return;
+            t_begin = part * p.partition_tokens;
+            if (part >= p.num_partitions || t_begin >= len) return;
+            t_end = min(len, t_begin + p.partition_tokens);
+        }
+        hbase = hk * g;
+        ncols = nmem * g;
+        trow = p.block_table + (int64_t)b0 * p.MB;
+    } else {
+        const int ngroups = (g + 15) / 16;
+        int unit = blockIdx.x;
+        b0 = unit % p.B;
+        unit /= p.B;
+        const int hg = unit % ngroups;
+        hk = unit / ngroups;
+        hbase = hk * g + hg * 16;
+        ncols = min(16, g - hg * 16);
+        trow = p.block_table + (int64_t)b0 * p.MB;
+        nstaged = min(min(p.MB, p.table_cap), 64);
+        for (int j = threadIdx.x; j < nstaged; j += blockDim.x) tbl[j] = trow[j];
+        const int32_t len = p.seq_lens[b0];
+        if (len <= 0 || (int64_t)len > (int64_t)p.MB * p.bs) {
+            if (len != 0 && threadIdx.x == 0) report(p.err_word, PA_DEVERR_BAD_LEN);
+            for (int i = threadIdx.x; i < ncols * D; i += blockDim.x)
+                out[((int64_t)b0 * p.H + hbase) * D + i] = Elem<T>::from_float(0.f);
+            return;
+        }
+        t_begin = 0;
+        t_end = len;
     }
+    // row of q, out and the workspace for query column c
+    auto qrow = [&](int c) -> int64_t {
+        if constexpr (PFX) return (int64_t)(b0 + c / g) * p.H + hbase + c % g;
+        else return (int64_t)b0 * p.H + hbase + c;
+    };
     auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
     auto blk_of = [&](int t) { return p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs; };
-    const int nblk = (len - 1) / p.bs + 1;
+    // table entries j0 .. j0 + nblk - 1 cover the unit; the first ncache of
+    // them (and their scales) are staged in shared memory
+    const int j0 = blk_of(t_begin);
+    const int nblk = blk_of(t_end - 1) + 1 - j0;
     const int ncache = min(nblk, p.table_cap);
-    for (int j = nspec + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j];
+    for (int j = nstaged + threadIdx.x; j < ncache; j += blockDim.x) tbl[j] = trow[j0 + j];
     if (threadIdx.x == 0) {
         flags[0] = 0;
         if constexpr (BOXES) {
@@ -183,14 +252,35 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
         sk_tab[j] = good(blk) ? kv_scales[((int64_t)blk * 2 + 0) * p.Hkv + hk] : 0.f;
         sv_tab[j] = good(blk) ? kv_scales[((int64_t)blk * 2 + 1) * p.Hkv + hk] : 0.f;
     }
+    // lookups by absolute table index j
+    auto lookup = [&](int j) -> int32_t { return j - j0 < ncache ? tbl[j - j0] : trow[j]; };
+    if constexpr (PFX) {
+        if (shared_unit) {
+            // every member must hold the partition and name the same blocks
+            // for it
+            bool bad = false;
+            const int64_t need = (int64_t)nmem * nblk;
+            for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
+                const int m = (int)(i / nblk), j = (int)(i % nblk);
+                bad |= p.block_table[(int64_t)(b0 + m) * p.MB + j0 + j] != lookup(j0 + j);
+            }
+            for (int m = threadIdx.x; m < nmem; m += blockDim.x) {
+                const int32_t len = p.seq_lens[b0 + m];
+                bad |= len < t_end || (int64_t)len > (int64_t)p.MB * p.bs;
+            }
+            if (bad) {
+                flags[0] = 2;
+                report(p.err_word, PA_DEVERR_BAD_PREFIX);
+            }
+        }
+    }
     __syncthreads();
 
-    const int ntiles = (len + kTcTile - 1) / kTcTile;
+    const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
     const int my_tiles = warp < ntiles ? (ntiles - 1 - warp) / kI8TcWarps + 1 : 0;
     const int64_t head_off = (int64_t)hk * p.bs * D;
-    auto lookup = [&](int j) -> int32_t { return j < ncache ? tbl[j] : trow[j]; };
     auto scale_of = [&](int j, int kv) -> float {
-        if (j < ncache) return kv ? sv_tab[j] : sk_tab[j];
+        if (j - j0 < ncache) return kv ? sv_tab[j - j0] : sk_tab[j - j0];
         const int32_t blk = trow[j];
         return good(blk) ? kv_scales[((int64_t)blk * 2 + kv) * p.Hkv + hk] : 0.f;
     };
@@ -202,7 +292,7 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
     // past the length are not fetched or belong to the last box: their codes
     // are finite and get zero weight.
     auto issue = [&](int k) {
-        const int t0 = (warp + k * kI8TcWarps) * kTcTile;
+        const int t0 = t_begin + (warp + k * kI8TcWarps) * kTcTile;
         if constexpr (BOXES) {
             if (lane != 0) return;
             const int slot = k % S;
@@ -214,7 +304,7 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
             bool bad = false;
             for (int sb = 0; sb < subs; ++sb) {
                 const int t = t0 + sb * box_rows;
-                if (t >= len) break;
+                if (t >= t_end) break;
                 if (good(lookup(blk_of(t)))) nbytes += (uint32_t)box_rows * D * 2;
                 else bad = true;
             }
@@ -225,7 +315,7 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
             mbar_arrive_expect_tx(bar, nbytes);
             for (int sb = 0; sb < subs; ++sb) {
                 const int t = t0 + sb * box_rows;
-                if (t >= len) break;
+                if (t >= t_end) break;
                 const int j = blk_of(t);
                 const int32_t blk = lookup(j);
                 if (!good(blk)) continue;
@@ -238,7 +328,7 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
         }
         const int r = lane & 15, kv = lane >> 4;
         const int t = t0 + r;
-        const bool live = t < len;
+        const bool live = t < t_end;
         const int j = live ? blk_of(t) : 0;
         const int32_t blk = live ? lookup(j) : -1;
         const bool ok = live && good(blk);
@@ -264,14 +354,14 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
     for (int k = 0; k < min(S, my_tiles); ++k) issue(k);
 
     // Q^T as fp16 MMA B fragments in the K-step order above: column gid of
-    // head tile nt is head h0 + nt*8 + gid (zero past nh)
+    // tile nt is query column nt*8 + gid (zero past ncols)
     uint32_t qb[C::KSTEPS][NT][2];
     {
         const T *qp = reinterpret_cast<const T *>(p.q);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const bool live = nt * 8 + gid < nh;
-            const int64_t row = ((int64_t)b * p.H + h0 + (live ? nt * 8 + gid : 0)) * D;
+            const bool live = nt * 8 + gid < ncols;
+            const int64_t row = qrow(live ? nt * 8 + gid : 0) * D;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
                 const int d = 16 * (tig * C::CPT + kk / 4) + 4 * (kk % 4);
@@ -329,8 +419,8 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
         __syncwarp();
         if (k + S < my_tiles) issue(k + S);
 
-        const int t0 = (warp + k * kI8TcWarps) * kTcTile;
-        const int nvalid = min(kTcTile, len - t0);
+        const int t0 = t_begin + (warp + k * kI8TcWarps) * kTcTile;
+        const int nvalid = min(kTcTile, t_end - t0);
         if constexpr (FP8) {
             // rows past the length hold stale or unwritten bytes, which may be
             // NaN codes: clear them so that their zero weights meet zeros
@@ -398,7 +488,7 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
 
     // merge the warps through shared memory (reusing the ring)
     __syncthreads();
-    float *red_o = reinterpret_cast<float *>(smem);   // [W][16 heads][D]
+    float *red_o = reinterpret_cast<float *>(smem);   // [W][16 columns][D]
     float *red_m = red_o + kI8TcWarps * 16 * D;       // [W][16]
     float *red_l = red_m + kI8TcWarps * 16;           // [W][16]
 #pragma unroll
@@ -422,19 +512,28 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
     }
     __syncthreads();
     const bool bad = flags[0] != 0;
-    for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
-        const int row = i / D, d = i % D;
+    for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
+        const int col = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kI8TcWarps; ++w) M = fmaxf(M, red_m[w * 16 + row]);
+        for (int w = 0; w < kI8TcWarps; ++w) M = fmaxf(M, red_m[w * 16 + col]);
         float a = 0.f, lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kI8TcWarps; ++w) {
-            const float sc = merge_weight(red_m[w * 16 + row], M);
-            a = fmaf(red_o[(w * 16 + row) * D + d], sc, a);
-            lsum = fmaf(red_l[w * 16 + row], sc, lsum);
+            const float sc = merge_weight(red_m[w * 16 + col], M);
+            a = fmaf(red_o[(w * 16 + col) * D + d], sc, a);
+            lsum = fmaf(red_l[w * 16 + col], sc, lsum);
         }
-        out[((int64_t)b * p.H + h0 + row) * D + d] = Elem<T>::from_float(bad ? 0.f : a / lsum);
+        if constexpr (PFX) {
+            const int64_t ws = qrow(col) * p.num_partitions + part;
+            p.ws_acc[ws * D + d] = a;
+            if (d == 0) {
+                p.ws_m[ws] = M;
+                p.ws_l[ws] = bad ? -1.f : lsum;
+            }
+        } else {
+            out[qrow(col) * D + d] = Elem<T>::from_float(bad ? 0.f : a / lsum);
+        }
     }
 }
 
@@ -442,53 +541,99 @@ template <typename T, int D, int NT, bool BOXES>
 __global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
     decode_int8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           DecodeParams p, const float *kv_scales, int box_rows) {
-    codes_tc_body<T, D, NT, BOXES, false>(kmap, vmap, p, kv_scales, box_rows);
+    codes_tc_body<T, D, NT, BOXES, false, false>(kmap, vmap, p, kv_scales, box_rows);
 }
 
 template <typename T, int D, int NT, bool BOXES>
 __global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
     decode_fp8_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          DecodeParams p, const float *kv_scales, int box_rows) {
-    codes_tc_body<T, D, NT, BOXES, true>(kmap, vmap, p, kv_scales, box_rows);
+    codes_tc_body<T, D, NT, BOXES, true, false>(kmap, vmap, p, kv_scales, box_rows);
 }
 
-template <typename T, int D, int NT, bool BOXES, bool FP8>
+template <typename T, int D, int NT, bool BOXES>
+__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
+    decode_prefix_int8_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                 const __grid_constant__ CUtensorMap vmap, DecodeParams p,
+                                 const float *kv_scales, int box_rows) {
+    codes_tc_body<T, D, NT, BOXES, false, true>(kmap, vmap, p, kv_scales, box_rows);
+}
+
+template <typename T, int D, int NT, bool BOXES>
+__global__ void __launch_bounds__(kI8TcWarps * 32, (NT == 1 ? 16 : 8) / kI8TcWarps)
+    decode_prefix_fp8_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                const __grid_constant__ CUtensorMap vmap, DecodeParams p,
+                                const float *kv_scales, int box_rows) {
+    codes_tc_body<T, D, NT, BOXES, true, true>(kmap, vmap, p, kv_scales, box_rows);
+}
+
+// CTAs of a launch: one per (sequence, kv head, group of 16 query heads)
+// for the plain decode; for the shared prefix, one per (group, kv head,
+// shared partition) and one per (sequence, kv head, partition after the
+// fewest shared ones).
+static int64_t codes_grid(const DecodeParams &p, bool pfx) {
+    if (!pfx) return (int64_t)p.B * p.Hkv * ((p.H / p.Hkv + 15) / 16);
+    int64_t grid = 0;
+    for (int i = 0; i < p.groups.n; ++i) grid += (int64_t)p.groups.parts[i] * p.Hkv;
+    // a sequence outside every group shares no partition
+    int32_t fewest = p.groups.n > 0 && p.groups.first[0] == 0 && p.groups.first[p.groups.n] == p.B ? INT32_MAX : 0;
+    for (int i = 0; i < p.groups.n; ++i) fewest = min(fewest, p.groups.parts[i]);
+    if (fewest == INT32_MAX) fewest = 0;
+    return grid + (int64_t)(p.num_partitions - fewest) * p.Hkv * p.B;
+}
+
+template <typename T, int D, int NT, bool BOXES, bool FP8, bool PFX>
 static cudaError_t launch_int8_tc_t(const DecodeParams &params, const float *kv_scales, const CUtensorMap &kmap,
                                    const CUtensorMap &vmap, int box_rows, cudaStream_t stream) {
     DecodeParams p = params;
     p.table_cap = min(p.table_cap, kI8TcTableCap);
     const size_t smem = I8TcCfg<D, BOXES>::bytes(p.table_cap);
-    auto kern = FP8 ? decode_fp8_tc_kernel<T, D, NT, BOXES> : decode_int8_tc_kernel<T, D, NT, BOXES>;
+    auto kern = PFX ? (FP8 ? decode_prefix_fp8_tc_kernel<T, D, NT, BOXES> : decode_prefix_int8_tc_kernel<T, D, NT, BOXES>)
+                    : (FP8 ? decode_fp8_tc_kernel<T, D, NT, BOXES> : decode_int8_tc_kernel<T, D, NT, BOXES>);
     static std::atomic<int> configured[64];   // per template instance of this launcher
     cudaError_t e = ensure_smem_limit(kern, smem, configured);
     if (e != cudaSuccess) return e;
-    const int g = p.H / p.Hkv;
-    const int64_t grid = (int64_t)p.B * p.Hkv * ((g + 15) / 16);
+    const int64_t grid = codes_grid(p, PFX);
     if (grid == 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
     return launch_clustered(kern, grid, kI8TcWarps * 32, smem, 1, stream, kmap, vmap, p, kv_scales, box_rows);
 }
 
-template <typename T, int D, int NT, bool FP8>
+template <typename T, int D, int NT, bool FP8, bool PFX>
 static cudaError_t launch_int8_tc_b(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
                                     const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
     if (kmap != nullptr && vmap != nullptr)
-        return launch_int8_tc_t<T, D, NT, true, FP8>(p, kv_scales, *kmap, *vmap, box_rows, stream);
+        return launch_int8_tc_t<T, D, NT, true, FP8, PFX>(p, kv_scales, *kmap, *vmap, box_rows, stream);
     const CUtensorMap none{};
-    return launch_int8_tc_t<T, D, NT, false, FP8>(p, kv_scales, none, none, box_rows, stream);
+    return launch_int8_tc_t<T, D, NT, false, FP8, PFX>(p, kv_scales, none, none, box_rows, stream);
 }
 
-template <typename T, bool FP8>
+// cols: the widest unit's query columns (at most 16)
+template <typename T, bool FP8, bool PFX>
 static cudaError_t launch_int8_tc_d(const DecodeParams &p, const float *kv_scales, const CUtensorMap *kmap,
-                                    const CUtensorMap *vmap, int box_rows, cudaStream_t stream) {
-    const bool one = p.H / p.Hkv <= 8;
+                                    const CUtensorMap *vmap, int box_rows, int cols, cudaStream_t stream) {
+    const bool one = cols <= 8;
     switch (p.D) {
         case 64:
-            return one ? launch_int8_tc_b<T, 64, 1, FP8>(p, kv_scales, kmap, vmap, box_rows, stream)
-                       : launch_int8_tc_b<T, 64, 2, FP8>(p, kv_scales, kmap, vmap, box_rows, stream);
+            return one ? launch_int8_tc_b<T, 64, 1, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 64, 2, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, stream);
         case 128:
-            return one ? launch_int8_tc_b<T, 128, 1, FP8>(p, kv_scales, kmap, vmap, box_rows, stream)
-                       : launch_int8_tc_b<T, 128, 2, FP8>(p, kv_scales, kmap, vmap, box_rows, stream);
+            return one ? launch_int8_tc_b<T, 128, 1, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, stream)
+                       : launch_int8_tc_b<T, 128, 2, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, stream);
     }
+    return cudaErrorInvalidValue;
+}
+
+template <bool FP8, bool PFX>
+static cudaError_t launch_codes_tc(int dtype, const DecodeParams &p, const float *kv_scales,
+                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows, int cols,
+                                   cudaStream_t stream) {
+    if (cols < 1 || cols > 16) return cudaErrorInvalidValue;
+    if (dtype == PA_BF16)
+        return launch_int8_tc_d<__nv_bfloat16, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, cols, stream);
+    if (dtype == PA_F16) return launch_int8_tc_d<__half, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, cols, stream);
+    if (FP8 && dtype == PA_F32)
+        return launch_int8_tc_d<float, FP8, PFX>(p, kv_scales, kmap, vmap, box_rows, cols, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -504,18 +649,23 @@ bool fp8_supported(int dtype, int head_dim) {
 cudaError_t launch_decode_int8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                   cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16, false>(p, kv_scales, kmap, vmap, box_rows, stream);
-    if (dtype == PA_F16) return launch_int8_tc_d<__half, false>(p, kv_scales, kmap, vmap, box_rows, stream);
-    return cudaErrorInvalidValue;
+    const int g = p.H / p.Hkv;
+    return launch_codes_tc<false, false>(dtype, p, kv_scales, kmap, vmap, box_rows, g < 16 ? g : 16, stream);
 }
 
 cudaError_t launch_decode_fp8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                  const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                  cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_int8_tc_d<__nv_bfloat16, true>(p, kv_scales, kmap, vmap, box_rows, stream);
-    if (dtype == PA_F16) return launch_int8_tc_d<__half, true>(p, kv_scales, kmap, vmap, box_rows, stream);
-    if (dtype == PA_F32) return launch_int8_tc_d<float, true>(p, kv_scales, kmap, vmap, box_rows, stream);
-    return cudaErrorInvalidValue;
+    const int g = p.H / p.Hkv;
+    return launch_codes_tc<true, false>(dtype, p, kv_scales, kmap, vmap, box_rows, g < 16 ? g : 16, stream);
+}
+
+cudaError_t launch_prefix_codes_tc(int dtype, bool fp8, const DecodeParams &p, const float *kv_scales,
+                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
+                                   int members_times_group, cudaStream_t stream) {
+    return fp8 ? launch_codes_tc<true, true>(dtype, p, kv_scales, kmap, vmap, box_rows, members_times_group, stream)
+               : launch_codes_tc<false, true>(dtype, p, kv_scales, kmap, vmap, box_rows, members_times_group,
+                                              stream);
 }
 
 }  // namespace pa

@@ -254,6 +254,12 @@ cudaError_t launch_decode_fp8_simt(int dtype, const DecodeParams &p, const float
 cudaError_t launch_decode_fp8_tc(int dtype, const DecodeParams &p, const float *kv_scales,
                                  const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
                                  cudaStream_t stream);
+// Shared-prefix split-KV partials over the int8 (fp8 false) or fp8 cache on
+// the tensor-core code kernel (DecodeParams as for launch_prefix_tc, plus the
+// scales); members_times_group is the widest unit's query columns (<= 16).
+cudaError_t launch_prefix_codes_tc(int dtype, bool fp8, const DecodeParams &p, const float *kv_scales,
+                                   const CUtensorMap *kmap, const CUtensorMap *vmap, int box_rows,
+                                   int members_times_group, cudaStream_t stream);
 
 // Load-balanced persistent decode (final mode; plain, fused append or sliding
 // window as DecodeParams says).  A plan fixes the grid for a shape on the

@@ -257,6 +257,43 @@ def test_shared_prefix_rejects_bad_arguments(lib):
     assert call(shape=base_shape(batch=0)) == pa.PA_OK
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_shared_prefix_codes_reject_bad_arguments(lib, fmt):
+    f = getattr(lib, f"paged_attention_decode_shared_prefix_{fmt}")
+    s = base_shape()   # block_stride counts bytes: one per element
+    need = pa.paged_attention_partial_workspace(s, 32)
+    first = (ctypes.c_int32 * 3)(0, 1, 2)
+    shared = (ctypes.c_int32 * 2)(32, 0)
+
+    def call(shape=s, n=2, fst=first, sh=shared, ptok=32, ws=FAKE, nbytes=need, kp=FAKE, scales=FAKE,
+             scale=0.1):
+        return f(ctypes.byref(shape), FAKE, FAKE, kp, FAKE, scales, FAKE, FAKE, n,
+                 ctypes.cast(fst, ctypes.c_void_p) if fst is not None else None,
+                 ctypes.cast(sh, ctypes.c_void_p) if sh is not None else None, scale, ptok, ws, nbytes,
+                 None, None)
+
+    assert call(ptok=24) == pa.PA_ERR_INVALID_ARG
+    assert call(n=17) == pa.PA_ERR_INVALID_ARG
+    assert call(fst=None) == pa.PA_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == pa.PA_ERR_INVALID_ARG
+    assert call(scales=None) == pa.PA_ERR_INVALID_ARG
+    assert call(scales=FAKE + 2) == pa.PA_ERR_MISALIGNED
+    assert call(kp=FAKE + 8) == pa.PA_ERR_MISALIGNED
+    assert call(shape=base_shape(block_stride=2 * 2 * 16 * 128 + 8)) == pa.PA_ERR_MISALIGNED
+    assert call(shape=base_shape(head_dim=256, block_stride=2 * 2 * 16 * 256)) == pa.PA_ERR_UNSUPPORTED
+    f32 = base_shape(dtype=pa.PA_F32)
+    if fmt == "int8":   # fp32 queries over int8 have no tensor-core kernel
+        assert call(shape=f32) == pa.PA_ERR_UNSUPPORTED
+    else:               # fp8 takes them: the call gets as far as the workspace check
+        assert call(shape=f32, nbytes=need - 1) == pa.PA_ERR_WORKSPACE
+    assert call(nbytes=need - 1) == pa.PA_ERR_WORKSPACE
+    assert call(fst=(ctypes.c_int32 * 3)(0, 2, 1)) == pa.PA_ERR_INVALID_ARG       # not ascending
+    wide = base_shape(batch=3, num_heads=16, num_kv_heads=2)   # 3 members x 8 heads > 16 columns
+    assert call(shape=wide, n=1, fst=(ctypes.c_int32 * 2)(0, 3), sh=(ctypes.c_int32 * 1)(64),
+                nbytes=1 << 30) == pa.PA_ERR_UNSUPPORTED
+    assert call(shape=base_shape(batch=0)) == pa.PA_OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
     monkeypatch.setattr(pa, "_lib", None)
