@@ -55,6 +55,23 @@ def test_quantised_cache_counts_one_byte_per_element_and_the_scales():
         assert bench.append_bytes(w) == 2 * w.B * w.Hkv * w.D * (2 + 1) + 2 * 4 * w.B * w.Hkv + 8 * w.B
 
 
+def test_quantised_cache_reads_shared_blocks_and_their_scales_once():
+    """The shared-beam figures over an int8 or fp8 cache divide by unique
+    bytes: a block named by several rows adds its codes and its K and V
+    scales once."""
+    for conv in (workloads.to_int8, workloads.to_fp8):
+        w16 = _tiny([8, 8, 5])
+        w16.block_table[1, :2] = w16.block_table[0, :2]   # rows 0 and 1 share their two blocks
+        w = conv(w16)
+        unique_rows = 8 + 5
+        unique_blocks = 2 + 2
+        tables = 2 + 2 + 2
+        want = (2 * w.Hkv * w.D * unique_rows + 2 * 4 * w.Hkv * unique_blocks + 4 * tables + 4 * w.B
+                + 2 * w.B * w.H * w.D * 2)
+        assert bench.decode_bytes(w, [8, 8, 5]) == want
+        assert bench.logical_kv_bytes(w, [8, 8, 5]) == 2 * w.Hkv * w.D * (8 + 8 + 5)
+
+
 def test_kernel_traffic_refuses_a_stale_summary(tmp_path, monkeypatch):
     digest = bench.source_digest(bench.KERNEL_SOURCES["decode_simt"])
     good = tmp_path / "decode_simt__tiny_w9_fused.md"
