@@ -1,8 +1,16 @@
-"""The host-side accounting of bench.py, on CPU: the algorithmic byte
-counts that the roofline fraction divides by (valid rows only, shared
-blocks once, the window's rows, the scales of a quantised cache), and the
-lookup of DRAM traffic from the committed ncu summaries, which must refuse a
-summary whose kernel sources have changed."""
+"""The host-side parts of bench.py, on CPU: the algorithmic byte counts
+that the roofline fraction divides by (valid rows only, shared blocks once,
+the window's rows, the scales of a quantised cache), the lookup of DRAM
+traffic from the committed ncu summaries, which must refuse a summary whose
+kernel sources have changed, and the JSON line of the reference arm (the
+oracle on the host cores), which runs without a GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
 import bench
 import workloads
 
@@ -93,3 +101,27 @@ def test_every_profiled_kernel_has_a_source():
     for f in bench.PROFILE_DIR.glob("*.md"):
         kernel = f.name.split("__")[0]
         assert kernel == "launches" or kernel in bench.KERNEL_SOURCES, f.name
+
+
+@pytest.mark.parametrize("extra", [[], ["--int8"], ["--fp8"]])
+def test_reference_arm_prints_the_contract_line(extra):
+    cmd = [sys.executable, str(bench.ROOT / "bench.py"), "--impl", "reference", "--workload", "1",
+           "--steps", "3", "--warmup", "3", *extra]
+    env = dict(os.environ)
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=bench.ROOT)
+    assert res.returncode == 0, res.stderr
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 3, 3)
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
