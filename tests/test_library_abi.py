@@ -294,6 +294,34 @@ def test_shared_prefix_codes_reject_bad_arguments(lib, fmt):
     assert call(shape=base_shape(batch=0)) == pa.PA_OK
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_shared_prefix_codes_wrappers_marshal_their_arguments(lib, fmt):
+    """The Python wrappers pass every argument through ctypes (a mismatch with
+    the declared argument types raises before the call); the library then
+    rejects the partition size on the host, before any CUDA call (the
+    default stream is passed as 0, so torch needs no device either)."""
+    import torch
+    fn = getattr(pa, f"paged_attention_decode_shared_prefix_{fmt}")
+    B, H, Hkv, D, bs, NB, MB = 2, 4, 2, 128, 16, 8, 4
+    q = torch.zeros((B, H, D), dtype=torch.bfloat16)
+    pool = torch.zeros((NB, 2, Hkv, bs, D), dtype=torch.int8 if fmt == "int8" else torch.uint8)
+    flat = pool.view(-1)
+    scales = torch.ones((NB, 2, Hkv), dtype=torch.float32)
+    table = torch.zeros((B, MB), dtype=torch.int32)
+    lens = torch.ones(B, dtype=torch.int32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    with pytest.raises(pa.PagedAttnError) as ei:
+        fn(torch.empty_like(q), q, flat, flat[Hkv * bs * D:], scales, table, lens, 0.1, 24, ws,
+           group_first=[0, 2], shared_tokens=[32], num_kv_heads=Hkv, block_size=bs, num_blocks=NB,
+           block_stride=2 * Hkv * bs * D, stream=0)
+    assert ei.value.status == pa.PA_ERR_INVALID_ARG
+    call = fn(torch.empty_like(q), q, flat, flat[Hkv * bs * D:], scales, table, lens, 0.1, 24, ws,
+              group_first=[0, 2], shared_tokens=[32], num_kv_heads=Hkv, block_size=bs, num_blocks=NB,
+              block_stride=2 * Hkv * bs * D, stream=0, prepare=True)
+    with pytest.raises(pa.PagedAttnError):
+        call()
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "LIB_PATH", tmp_path / "missing.so")
     monkeypatch.setattr(pa, "_lib", None)
