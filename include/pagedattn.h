@@ -59,8 +59,19 @@
  *                     separate K and V pools use block_stride =
  *                     num_kv_heads*block_size*head_dim.  Each (block, kv
  *                     head) K or V chunk is block_size*head_dim contiguous
- *                     elements.  Block starts should be 128-byte aligned
- *                     ([KB] s3.7); 16-byte alignment is required.
+ *                     elements.
+ *   alignment         The pool pointers, q, out, k_new and v_new must be
+ *                     16-byte aligned and block_stride*element_size a multiple
+ *                     of 16 bytes: the kernels move rows with 16-byte vector
+ *                     and bulk (TMA) copies, which fault on anything less, so
+ *                     the host checks reject it with PA_ERR_MISALIGNED.
+ *                     Block starts SHOULD be 128-byte aligned ([KB] s3.7: a
+ *                     block start off the 128-byte boundary costs bandwidth):
+ *                     a pool base on a 128-byte boundary with block_stride and
+ *                     the K-to-V offset multiples of 128 bytes keeps every
+ *                     block and every (block, kv head) chunk on one.  This is
+ *                     a performance expectation, not checked: a pool that is
+ *                     16- but not 128-byte aligned gives the same results.
  *
  * Query head h reads kv head h / (num_heads / num_kv_heads) (grouped-query
  * attention; num_heads must be a multiple of num_kv_heads).
@@ -146,10 +157,12 @@ typedef struct pa_shape {
  * (f16/bf16: D = 32, 64, 128, 256; f32: D = 16, 32, 64, 128) and
  * head_dim*element_size a multiple of 16 for the append. */
 
-/* Human-readable name of a status. Never NULL. */
+/* Human-readable name of a status. Never NULL.  (Library housekeeping: no
+ * counterpart on the pages.) */
 const char *pa_status_string(pa_status status);
 
-/* Library ABI version (major*10000 + minor*100 + patch). */
+/* Library ABI version (major*10000 + minor*100 + patch).  (Library
+ * housekeeping: no counterpart on the pages.) */
 int32_t pa_version(void);
 
 /*
@@ -255,7 +268,9 @@ pa_status paged_attention_decode_window(const pa_shape *shape, void *out, const 
                                         float scale, int32_t window, int32_t *err_word,
                                         pa_stream_t stream);
 
-/* Which kernel family paged_attention_decode and _partial use for `shape`. */
+/* Which kernel family paged_attention_decode and _partial use for `shape`.
+ * (An implementation query: no counterpart on the pages, which leave the
+ * kernel to the implementation; [PG] s2.2 gives only its arithmetic.) */
 typedef enum pa_path {
     PA_PATH_INVALID = 0,     /* shape rejected                                  */
     PA_PATH_SIMT = 1,        /* fp32 CUDA-core path, one (sequence, head) per CTA */
@@ -265,6 +280,16 @@ pa_path paged_attention_decode_path(const pa_shape *shape);
 
 /*
  * Split-KV ("flash decoding") pair for long contexts.
+ *
+ * [PG] s2.2 computes attention block by block -- scores per block, then the
+ * per-block results aggregated before the softmax is normalised and the V
+ * blocks summed with their weights.  This pair makes that aggregation
+ * explicit across thread blocks: each partition of blocks keeps its own
+ * running softmax state, and the reduce combines the states.  The pages do
+ * not spell out how partial states combine; the merge below is the
+ * log-sum-exp identity (rescale each partition's sum and weighted V by
+ * 2^(m_p - M) for the overall maximum M), which makes the result equal to
+ * the single-pass attention.
  *
  * paged_attention_decode_partial splits each sequence's valid tokens into
  * partitions of partition_tokens tokens (a positive multiple of 16) and,
@@ -291,7 +316,8 @@ pa_path paged_attention_decode_path(const pa_shape *shape);
  * reduce then writes zeros for the whole sequence.
  *
  * paged_attention_partial_workspace returns 0 for an invalid shape or
- * partition size.
+ * partition size.  (A size query for the workspace above: [PG] s2.2's
+ * per-block results, one slot per partition.)
  */
 size_t paged_attention_partial_workspace(const pa_shape *shape, int32_t partition_tokens);
 
@@ -380,6 +406,8 @@ pa_status paged_attention_decode_shared_prefix(const pa_shape *shape, void *out,
  * that may overlap on the GPU need separate workspaces.  The size depends on
  * the shape and on the GPU the call runs on (SM count); query it with the
  * target device current.  Returns 0 for a shape this entry point rejects.
+ * (paged_attention_balanced_workspace is a size query with no counterpart
+ * on the pages.)
  *
  * Rejected shapes (PA_ERR_UNSUPPORTED): the schedule keeps two int32 per
  * sequence in shared memory and counts tiles in int32, which bounds batch
@@ -534,8 +562,14 @@ pa_status paged_attention_decode_shared_prefix_fp8(const pa_shape *shape, void *
  * for such shapes.
  *
  * Set-up: the first call on each device looks up the device address of the
- * scratch array (with that device current) and caches it; make that first
- * call before any stream capture.
+ * scratch array (with that device current) and caches it together with the
+ * identity of the CUDA context that was current; make that first call before
+ * any stream capture.  The address belongs to that context: when a later call
+ * finds another context current on the device (after cudaDeviceReset, or a
+ * context the caller created), it looks the address up again in the new
+ * context before launching, so a reset never leaves a stale address behind.
+ * A call that has to look the address up is not capturable, so after a
+ * reset make one call again before capturing.
  *
  * Sharing: all calls on a device use the same scratch array, and it keeps
  * whatever the previous call left in it.  Nothing in it needs to start at

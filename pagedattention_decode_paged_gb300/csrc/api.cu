@@ -964,10 +964,47 @@ static __device__ __align__(256) unsigned char g_split_scratch[PA_STATIC_SCRATCH
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_split_scratch on the current device, looked up once per
-// device and cached.  Returns nullptr (and the error) if the lookup fails.
+// The cached address of g_split_scratch on a device, and the unique id of the
+// CUDA context it was looked up in: a symbol's device address belongs to the
+// context that loaded the module, so a reset device (a new primary context)
+// or a caller-created context needs a fresh lookup.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void *addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique id of the context current on this thread (ids are never reused
+// within a process, unlike context handles); false when no context is
+// current yet or the driver cannot tell.
+bool current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_split_scratch in the context current on this device,
+// looked up once per (device, context) and cached.  Returns nullptr (and the
+// error) if the lookup fails.
 void *split_scratch_for_current_device(cudaError_t *err) {
     int dev = 0;
     *err = cudaGetDevice(&dev);
@@ -976,14 +1013,19 @@ void *split_scratch_for_current_device(cudaError_t *err) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *addr = nullptr;
-        *err = cudaGetSymbolAddress(&addr, g_split_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = addr;
-    }
-    return g_scratch_addr[dev];
+    if (known && g_scratch_addr[dev].addr != nullptr && g_scratch_addr[dev].ctx_id == id)
+        return g_scratch_addr[dev].addr;
+    // first call in this context (the lookup also makes the device's primary
+    // context current when no context is)
+    void *addr = nullptr;
+    *err = cudaGetSymbolAddress(&addr, g_split_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    if (current_context_id(&id)) g_scratch_addr[dev] = ScratchAddr{id, addr};
+    else g_scratch_addr[dev] = ScratchAddr{0, nullptr};   // cannot tell contexts apart: never cache
+    return addr;
 }
 
 }  // namespace

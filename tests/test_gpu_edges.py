@@ -237,3 +237,37 @@ def test_fused_append_decode_errors(H, Hkv):
     ref_pool, _ = hz.oracle_append(w)
     ref, _ = hz.oracle_decode(w, ref_pool, w.lens + 1)
     hz.assert_close(out[0:1], ref[0:1], BF16)
+
+
+@pytest.mark.parametrize("H,Hkv,dtype", [(8, 8, F16), (16, 2, BF16)])
+def test_pool_alignment_128_expected_16_required(H, Hkv, dtype):
+    """Device pools start on a 128-byte boundary ("KV Block design" s3.7);
+    a pool moved to a 16- but not 128-byte aligned address (allowed, slower)
+    gives bit-identical results, and a pool off the 16-byte rule is refused
+    before anything runs."""
+    w = workloads.make_generic(B=3, H=H, Hkv=Hkv, D=128, bs=16, dtype=dtype, lens=[70, 5, 300],
+                               seed=51, poison=True)
+    g = w.to("cuda")
+    assert g.pool.data_ptr() % 128 == 0
+    out = hz.gpu_decode(g, g.lens, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    es = g.pool.element_size()
+    n = g.pool.numel()
+    buf = torch.empty(n + 64 // es, dtype=dtype, device="cuda")
+    off = 16 // es                                      # 16 bytes past a 512-byte boundary
+    shifted = buf[off:off + n]
+    shifted.copy_(g.pool.view(-1))
+    assert shifted.data_ptr() % 128 == 16
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out2 = torch.empty_like(g.q)
+    pa.paged_attention_decode(out2, g.q, shifted, shifted[w.v_offset:], g.block_table, g.lens, g.scale,
+                              num_kv_heads=Hkv, err_word=err, **hz.kw(g))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(hz.int_view(out), hz.int_view(out2))
+    ref, _ = hz.oracle_decode(w, w.pool, w.lens)
+    hz.assert_close(out2, ref, dtype)
+    bad = buf[off + 1:off + 1 + n - 8]                  # 2 bytes off: breaks the 16-byte rule
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.paged_attention_decode(out2, g.q, bad, bad[w.v_offset:], g.block_table, g.lens, g.scale,
+                                  num_kv_heads=Hkv, **hz.kw(g))
+    assert e.value.status == pa.PA_ERR_MISALIGNED

@@ -327,3 +327,68 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         pa.load()
+
+
+PAGE_TAGS = ("[BM]", "[KB]", "[BUG]", "[PG]")
+
+
+def declaration_comments():
+    """For each function the header declares, the comment block nearest above
+    its declaration (declarations that follow one another without a comment
+    of their own share the block above the first; comments that trail a line,
+    such as those of enum members, do not count)."""
+    text = open(HEADER).read()
+    out, last = {}, ""
+    for m in re.finditer(r"^/\*.*?\*/|^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.S | re.M):
+        if m.group(0).startswith("/*"):
+            last = " ".join(re.sub(r"\n\s*\*(?!/)", " ", m.group(0)).split())   # one line of words
+        elif m.group(1) and m.group(1) != "defined":
+            out[m.group(1)] = last
+    return out
+
+
+def test_every_declaration_cites_its_passage_or_says_it_has_none():
+    """Each entry point names the passage of the pages that defines what it
+    computes, or states that the pages have no counterpart for it."""
+    comments = declaration_comments()
+    assert set(comments) == set(declared_functions())
+    for name, comment in comments.items():
+        assert any(t in comment for t in PAGE_TAGS) or "no counterpart" in comment, name
+    # the split-KV pair rests on the per-block aggregation of [PG] s2.2
+    for name in ("paged_attention_partial_workspace", "paged_attention_decode_partial",
+                 "paged_attention_decode_reduce"):
+        assert "[PG] s2.2" in comments[name], name
+
+
+def _layouts():
+    """Every workload layout the tests and the benchmark use, with its int8
+    and fp8 counterparts (the strides do not depend on the lengths, so short
+    sequences keep the pools small)."""
+    import workloads
+    for index, bs in [(1, None), (2, None), (3, 8), (3, 16), (3, 32), (3, 64), (4, 16), (4, 256),
+                      (5, None)]:
+        w = workloads.make_workload(index, block_size=bs, batch=4 if index in (2, 3, 4) else None,
+                                    max_len=64)
+        yield f"workload {index} bs {w.bs}", w
+        if w.D in (64, 128, 256):
+            yield f"workload {index} bs {w.bs} int8", workloads.to_int8(w)
+            yield f"workload {index} bs {w.bs} fp8", workloads.to_fp8(w)
+
+
+def test_workload_blocks_start_on_128_byte_boundaries():
+    """"KV Block design" s3.7 wants every block to start on a 128-byte
+    boundary.  With a pool base on a 128-byte boundary (the caching allocator
+    of the GPU hands out 512-byte aligned blocks; test_gpu_edges checks the
+    device pools), that holds for every block, both halves and every kv head
+    when the block stride, the K-to-V offset and the (block, kv head) chunk
+    are multiples of 128 bytes."""
+    for what, w in _layouts():
+        es = w.pool.element_size()
+        assert w.pool.is_contiguous(), what
+        assert (w.block_stride * es) % 128 == 0, what
+        assert (w.v_offset * es) % 128 == 0, what
+        assert (w.bs * w.D * es) % 128 == 0, what
+        # the chunk start of every (block, K|V, kv head) relative to the base
+        starts = [(blk * w.block_stride + half * w.v_offset + hk * w.bs * w.D) * es
+                  for blk in (0, 1, w.NB - 1) for half in (0, 1) for hk in range(w.Hkv)]
+        assert all(s % 128 == 0 for s in starts), what

@@ -8,11 +8,15 @@ an allocation would break the capture.  For them the library keeps the
 split-KV partial results in a fixed scratch array of its own.  These tests
 call that entry point through the C ABI, twice in a row on different shapes
 (the array keeps whatever the previous call left), and compare each result
-with paged_attention_decode on the same inputs.
+with the CPU oracle and with paged_attention_decode on the same inputs; they
+also probe the size limit at the exact shape where the workspace stops
+fitting.
 
 This file is named so that pytest collects it last.
 """
 import ctypes
+import re
+from pathlib import Path
 
 import pytest
 import torch
@@ -23,7 +27,14 @@ from tests import harness as hz
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 8 << 20      # PA_STATIC_SCRATCH_BYTES in include/pagedattn.h
+HEADER = Path(__file__).resolve().parent.parent / "include" / "pagedattn.h"
+
+
+def scratch_bytes() -> int:
+    """PA_STATIC_SCRATCH_BYTES as include/pagedattn.h defines it."""
+    m = re.search(r"#define\s+PA_STATIC_SCRATCH_BYTES\s+\((\d+)u?\s*<<\s*(\d+)\)", HEADER.read_text())
+    assert m, "PA_STATIC_SCRATCH_BYTES not found in the header"
+    return int(m.group(1)) << int(m.group(2))
 
 
 def _entry():
@@ -43,27 +54,71 @@ def _call(f, g, lens, ptok, out, err):
              err.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-def test_static_scratch_split_matches_decode_twice_in_a_row(cuda_ok):
+def _check_against_both(f, w, ptok):
+    """One static call on w (no append; attention over w.lens) against the
+    oracle and against paged_attention_decode, each with its own err word."""
+    g = w.to("cuda")
+    err_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref_gpu = hz.gpu_decode(g, g.lens, err_ref)
+    torch.cuda.synchronize()
+    assert int(err_ref.item()) == 0, f"paged_attention_decode raised device bits {int(err_ref.item())}"
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(g.q, float("nan"))
+    st = _call(f, g, g.lens, ptok, out, err)
+    assert st == pa.PA_OK, pa.status_string(st)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"split_static raised device bits {int(err.item())}"
+    ref, e = hz.oracle_decode(w, w.pool, w.lens)
+    assert not e.any()
+    hz.assert_close(out, ref, w.dtype, f"{w.name} split_static vs oracle")
+    atol, rtol = hz.TOL[w.dtype]
+    diff = (out.float() - ref_gpu.float()).abs()
+    assert bool((diff <= atol + rtol * ref_gpu.float().abs()).all()), float(diff.max())
+
+
+def test_static_scratch_split_matches_oracle_twice_in_a_row(cuda_ok):
     f = _entry()
+    limit = scratch_bytes()
     cases = [
         (workloads.make_workload(5, max_len=6000, poison=True), 1024),        # MHA, shared prefix
         (workloads.make_workload(4, batch=6, max_len=900, poison=True), 256),  # GQA, tensor cores
     ]
     for w, ptok in cases:
-        g = w.to("cuda")
-        shape = hz.shape_of(g)
-        assert 0 < pa.paged_attention_partial_workspace(shape, ptok) <= SCRATCH_BYTES
-        err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        ref = hz.gpu_decode(g, g.lens, err)
-        out = torch.full_like(g.q, float("nan"))
-        st = _call(f, g, g.lens, ptok, out, err)
-        assert st == pa.PA_OK, pa.status_string(st)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        atol, rtol = hz.TOL[w.dtype]
-        diff = (out.float() - ref.float()).abs()
-        assert torch.isfinite(out.float()).all()
-        assert bool((diff <= atol + rtol * ref.float().abs()).all()), float(diff.max())
+        assert 0 < pa.paged_attention_partial_workspace(hz.shape_of(w), ptok) <= limit
+        _check_against_both(f, w, ptok)
+
+
+def _boundary_workload(mb: int):
+    """One sequence of 40 tokens whose table row holds mb entries (the rest
+    -1), so that the split-KV workspace grows with mb at 16-token partitions."""
+    w = workloads.make_generic(B=1, H=4, Hkv=4, D=128, bs=16, dtype=torch.bfloat16,
+                               lens=[40], seed=5, poison=True)
+    table = torch.full((1, mb), -1, dtype=torch.int32)
+    table[0, :w.MB] = w.block_table[0]
+    w.block_table = table
+    w.MB = mb
+    return w
+
+
+def test_static_scratch_size_limit_is_exact(cuda_ok):
+    f = _entry()
+    limit = scratch_bytes()
+    ptok = 16
+    # largest row length whose workspace still fits (workspace grows with it)
+    ws = lambda mb: pa.paged_attention_partial_workspace(hz.shape_of(_boundary_workload(mb)), ptok)  # noqa: E731
+    lo, hi = 1, 1 << 16
+    assert ws(lo) <= limit < ws(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if ws(mid) <= limit else (lo, mid)
+    assert ws(lo) <= limit < ws(lo + 1)
+    _check_against_both(f, _boundary_workload(lo), ptok)            # at the limit: runs
+    g = _boundary_workload(lo + 1).to("cuda")                       # one partition more: rejected
+    out = torch.empty_like(g.q)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _call(f, g, g.lens, ptok, out, err) == pa.PA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size(cuda_ok):
@@ -73,7 +128,7 @@ def test_static_scratch_rejects_shapes_beyond_its_size(cuda_ok):
     w.MB = 4096                      # room for 65536 tokens per sequence
     w.block_table = torch.full((w.B, w.MB), -1, dtype=torch.int32)
     g = w.to("cuda")
-    assert pa.paged_attention_partial_workspace(hz.shape_of(g), 16) > SCRATCH_BYTES
+    assert pa.paged_attention_partial_workspace(hz.shape_of(g), 16) > scratch_bytes()
     out = torch.empty_like(g.q)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert _call(f, g, g.lens, 16, out, err) == pa.PA_ERR_WORKSPACE
