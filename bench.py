@@ -15,6 +15,14 @@ reported: query tokens/s, microseconds per layer-step, the decode kernel's
 fraction of measured HBM bandwidth, an end-to-end figure with host buffers,
 and the CPU oracle's throughput on the host cores.
 
+The kernel's duration comes from a pass of 64 isolated launches after the
+timed region (each bracketed by its own events, one launch after a
+synchronize discarded), so it does not depend on --steps.  A one-GPU run
+then measures the other configurations of the report the same way (the
+five workloads, the long tail at block sizes 8/16/32/64, the GQA layer at
+16/256, the int8 and fp8 caches, a pool 16 bytes off the 128-byte boundary)
+and adds them to the same JSON line under "per_workload".
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
        [--block-size BS] [--impl reference]
 Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
@@ -33,6 +41,7 @@ import subprocess
 import sys
 import time
 from pathlib import Path
+from types import SimpleNamespace
 
 import torch
 
@@ -277,6 +286,359 @@ def describe(w, index) -> dict:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def step_options(**over) -> SimpleNamespace:
+    """The step-shaping flags of the command line, with their defaults."""
+    o = dict(unfused=False, window=0, balanced=False, prefill=False, split_tokens=None,
+             shared_prefix=None, int8=False, fp8=False, graph=0, long_seq=0, pool_offset=0)
+    o.update(over)
+    return SimpleNamespace(**o)
+
+
+def make_bench_workload(index, o, dev, rank=0, block_size=None, batch=None):
+    """Workload `index` on `dev` as the options shape it: a long request
+    beside the batch, an int8 or fp8 cache (codes drawn on the device), or a
+    pool moved `pool_offset` bytes off its 512-byte aligned allocation."""
+    w = workloads.make_workload(index, block_size=block_size, device=dev,
+                                seed=replica_seed(index, rank), batch=batch)
+    if o.long_seq:
+        w = workloads.with_long_sequence(w, o.long_seq, seed=7 + rank, device=dev)
+    if o.int8 and o.fp8:
+        raise SystemExit("--int8 and --fp8 are two cache formats: pick one")
+    if o.int8 or o.fp8:
+        if o.prefill or o.window or o.balanced or o.graph:
+            raise SystemExit("--int8 / --fp8 time the quantising append + decode pair only")
+        w = (workloads.to_fp8(w, seed=19 + rank, device=dev) if o.fp8
+             else workloads.to_int8(w, seed=17 + rank, device=dev))
+    if o.pool_offset:
+        es = w.pool.element_size()
+        if o.pool_offset % 16 or o.pool_offset % es:
+            raise SystemExit("--pool-offset must keep the 16-byte alignment the library requires")
+        n = w.pool.numel()
+        buf = torch.empty(n + 1024 // es, dtype=w.pool.dtype, device=dev)
+        off = o.pool_offset // es
+        buf[off:off + n].copy_(w.pool.view(-1))
+        w.pool = buf[off:off + n].view(w.pool.shape)
+    return w
+
+
+class StepPlan:
+    """One step of the hot path over workload `w` through the C ABI: the calls,
+    the kernel they centre on and the bytes they move.
+
+    A step is the append of the step's K/V row for every (sequence, kv head)
+    and decode attention over the L + 1 valid tokens: one fused
+    paged_attention_decode_append launch by default; append + decode (or the
+    split-KV pair, or the shared-prefix split) as separate launches otherwise;
+    the prompt write of every sequence for --prefill.
+    """
+
+    def __init__(self, pa, w, index, o, dev, stream):
+        self.pa, self.w, self.index, self.o, self.stream = pa, w, index, o, stream
+        kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
+        self.kw = kw
+        shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
+                              block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
+                              block_stride=w.block_stride, dtype=w.dtype)
+        path = pa.paged_attention_decode_path(shape)
+        kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
+        self.quant = "fp8" if o.fp8 else "int8" if o.int8 else None
+        if o.int8:
+            # grouped-query shapes with 16-bit queries and head_dim 64/128 run on
+            # the tensor cores (the rule of paged_attention_decode_int8)
+            tc8 = w.H // w.Hkv >= 2 and w.D in (64, 128) and w.dtype in (torch.float16, torch.bfloat16)
+            kernel = "decode_int8_tc" if tc8 else "decode_int8"
+        if o.fp8:
+            # grouped-query shapes at head_dim 64/128 on the tensor cores, the
+            # rest on the CUDA cores (the rule of paged_attention_decode_fp8)
+            kernel = "decode_fp8_tc" if w.H // w.Hkv >= 2 and w.D in (64, 128) else "decode_fp8"
+        if o.prefill:
+            kernel = "append_tokens"
+        ptok = SPLIT_PTOK.get(index) if o.split_tokens is None else (o.split_tokens or None)
+        self.positions = w.lens.clone()
+        self.lens_after = (w.lens + 1).clone()
+        self.out = torch.empty_like(w.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw) if ptok else None
+        fused = not ptok and not o.unfused and not self.quant
+        window = o.window or 0
+        if window and not o.balanced:
+            fused = False
+        if self.quant:
+            ptok = None
+        groups = None
+        shared = o.shared_prefix
+        if shared is None:
+            shared = index in SHARED_PREFIX and not o.balanced and not o.long_seq \
+                and not o.prefill and not window
+        if shared:
+            if "shared_blocks" not in w.meta:
+                raise SystemExit("--shared-prefix needs a workload with a shared prefix (workload 5)")
+            groups = {"first": [0, w.B], "shared": [w.meta["shared_blocks"] * w.bs]}
+            ptok = o.split_tokens or (SHARED_PREFIX_CODES if self.quant else SHARED_PREFIX).get(index, 4096)
+            ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
+            fused = False
+            kernel = {"fp8": "decode_prefix_fp8_tc", "int8": "decode_prefix_int8_tc"}.get(
+                self.quant, "decode_prefix_tc")
+        bws = None
+        if o.balanced:
+            ptok = None
+            fused = not o.unfused
+            kernel = kernel.replace("decode_gqa_tc", "decode_tc") + "_balanced"
+            bws = pa.balanced_workspace_for(w.q, w.block_table, num_kv_heads=w.Hkv, **kw)
+        prefill = None
+        if o.prefill:
+            # the padded batch of whole prompts, lengths = the workload's lengths
+            T = int(w.lens.max())
+            gen = torch.Generator(device=dev).manual_seed(99)
+            prefill = {
+                "k": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
+                "v": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
+                "start": torch.zeros(w.B, dtype=torch.int32, device=dev),
+            }
+            fused = False
+        self.kernel, self.fused, self.ptok, self.window = kernel, fused, ptok, window
+        self.shared, self.groups, self.ws, self.bws, self.prefill = shared, groups, ws, bws, prefill
+        self.main_calls, self.app_calls = self.make_calls(prepared=True)
+
+    def make_calls(self, prepared: bool, t=None):
+        """The step's C-ABI calls on the tensors `t` (default: the workload's
+        own q, k_new, v_new, block_table, positions, lens_after and out).
+        Prepared calls marshal their arguments once (a serving loop reuses
+        its buffers every step) and are bound to the bench stream; graph
+        capture needs calls on the capture stream."""
+        pa, w, o, kw = self.pa, self.w, self.o, self.kw
+        t = t or dict(q=w.q, k_new=w.k_new, v_new=w.v_new, block_table=w.block_table,
+                      positions=self.positions, lens_after=self.lens_after, out=self.out)
+        ptok, ws, bws, groups, window = self.ptok, self.ws, self.bws, self.groups, self.window
+        kflat, vflat = w.k_flat(), w.v_flat()
+        opt = dict(err_word=self.err, prepare=prepared,
+                   stream=self.stream.cuda_stream if prepared else None)
+
+        def bind(fn, *a, **k):
+            c = fn(*a, **k, **opt)
+            return c if prepared else (lambda: fn(*a, **k, **dict(opt, prepare=False)))
+
+        if self.prefill is not None:
+            p = self.prefill
+            return [bind(pa.paged_kv_append_tokens, p["k"], p["v"], kflat, vflat, w.block_table, p["start"],
+                         w.lens, **kw)], []
+        if self.shared and self.quant:
+            fn = (pa.paged_attention_decode_shared_prefix_fp8 if o.fp8
+                  else pa.paged_attention_decode_shared_prefix_int8)
+            app_fn = pa.paged_kv_append_fp8 if o.fp8 else pa.paged_kv_append_int8
+            return ([bind(fn, t["out"], t["q"], kflat, vflat, w.scales, t["block_table"], t["lens_after"],
+                          w.scale, ptok, ws, group_first=groups["first"], shared_tokens=groups["shared"],
+                          num_kv_heads=w.Hkv, **kw)],
+                    [bind(app_fn, t["k_new"], t["v_new"], kflat, vflat, w.scales, t["block_table"],
+                          t["positions"], **kw)])
+        if self.shared:
+            return ([bind(pa.paged_attention_decode_shared_prefix, t["out"], t["q"], kflat, vflat,
+                          t["block_table"], t["lens_after"], w.scale, ptok, ws, group_first=groups["first"],
+                          shared_tokens=groups["shared"], num_kv_heads=w.Hkv, **kw)],
+                    [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
+                          t["positions"], **kw)])
+        if self.quant:
+            dec = pa.paged_attention_decode_fp8 if o.fp8 else pa.paged_attention_decode_int8
+            app_fn = pa.paged_kv_append_fp8 if o.fp8 else pa.paged_kv_append_int8
+            return ([bind(dec, t["out"], t["q"], kflat, vflat, w.scales, t["block_table"], t["lens_after"],
+                          w.scale, num_kv_heads=w.Hkv, **kw)],
+                    [bind(app_fn, t["k_new"], t["v_new"], kflat, vflat, w.scales, t["block_table"],
+                          t["positions"], **kw)])
+        app = [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
+                    t["positions"], **kw)]
+        if o.balanced:
+            if self.fused:
+                return [bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
+                             t["block_table"], w.scale, bws, positions=t["positions"], k_new=t["k_new"],
+                             v_new=t["v_new"], window=window, num_kv_heads=w.Hkv, **kw)], []
+            return [bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
+                         t["block_table"], w.scale, bws, seq_lens=t["lens_after"], window=window,
+                         num_kv_heads=w.Hkv, **kw)], app
+        if self.fused:
+            return [bind(pa.paged_attention_decode_append, t["out"], t["q"], t["k_new"], t["v_new"], kflat,
+                         vflat, t["block_table"], t["positions"], w.scale, num_kv_heads=w.Hkv, **kw)], []
+        if window:
+            return [bind(pa.paged_attention_decode_window, t["out"], t["q"], kflat, vflat, t["block_table"],
+                         t["lens_after"], w.scale, window, num_kv_heads=w.Hkv, **kw)], app
+        if ptok:
+            return [bind(pa.paged_attention_decode_partial, t["q"], kflat, vflat, t["block_table"],
+                         t["lens_after"], w.scale, ptok, ws, num_kv_heads=w.Hkv, **kw),
+                    bind(pa.paged_attention_decode_reduce, t["out"], ws, t["lens_after"], ptok,
+                         num_kv_heads=w.Hkv, max_blocks_per_seq=w.MB, **kw)], app
+        return [bind(pa.paged_attention_decode, t["out"], t["q"], kflat, vflat, t["block_table"],
+                     t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw)], app
+
+    def append(self):
+        for c in self.app_calls:
+            c()
+
+    def decode(self):
+        for c in self.main_calls:
+            c()
+
+    def step(self):
+        self.append()
+        self.decode()
+
+    @property
+    def launches_per_step(self) -> int:
+        return len(self.main_calls) + len(self.app_calls)
+
+    def check_err(self, when: str) -> None:
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(self.err.item())} during {when}")
+
+    def byte_counts(self):
+        """(decode bytes, step bytes, bytes of the timed kernel launch(es))."""
+        w = self.w
+        if self.prefill is not None:
+            b = prefill_bytes(w)
+            return b, b, b
+        dbytes = decode_bytes(w, self.lens_after, self.window)
+        # the fused kernel also writes the appended rows into the pool
+        kbytes = dbytes + (2 * w.B * w.Hkv * w.D * w.q.element_size() if self.fused else 0)
+        return dbytes, dbytes + append_bytes(w), kbytes
+
+
+def time_steps(plan: StepPlan, K: int, stream) -> float:
+    """Milliseconds of K back-to-back steps, bracketed by events on `stream`
+    after a synchronize (no events between the steps, so that programmatic
+    dependent launch overlaps one step's tail with the next one's start)."""
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        plan.step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
+KERNEL_PASS = 64
+
+
+def kernel_pass(plan: StepPlan, stream, n: int = KERNEL_PASS) -> list[float]:
+    """Durations (us) of n launches of the step's timed kernel(s), each
+    bracketed by its own pair of events on the launching stream, so that no
+    launch overlaps a neighbour: the whole launch, ramp-up and drain
+    included, as ncu's gpu__time_duration counts it.  One more launch runs
+    first, right after a synchronize, and is discarded; the pass does not
+    depend on the number of timed steps."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        plan.decode()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev[1:]]
+
+
+def spread(samples: list[float]) -> dict:
+    s = sorted(samples)
+    return {"mean": round(statistics.fmean(s), 3), "median": round(statistics.median(s), 3),
+            "p10": round(s[len(s) // 10], 3), "p90": round(s[(9 * len(s)) // 10], 3), "samples": len(s)}
+
+
+DEFAULT_BLOCK_SIZE = {1: 16, 2: 16, 3: 16, 4: 16, 5: 32}
+
+
+def workload_key(index, o, block_size=None) -> str:
+    """The key profile summaries are filed under: workload, block size when
+    it is not the workload's default, cache variant, skew and pool offset."""
+    key = f"w{index}"
+    if block_size and block_size != DEFAULT_BLOCK_SIZE.get(index):
+        key += f"_bs{block_size}"
+    if o.long_seq:
+        key += f"_long{o.long_seq}"
+    key += "_fp8" if o.fp8 else "_int8" if o.int8 else ""
+    return key + (f"_pool_off{o.pool_offset}" if o.pool_offset else "")
+
+
+# Configurations measured beside the headline step in the same run (one
+# entry each): the five workloads of the report, the block-size sweep of the
+# long tail and of the GQA layer, the quantised caches, and a pool that is
+# 16- but not 128-byte aligned.
+PER_WORKLOAD = [
+    ("w1", 1, None, {}),
+    ("w2", 2, None, {}),
+    ("w3_bs8", 3, 8, {}), ("w3_bs16", 3, 16, {}), ("w3_bs32", 3, 32, {}), ("w3_bs64", 3, 64, {}),
+    ("w4_bs16", 4, 16, {}), ("w4_bs256", 4, 256, {}),
+    ("w5", 5, None, {}),
+    ("w2_int8", 2, None, {"int8": True}), ("w4_int8", 4, 16, {"int8": True}),
+    ("w5_int8", 5, None, {"int8": True}),
+    ("w2_fp8", 2, None, {"fp8": True}), ("w4_fp8", 4, 16, {"fp8": True}),
+    ("w5_fp8", 5, None, {"fp8": True}),
+    ("w2_pool_off16", 2, None, {"pool_offset": 16}),
+]
+
+
+def measure_entry(pa, index, block_size, o, dev, stream, seconds: float, peaks: dict) -> dict:
+    """One configuration: a few warm-up steps, about `seconds` of timed
+    steps, then the kernel pass; the same figures as the headline line."""
+    w = make_bench_workload(index, o, dev, block_size=block_size)
+    plan = StepPlan(pa, w, index, o, dev, stream)
+    for _ in range(5):
+        plan.step()
+    torch.cuda.synchronize()
+    plan.check_err("warm-up")
+    probe_ms = time_steps(plan, 10, stream) / 10
+    K = int(min(20000, max(20, seconds * 1e3 / max(probe_ms, 1e-3))))
+    ms_step = time_steps(plan, K, stream) / K
+    samples = kernel_pass(plan, stream)
+    torch.cuda.synchronize()
+    plan.check_err("timing")
+    dbytes, step_bytes, kbytes = plan.byte_counts()
+    kd = spread(samples)
+    achieved = kbytes / (kd["mean"] * 1e-6) / 1e9
+    lens = [int(x) for x in w.lens]
+    entry = {
+        "workload": f"{w.name} (workload {index})", "batch": w.B, "num_heads": w.H,
+        "num_kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs, "cache": plan.quant or DTYPE_NAME[w.dtype],
+        "seq_len_mean": round(sum(lens) / len(lens) + 1, 1), "steps": K,
+        "us_per_layer_step": round(ms_step * 1e3, 3),
+        "gbs": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "tokens_per_s": round(w.B / (ms_step * 1e-3), 1),
+        "kernel": plan.kernel, "launches_per_step": plan.launches_per_step,
+        "kernel_us": kd, "kernel_bytes": kbytes,
+        "kernel_gbs": round(achieved, 1), "frac": round(achieved / peaks["hbm_gbs"], 4),
+        "traffic": kernel_traffic(plan.kernel, workload_key(index, o, block_size), plan.fused),
+        "step": ("fused append + decode" if plan.fused else
+                 "append + shared-prefix split" if plan.shared else
+                 "append + decode" if not plan.ptok else "append + split-KV pair"),
+    }
+    if plan.ptok:
+        entry["split_kv_partition"] = plan.ptok
+    if o.pool_offset:
+        entry["pool_base_mod_128"] = w.pool.data_ptr() % 128
+    if index == 5:
+        lb = logical_kv_bytes(w, plan.lens_after)
+        entry["logical_kv_gbs"] = round(lb / (ms_step * 1e-3) / 1e9, 1)
+        entry["bytes_note"] = "unique bytes: shared blocks counted once"
+    del plan, w
+    torch.cuda.empty_cache()
+    return entry
+
+
+def per_workload_summary(entries: dict) -> dict:
+    """Derived comparisons that the pages quote figures for (on their own
+    hardware, as context): the cost of address translation at small blocks
+    ("KV Cache and BlockManager" s2: 12% at block_size 8, 3.7% at 32 on an
+    A100) and of a block start off the 128-byte boundary ("KV Block design"
+    s3.7: about 15%)."""
+    notes = {}
+    t = {k: e["us_per_layer_step"] for k, e in entries.items() if "us_per_layer_step" in e}
+    if "w3_bs8" in t and "w3_bs32" in t:
+        notes["long_tail_bs8_over_bs32"] = round(t["w3_bs8"] / t["w3_bs32"] - 1, 4)
+    if "w3_bs16" in t and "w3_bs64" in t:
+        notes["long_tail_bs64_over_bs16"] = round(t["w3_bs64"] / t["w3_bs16"] - 1, 4)
+    if "w2" in t and "w2_pool_off16" in t:
+        notes["pool_16_not_128_aligned_over_aligned"] = round(t["w2_pool_off16"] / t["w2"] - 1, 4)
+    return notes
+
+
 def run_gpu(args) -> None:
     import pagedattention_decode_paged_gb300 as pa
 
@@ -290,183 +652,21 @@ def run_gpu(args) -> None:
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     pa.load()
+    stream = torch.cuda.current_stream()
+    o = step_options(unfused=args.unfused, window=args.window, balanced=args.balanced,
+                     prefill=args.prefill, split_tokens=args.split_tokens,
+                     shared_prefix=args.shared_prefix, int8=args.int8, fp8=args.fp8,
+                     graph=args.graph, long_seq=args.long_seq, pool_offset=args.pool_offset)
 
     # each rank holds its own replica of the workload (weak scaling)
-    w = workloads.make_workload(args.workload, block_size=args.block_size, device=dev,
-                                seed=replica_seed(args.workload, rank), batch=args.batch)
-    workload_key = f"w{args.workload}" + (f"_bs{args.block_size}" if args.block_size else "")
-    if args.long_seq:
-        w = workloads.with_long_sequence(w, args.long_seq, seed=7 + rank, device=dev)
-        workload_key += f"_long{args.long_seq}"
-    if args.int8 and args.fp8:
-        raise SystemExit("--int8 and --fp8 are two cache formats: pick one")
-    if args.int8 or args.fp8:
-        if args.prefill or args.window or args.balanced or args.graph:
-            raise SystemExit("--int8 / --fp8 time the quantising append + decode pair only")
-        w = (workloads.to_fp8(w, seed=19 + rank) if args.fp8 else workloads.to_int8(w, seed=17 + rank)).to(dev)
-        workload_key += "_fp8" if args.fp8 else "_int8"
-    kw = dict(block_size=w.bs, num_blocks=w.NB, block_stride=w.block_stride)
-    shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
-                          block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
-                          block_stride=w.block_stride, dtype=w.dtype)
-    path = pa.paged_attention_decode_path(shape)
-    kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
-    if args.int8:
-        # grouped-query shapes with 16-bit queries and head_dim 64/128 run on
-        # the tensor cores (the rule of paged_attention_decode_int8)
-        tc8 = w.H // w.Hkv >= 2 and w.D in (64, 128) and w.dtype in (torch.float16, torch.bfloat16)
-        kernel = "decode_int8_tc" if tc8 else "decode_int8"
-    if args.fp8:
-        # grouped-query shapes at head_dim 64/128 on the tensor cores, the
-        # rest on the CUDA cores (the rule of paged_attention_decode_fp8)
-        kernel = "decode_fp8_tc" if w.H // w.Hkv >= 2 and w.D in (64, 128) else "decode_fp8"
-    if args.prefill:
-        kernel = "append_tokens"
-    ptok = SPLIT_PTOK.get(args.workload) if args.split_tokens is None else (args.split_tokens or None)
-    positions = w.lens.clone()
-    lens_after = (w.lens + 1).clone()
-    out = torch.empty_like(w.q)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = (pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
-          if ptok else None)
-    stream = torch.cuda.current_stream()
-
-    quant = args.int8 or args.fp8
-    fused = not ptok and not args.unfused and not quant
-
-    window = args.window or 0
-    balanced = args.balanced
-    if window and not balanced:
-        fused = False
-    bws = None
-    if quant:
-        ptok = None
-    groups = None
-    if args.shared_prefix is None:
-        args.shared_prefix = args.workload in SHARED_PREFIX and not args.balanced \
-            and not args.long_seq and not args.prefill and not window
-    if args.shared_prefix:
-        if "shared_blocks" not in w.meta:
-            raise SystemExit("--shared-prefix needs a workload with a shared prefix (workload 5)")
-        groups = {"first": [0, w.B], "shared": [w.meta["shared_blocks"] * w.bs]}
-        ptok = args.split_tokens or (SHARED_PREFIX_CODES if quant else SHARED_PREFIX).get(args.workload, 4096)
-        ws = pa.workspace_for(w.q, w.block_table, ptok, num_kv_heads=w.Hkv, **kw)
-        fused = False
-        kernel = "decode_prefix_fp8_tc" if args.fp8 else "decode_prefix_int8_tc" if args.int8 else "decode_prefix_tc"
-    if balanced:
-        ptok = None
-        fused = not args.unfused
-        kernel = kernel.replace("decode_gqa_tc", "decode_tc") + "_balanced"
-        bws = pa.balanced_workspace_for(w.q, w.block_table, num_kv_heads=w.Hkv, **kw)
-    prefill = None
-    if args.prefill:
-        # the padded batch of whole prompts, lengths = the workload's lengths
-        T = int(w.lens.max())
-        gen = torch.Generator(device=dev).manual_seed(99)
-        prefill = {
-            "k": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
-            "v": torch.randn((w.B, T, w.Hkv, w.D), generator=gen, device=dev).to(w.dtype),
-            "start": torch.zeros(w.B, dtype=torch.int32, device=dev),
-        }
-        fused = False
-    kflat, vflat = w.k_flat(), w.v_flat()
-
-    def make_calls(prepared: bool, t=None):
-        """The step's C-ABI calls on the tensors `t` (default: the workload's
-        own q, k_new, v_new, block_table, positions, lens_after and out).
-        Prepared calls marshal their arguments once (a serving loop reuses
-        its buffers every step) and are bound to the bench stream; graph
-        capture needs calls on the capture stream."""
-        t = t or dict(q=w.q, k_new=w.k_new, v_new=w.v_new, block_table=w.block_table,
-                      positions=positions, lens_after=lens_after, out=out)
-        o = dict(err_word=err, prepare=prepared,
-                 stream=stream.cuda_stream if prepared else None)
-
-        def bind(fn, *a, **k):
-            c = fn(*a, **k, **o)
-            return c if prepared else (lambda: fn(*a, **k, **dict(o, prepare=False)))
-
-        calls = []
-        if prefill is not None:
-            calls.append(bind(pa.paged_kv_append_tokens, prefill["k"], prefill["v"], kflat, vflat,
-                              w.block_table, prefill["start"], w.lens, **kw))
-            return calls, []
-        if args.shared_prefix and quant:
-            fn = (pa.paged_attention_decode_shared_prefix_fp8 if args.fp8
-                  else pa.paged_attention_decode_shared_prefix_int8)
-            calls.append(bind(fn, t["out"], t["q"], kflat, vflat, w.scales, t["block_table"], t["lens_after"],
-                              w.scale, ptok, ws, group_first=groups["first"], shared_tokens=groups["shared"],
-                              num_kv_heads=w.Hkv, **kw))
-            app_fn = pa.paged_kv_append_fp8 if args.fp8 else pa.paged_kv_append_int8
-            return calls, [bind(app_fn, t["k_new"], t["v_new"], kflat, vflat, w.scales, t["block_table"],
-                                t["positions"], **kw)]
-        if args.shared_prefix:
-            calls.append(bind(pa.paged_attention_decode_shared_prefix, t["out"], t["q"], kflat, vflat,
-                              t["block_table"], t["lens_after"], w.scale, ptok, ws,
-                              group_first=groups["first"], shared_tokens=groups["shared"],
-                              num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
-                                t["positions"], **kw)]
-        if args.fp8:
-            calls.append(bind(pa.paged_attention_decode_fp8, t["out"], t["q"], kflat, vflat, w.scales,
-                              t["block_table"], t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append_fp8, t["k_new"], t["v_new"], kflat, vflat, w.scales,
-                                t["block_table"], t["positions"], **kw)]
-        if args.int8:
-            calls.append(bind(pa.paged_attention_decode_int8, t["out"], t["q"], kflat, vflat, w.scales,
-                              t["block_table"], t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append_int8, t["k_new"], t["v_new"], kflat, vflat, w.scales,
-                                t["block_table"], t["positions"], **kw)]
-        if balanced:
-            if fused:
-                calls.append(bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
-                                  t["block_table"], w.scale, bws, positions=t["positions"], k_new=t["k_new"],
-                                  v_new=t["v_new"], window=window, num_kv_heads=w.Hkv, **kw))
-                return calls, []
-            calls.append(bind(pa.paged_attention_decode_balanced, t["out"], t["q"], kflat, vflat,
-                              t["block_table"], w.scale, bws, seq_lens=t["lens_after"], window=window,
-                              num_kv_heads=w.Hkv, **kw))
-            return calls, [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"],
-                                t["positions"], **kw)]
-        if fused:
-            calls.append(bind(pa.paged_attention_decode_append, t["out"], t["q"], t["k_new"], t["v_new"], kflat,
-                              vflat, t["block_table"], t["positions"], w.scale, num_kv_heads=w.Hkv, **kw))
-            return calls, []
-        app = [bind(pa.paged_kv_append, t["k_new"], t["v_new"], kflat, vflat, t["block_table"], t["positions"],
-                    **kw)]
-        if window:
-            calls.append(bind(pa.paged_attention_decode_window, t["out"], t["q"], kflat, vflat,
-                              t["block_table"], t["lens_after"], w.scale, window, num_kv_heads=w.Hkv, **kw))
-        elif ptok:
-            calls.append(bind(pa.paged_attention_decode_partial, t["q"], kflat, vflat, t["block_table"],
-                              t["lens_after"], w.scale, ptok, ws, num_kv_heads=w.Hkv, **kw))
-            calls.append(bind(pa.paged_attention_decode_reduce, t["out"], ws, t["lens_after"], ptok,
-                              num_kv_heads=w.Hkv, max_blocks_per_seq=w.MB, **kw))
-        else:
-            calls.append(bind(pa.paged_attention_decode, t["out"], t["q"], kflat, vflat, t["block_table"],
-                              t["lens_after"], w.scale, num_kv_heads=w.Hkv, **kw))
-        return calls, app
-
-    main_calls, app_calls = make_calls(prepared=True)
-
-    def append():
-        for c in app_calls:
-            c()
-
-    def decode():
-        for c in main_calls:
-            c()
-
-    def step():
-        append()
-        decode()
-
-    launches_per_step = len(main_calls) + len(app_calls)
+    w = make_bench_workload(args.workload, o, dev, rank=rank, block_size=args.block_size,
+                            batch=args.batch)
+    plan = StepPlan(pa, w, args.workload, o, dev, stream)
+    main_key = workload_key(args.workload, o, args.block_size)
     for _ in range(args.warmup):
-        step()
+        plan.step()
     torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+    plan.check_err("warm-up")
 
     K = args.steps
     graph = None
@@ -477,10 +677,10 @@ def run_gpu(args) -> None:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step()
+            plan.step()
         stream.wait_stream(side)
         torch.cuda.synchronize()
-        g_main, g_app = make_calls(prepared=False)
+        g_main, g_app = plan.make_calls(prepared=False)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for _ in range(args.graph):
@@ -488,12 +688,6 @@ def run_gpu(args) -> None:
                     c()
         graph.replay()
         torch.cuda.synchronize()
-    # kernel durations are sampled live on every EVERY-th step of the timed
-    # region (events bracket those launches on the launching stream); the
-    # other steps run back to back, so that events do not sit between kernels
-    EVERY = 16
-    sampled = [] if graph is not None else list(range(0, K, EVERY))
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if dist:
@@ -501,35 +695,20 @@ def run_gpu(args) -> None:
     torch.cuda.synchronize()
     with ClockSampler(local_gpu_index(local_rank)) as clk:
         t0.record(stream)
-        for i in range(K // args.graph if graph is not None else 0):
+        for _ in range(K // args.graph if graph is not None else 0):
             graph.replay()
-        for i in range(0 if graph is not None else K):
-            e = ev.get(i)
-            if e is None:
-                step()
-                continue
-            e[0].record(stream)
-            append()
-            e[1].record(stream)
-            decode()
-            e[2].record(stream)
+        for _ in range(0 if graph is not None else K):
+            plan.step()
         t1.record(stream)
         torch.cuda.synchronize()
+        # the kernel's launch duration, outside the timed region: isolated
+        # launches, each bracketed by its own events
+        samples = kernel_pass(plan, stream)
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    if graph is not None:
-        # no events inside the graph: the step time bounds the kernel time
-        decode_ms = append_ms = total_ms / K
-    else:
-        decode_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev.values())
-        append_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev.values())
-    # spread of the bracketed decode launches: p10 / median / p90 (us)
-    dsamples = sorted(e[1].elapsed_time(e[2]) * 1e3 for e in ev.values()) if graph is None else []
-    dspread = ({"p10": round(dsamples[len(dsamples) // 10], 3),
-                "median": round(statistics.median(dsamples), 3),
-                "p90": round(dsamples[(9 * len(dsamples)) // 10], 3), "samples": len(dsamples)}
-               if dsamples else None)
+    kd = spread(samples)
+    decode_ms = kd["mean"] * 1e-3
     total_ms = max_over_ranks(total_ms, dist, dev)
 
     # end to end through the C ABI with host buffers: every step copies its
@@ -541,7 +720,8 @@ def run_gpu(args) -> None:
     # serving loop would use.  Graph and prefill runs copy in line.
     names = ("q", "k_new", "v_new", "block_table", "positions", "lens_after")
     src = dict(q=w.q, k_new=w.k_new, v_new=w.v_new, block_table=w.block_table,
-               positions=positions, lens_after=lens_after)
+               positions=plan.positions, lens_after=plan.lens_after)
+    out = plan.out
     offs, total = {}, 0
     for n in names:
         offs[n] = total
@@ -554,7 +734,7 @@ def run_gpu(args) -> None:
         host_in[offs[n]:offs[n] + nb].copy_(src[n].contiguous().view(-1).view(torch.uint8).cpu())
     host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     Ke = max(3, min(K, 2000))
-    pipelined = graph is None and prefill is None
+    pipelined = graph is None and plan.prefill is None
     if pipelined:
         dev_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
         slots = []
@@ -562,7 +742,7 @@ def run_gpu(args) -> None:
             t = {n: buf[offs[n]:offs[n] + src[n].numel() * src[n].element_size()]
                  .view(src[n].dtype).view(src[n].shape) for n in names}
             t["out"] = torch.empty_like(out)
-            slots.append((buf, t, make_calls(prepared=True, t=t)))
+            slots.append((buf, t, plan.make_calls(prepared=True, t=t)))
         h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
         done = [torch.cuda.Event() for _ in range(2)]      # step in slot b finished
         loaded = [torch.cuda.Event() for _ in range(2)]    # inputs of slot b copied
@@ -598,7 +778,7 @@ def run_gpu(args) -> None:
             for _ in range(n):
                 for name in names:
                     src[name].copy_(host_views[name], non_blocking=True)
-                step()
+                plan.step()
                 host_out[0].copy_(out, non_blocking=True)
 
     e2e_run(3)
@@ -617,18 +797,11 @@ def run_gpu(args) -> None:
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     # the copies really landed: the last output read back equals the step's
     # (a prefill run writes no output)
-    out_checked = (None if prefill is not None else
+    out_checked = (None if plan.prefill is not None else
                    bool(torch.equal(host_out[(Ke - 1) % 2 if pipelined else 0].to(dev), out)))
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(err.item())} during timing")
+    plan.check_err("timing")
 
-    if prefill is not None:
-        dbytes = step_bytes = kbytes = prefill_bytes(w)
-    else:
-        dbytes = decode_bytes(w, lens_after, window)
-        step_bytes = dbytes + append_bytes(w)
-        # the fused kernel also writes the appended rows into the pool
-        kbytes = dbytes + (2 * w.B * w.Hkv * w.D * w.q.element_size() if fused else 0)
+    dbytes, step_bytes, kbytes = plan.byte_counts()
     peaks = measured_peaks()
     achieved = kbytes / (decode_ms * 1e-3) / 1e9
     ms_step = total_ms / K
@@ -637,14 +810,17 @@ def run_gpu(args) -> None:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w.to("cpu"), lens_after.cpu(), budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(w.to("cpu"), plan.lens_after.cpu(), budget_s=args.cpu_seconds)
 
+    line = None
     if rank == 0:
         cfg = describe(w, args.workload)
-        cfg["split_kv_partition"] = ptok
+        cfg["split_kv_partition"] = plan.ptok
         cfg["l2"] = ("inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2; no flush"
                      % (dbytes / 1e6)) if dbytes > 2 * 129e6 else "L2 flushed: no (small workload)"
         cfg["parallelism"] = f"replicas x{world}"
+        if o.pool_offset:
+            cfg["pool_offset_bytes"] = o.pool_offset
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
@@ -653,29 +829,67 @@ def run_gpu(args) -> None:
             "config": cfg,
             "tokens_per_s": round(world * w.B / (ms_step * 1e-3), 1),
             "us_per_layer_step": round(ms_step * 1e3, 3),
-            "decode_us": round(decode_ms * 1e3, 3), "append_us": round(append_ms * 1e3, 3),
-            "decode_us_spread": dspread,
+            "decode_us": kd["mean"], "decode_us_median": kd["median"],
+            "decode_us_spread": kd,
             "decode_bytes": dbytes, "kernel_bytes": kbytes,
-            "logical_kv_bytes": logical_kv_bytes(w, lens_after),
-            "decode_path": kernel, "fused_append": fused, "cuda_graph_steps": args.graph or None,
-            "window": window or None, "schedule": "balanced" if balanced else "one CTA per unit",
-            "op": "prefill write" if prefill is not None else "decode step",
+            "logical_kv_bytes": logical_kv_bytes(w, plan.lens_after),
+            "decode_path": plan.kernel, "fused_append": plan.fused, "cuda_graph_steps": args.graph or None,
+            "window": plan.window or None, "schedule": "balanced" if o.balanced else "one CTA per unit",
+            "op": "prefill write" if plan.prefill is not None else "decode step",
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": kernel_traffic(kernel, workload_key, fused),
-                         "kernel": kernel, "timed_launches": len(sampled),
-                         "kernel_timing": "graph step" if graph is not None else "events"},
+                         "traffic": kernel_traffic(plan.kernel, main_key, plan.fused),
+                         "kernel": plan.kernel, "timed_launches": len(samples),
+                         "kernel_timing": f"{len(samples)} isolated launches after the timed region, "
+                                          "each bracketed by its own events on the launching "
+                                          "stream; one launch after a synchronize discarded"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": Ke,
                     "ms_per_step": round(e2e_ms / Ke, 6),
                     "copies": ("one H2D and one D2H per step, double-buffered on two copy streams"
                                if pipelined else "in line with the step"),
                     "output_read_back_matches": out_checked},
-            "gpu_launches": K * launches_per_step,
+            "gpu_launches": K * plan.launches_per_step,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
+    del plan, w, src, out
+    if pipelined:
+        del slots, dev_in
+    torch.cuda.empty_cache()
+
+    # the other configurations, one after another on the same GPU (rank 0 of
+    # a one-GPU run only: every entry is a single-GPU measurement)
+    if line is not None and world == 1 and not args.no_per_workload:
+        peaks = measured_peaks()
+        entries = {}
+        # a plain run (no flag that reshapes the step) already measured its own entry
+        plain = not (o.unfused or o.window or o.balanced or o.prefill or o.graph or o.long_seq or
+                     o.split_tokens is not None or o.shared_prefix is not None or args.batch)
+        with ClockSampler(local_gpu_index(local_rank)) as pclk:
+            for key, index, bs, over in PER_WORKLOAD:
+                ovr = step_options(**over)
+                if plain and workload_key(index, ovr, bs) == main_key:
+                    # the headline line itself: its figures, not a second run
+                    entries[key] = {"headline": True, "us_per_layer_step": line["us_per_layer_step"],
+                                    "gbs": line["value"], "kernel": line["decode_path"],
+                                    "kernel_us": line["decode_us_spread"],
+                                    "frac": line["roofline"]["frac"], "traffic": line["roofline"]["traffic"]}
+                    continue
+                try:
+                    entries[key] = measure_entry(pa, index, bs, ovr, dev, stream,
+                                                 args.per_workload_seconds, peaks)
+                except (RuntimeError, torch.cuda.OutOfMemoryError) as exc:   # report, keep going
+                    entries[key] = {"error": str(exc).splitlines()[0][:200]}
+        line["per_workload"] = {
+            "entries": entries,
+            "notes": per_workload_summary(entries),
+            "clocks": pclk.summary(),
+            "timing": f"each entry: 5 warm-up steps, about {args.per_workload_seconds} s of back-to-back "
+                      f"steps, then {KERNEL_PASS} isolated launches of its kernel(s); not part of the "
+                      "headline's timed region"}
+    if line is not None:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -811,6 +1025,13 @@ def main() -> None:
                     help="time paged_kv_append and paged_attention_decode as two launches")
     ap.add_argument("--split-tokens", type=int, default=None,
                     help="split-KV partition size (0: single-pass decode); default per workload")
+    ap.add_argument("--pool-offset", type=int, default=0,
+                    help="move the pool this many bytes (a multiple of 16) off its 512-byte aligned "
+                         "allocation: the cost of block starts off the 128-byte boundary")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the other configurations measured after the headline")
+    ap.add_argument("--per-workload-seconds", type=float, default=0.3,
+                    help="timed seconds per configuration of the per_workload object")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

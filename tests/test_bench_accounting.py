@@ -125,3 +125,39 @@ def test_reference_arm_prints_the_contract_line(extra):
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("tiny")
+
+
+def test_workload_keys_and_per_workload_table():
+    """Profile keys drop the default block size and name the cache variant;
+    the per_workload table has unique labels, covers workloads 1-5, the
+    long tail at block sizes 8/16/32/64 and the GQA layer at 16/256, and each
+    label's key is distinct (no configuration measured twice)."""
+    o = bench.step_options()
+    assert bench.workload_key(4, o, 16) == bench.workload_key(4, o) == "w4"
+    assert bench.workload_key(4, o, 256) == "w4_bs256"
+    assert bench.workload_key(3, bench.step_options(int8=True), 8) == "w3_bs8_int8"
+    assert bench.workload_key(2, bench.step_options(pool_offset=16)) == "w2_pool_off16"
+    labels = [e[0] for e in bench.PER_WORKLOAD]
+    assert len(labels) == len(set(labels))
+    keys = [bench.workload_key(i, bench.step_options(**over), bs) for _, i, bs, over in bench.PER_WORKLOAD]
+    assert len(keys) == len(set(keys))
+    assert {i for _, i, _, _ in bench.PER_WORKLOAD} == {1, 2, 3, 4, 5}
+    assert {bs for _, i, bs, _ in bench.PER_WORKLOAD if i == 3} == {8, 16, 32, 64}
+    assert {bs for _, i, bs, over in bench.PER_WORKLOAD if i == 4 and not over} == {16, 256}
+
+
+def test_per_workload_notes():
+    e = {"w3_bs8": {"us_per_layer_step": 112.0}, "w3_bs32": {"us_per_layer_step": 100.0},
+         "w3_bs16": {"us_per_layer_step": 105.0}, "w3_bs64": {"us_per_layer_step": 110.25},
+         "w2": {"us_per_layer_step": 80.0}, "w2_pool_off16": {"us_per_layer_step": 84.0},
+         "w4_bs16": {"error": "x"}}
+    n = bench.per_workload_summary(e)
+    assert n == {"long_tail_bs8_over_bs32": 0.12, "long_tail_bs64_over_bs16": 0.05,
+                 "pool_16_not_128_aligned_over_aligned": 0.05}
+    assert bench.per_workload_summary({}) == {}
+
+
+def test_spread_of_kernel_samples():
+    s = bench.spread([float(x) for x in range(1, 65)])
+    assert s["samples"] == 64 and s["mean"] == 32.5 and s["median"] == 32.5
+    assert s["p10"] == 7.0 and s["p90"] == 58.0

@@ -384,37 +384,43 @@ class Int8Workload:
         return Int8Workload(**moved)
 
 
-def to_int8(w: Workload, *, seed: int = 17, scale_range=(0.004, 0.012)) -> Int8Workload:
+def to_int8(w: Workload, *, seed: int = 17, scale_range=(0.004, 0.012), device="cpu") -> Int8Workload:
     """The int8 counterpart of workload `w` (same shape, table, lengths, q
     and new rows): seeded uniform codes in [-127, 127] and per-(block, K|V,
     kv head) scales drawn uniformly from scale_range, so the values the
-    codes stand for have a spread comparable to N(0, 1) data."""
-    gen = torch.Generator().manual_seed(seed)
-    pool = torch.randint(-127, 128, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.int8)
+    codes stand for have a spread comparable to N(0, 1) data.  The codes and
+    scales are drawn on `device` (a CUDA generator gives other numbers than
+    the CPU one for the same seed) and every tensor lands there."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    pool = torch.randint(-127, 128, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.int8,
+                         device=device)
     lo, hi = scale_range
-    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32) * (hi - lo) + lo)
-    cpu = lambda t: t.cpu() if isinstance(t, torch.Tensor) else t
+    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32, device=device)
+              * (hi - lo) + lo)
+    mv = lambda t: t.to(device) if isinstance(t, torch.Tensor) else t
     return Int8Workload(w.name + "-int8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
-                        cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
-                        cpu(w.v_new), w.scale, dict(w.meta, int8_seed=seed))
+                        mv(w.lens), mv(w.block_table), pool, scales, mv(w.q), mv(w.k_new),
+                        mv(w.v_new), w.scale, dict(w.meta, int8_seed=seed))
 
 
-def to_fp8(w: Workload, *, seed: int = 19, scale_range=(0.002, 0.006)) -> Int8Workload:
+def to_fp8(w: Workload, *, seed: int = 19, scale_range=(0.002, 0.006), device="cpu") -> Int8Workload:
     """The fp8 (E4M3) counterpart of workload `w` (same shape, table,
     lengths, q and new rows): seeded uniform bytes over the finite E4M3 codes
     (the two NaN codes are redrawn as zero) and per-(block, K|V, kv head)
     scales drawn uniformly from scale_range, so that the values the codes
-    stand for stay within a few units.  The pool is uint8."""
-    gen = torch.Generator().manual_seed(seed)
-    pool = torch.randint(0, 256, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.int32)
+    stand for stay within a few units.  The pool is uint8.  Drawn on
+    `device`, as to_int8."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    pool = torch.randint(0, 256, (w.NB, 2, w.Hkv, w.bs, w.D), generator=gen, dtype=torch.uint8,
+                         device=device)
     pool[(pool & 0x7F) == 0x7F] = 0
-    pool = pool.to(torch.uint8)
     lo, hi = scale_range
-    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32) * (hi - lo) + lo)
-    cpu = lambda t: t.cpu() if isinstance(t, torch.Tensor) else t
+    scales = (torch.rand((w.NB, 2, w.Hkv), generator=gen, dtype=torch.float32, device=device)
+              * (hi - lo) + lo)
+    mv = lambda t: t.to(device) if isinstance(t, torch.Tensor) else t
     return Int8Workload(w.name + "-fp8", w.B, w.H, w.Hkv, w.D, w.bs, w.NB, w.MB, w.dtype,
-                        cpu(w.lens), cpu(w.block_table), pool, scales, cpu(w.q), cpu(w.k_new),
-                        cpu(w.v_new), w.scale, dict(w.meta, fp8_seed=seed))
+                        mv(w.lens), mv(w.block_table), pool, scales, mv(w.q), mv(w.k_new),
+                        mv(w.v_new), w.scale, dict(w.meta, fp8_seed=seed))
 
 
 def make_prefix_groups(*, group_sizes, shared_blocks, tails, H, Hkv, D, bs, dtype, seed=0,
