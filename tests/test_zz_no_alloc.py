@@ -93,6 +93,7 @@ def _boundary_workload(mb: int):
     -1), so that the split-KV workspace grows with mb at 16-token partitions."""
     w = workloads.make_generic(B=1, H=4, Hkv=4, D=128, bs=16, dtype=torch.bfloat16,
                                lens=[40], seed=5, poison=True)
+    assert mb >= w.MB
     table = torch.full((1, mb), -1, dtype=torch.int32)
     table[0, :w.MB] = w.block_table[0]
     w.block_table = table
@@ -106,7 +107,7 @@ def test_static_scratch_size_limit_is_exact(cuda_ok):
     ptok = 16
     # largest row length whose workspace still fits (workspace grows with it)
     ws = lambda mb: pa.paged_attention_partial_workspace(hz.shape_of(_boundary_workload(mb)), ptok)  # noqa: E731
-    lo, hi = 1, 1 << 16
+    lo, hi = 16, 1 << 16             # rows of at least 16 entries hold the sequence's 3 blocks
     assert ws(lo) <= limit < ws(hi)
     while hi - lo > 1:
         mid = (lo + hi) // 2
