@@ -58,6 +58,7 @@ SHARED_PREFIX = {5: 4096}       # ... or with the shared prefix read once per gr
 SHARED_PREFIX_CODES = {5: 2048}  # the same over an int8 / fp8 cache (measured best of 1024-4096)
 PROFILE_DIR = ROOT / "profiles"
 KERNEL_SOURCES = {"decode_simt": "decode_simt.cu", "decode_gqa_tc": "decode_gqa_tc.cu",
+                  "decode_gqa_umma": "decode_gqa_umma.cu",
                   "decode_simt_balanced": "decode_balanced_simt.cu",
                   "decode_tc_balanced": "decode_balanced_tc.cu",
                   "decode_int8": "decode_int8.cu",
@@ -339,8 +340,9 @@ class StepPlan:
         shape = pa.make_shape(batch=w.B, num_heads=w.H, num_kv_heads=w.Hkv, head_dim=w.D,
                               block_size=w.bs, max_blocks_per_seq=w.MB, num_blocks=w.NB,
                               block_stride=w.block_stride, dtype=w.dtype)
-        path = pa.paged_attention_decode_path(shape)
-        kernel = "decode_gqa_tc" if path == pa.PA_PATH_TENSOR_GQA else "decode_simt"
+        which = pa.paged_attention_decode_kernel(shape, o.window or 0, 0)
+        kernel = {pa.PA_KERNEL_TCGEN05: "decode_gqa_umma", pa.PA_KERNEL_MMA_SYNC: "decode_gqa_tc"}.get(
+            which, "decode_simt")
         self.quant = "fp8" if o.fp8 else "int8" if o.int8 else None
         if o.int8:
             # grouped-query shapes with 16-bit queries and head_dim 64/128 run on
@@ -383,7 +385,7 @@ class StepPlan:
         if o.balanced:
             ptok = None
             fused = not o.unfused
-            kernel = kernel.replace("decode_gqa_tc", "decode_tc") + "_balanced"
+            kernel = kernel.replace("decode_gqa_umma", "decode_tc").replace("decode_gqa_tc", "decode_tc") + "_balanced"
             bws = pa.balanced_workspace_for(w.q, w.block_table, num_kv_heads=w.Hkv, **kw)
         prefill = None
         if o.prefill:
@@ -396,6 +398,10 @@ class StepPlan:
                 "start": torch.zeros(w.B, dtype=torch.int32, device=dev),
             }
             fused = False
+        if ptok and not shared and not o.balanced and not self.quant and not o.prefill:
+            which = pa.paged_attention_decode_kernel(shape, 0, ptok)
+            kernel = {pa.PA_KERNEL_TCGEN05: "decode_gqa_umma", pa.PA_KERNEL_MMA_SYNC: "decode_gqa_tc"}.get(
+                which, "decode_simt")
         self.kernel, self.fused, self.ptok, self.window = kernel, fused, ptok, window
         self.shared, self.groups, self.ws, self.bws, self.prefill = shared, groups, ws, bws, prefill
         self.main_calls, self.app_calls = self.make_calls(prepared=True)

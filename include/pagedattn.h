@@ -278,6 +278,26 @@ typedef enum pa_path {
 } pa_path;
 pa_path paged_attention_decode_path(const pa_shape *shape);
 
+/* Which kernel a decode of `shape` runs on the CURRENT device: the single
+ * pass of paged_attention_decode / _append (window 0) or _window (window >
+ * 0) when partition_tokens is 0, else the partial pass of the split-KV pair
+ * with that partition size.  The tensor-core family has two kernels: the
+ * warp-level one (mma.sync; few long sequences also spread over
+ * thread-block clusters) and, at head_dim 128, one on the fifth-generation
+ * tensor cores (tcgen05.mma with accumulators in tensor memory, a
+ * persistent grid of at most one CTA per SM); which one runs depends on how
+ * many (sequence, kv head) units the launch has against the SM count.
+ * Results agree up to rounding order.  Returns PA_KERNEL_INVALID for a
+ * rejected shape, window or partition size.  (An implementation query: no
+ * counterpart on the pages.) */
+typedef enum pa_kernel {
+    PA_KERNEL_INVALID = 0,
+    PA_KERNEL_SIMT = 1,       /* CUDA cores                                       */
+    PA_KERNEL_MMA_SYNC = 2,   /* tensor cores, warp-level mma.sync                 */
+    PA_KERNEL_TCGEN05 = 3     /* tensor cores, tcgen05.mma and tensor memory        */
+} pa_kernel;
+pa_kernel paged_attention_decode_kernel(const pa_shape *shape, int32_t window, int32_t partition_tokens);
+
 /*
  * Split-KV ("flash decoding") pair for long contexts.
  *

@@ -11,6 +11,7 @@ paged_attention_decode_append (both in one launch), paged_kv_append_tokens
 (prefill write), paged_attention_decode_window (sliding window),
 paged_attention_partial_workspace, paged_attention_decode_partial,
 paged_attention_decode_reduce, paged_attention_decode_path,
+paged_attention_decode_kernel (which kernel runs a shape on this device),
 paged_attention_balanced_workspace, paged_attention_decode_balanced
 (persistent load-balanced schedule), paged_kv_append_int8,
 paged_attention_decode_int8 (int8 cache with per-block scales),
@@ -31,12 +32,14 @@ LIB_PATH = _PKG / "_lib" / "libpagedattn.so"
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_PATH_INVALID, PA_PATH_SIMT, PA_PATH_TENSOR_GQA = 0, 1, 2
+PA_KERNEL_INVALID, PA_KERNEL_SIMT, PA_KERNEL_MMA_SYNC, PA_KERNEL_TCGEN05 = 0, 1, 2, 3
 DEVERR_BAD_LEN, DEVERR_BAD_BLOCK, DEVERR_BAD_POS, DEVERR_TIMEOUT, DEVERR_BAD_PREFIX = 1, 2, 4, 8, 16
 
 EXPORTED = ("pa_status_string", "pa_version", "paged_kv_append", "paged_attention_decode",
             "paged_attention_decode_append", "paged_attention_decode_split_static",
             "paged_kv_append_tokens", "paged_attention_decode_window",
-            "paged_attention_decode_path", "paged_attention_partial_workspace",
+            "paged_attention_decode_path", "paged_attention_decode_kernel",
+            "paged_attention_partial_workspace",
             "paged_attention_decode_partial", "paged_attention_decode_reduce",
             "paged_attention_balanced_workspace", "paged_attention_decode_balanced",
             "paged_kv_append_int8", "paged_attention_decode_int8",
@@ -93,6 +96,8 @@ def load() -> ctypes.CDLL:
                                                           vp]
             lib.paged_attention_decode_path.restype = ctypes.c_int
             lib.paged_attention_decode_path.argtypes = [sp]
+            lib.paged_attention_decode_kernel.restype = ctypes.c_int
+            lib.paged_attention_decode_kernel.argtypes = [sp, i32, i32]
             lib.paged_attention_partial_workspace.restype = sz
             lib.paged_attention_partial_workspace.argtypes = [sp, i32]
             lib.paged_attention_decode_partial.restype = ctypes.c_int
@@ -272,6 +277,13 @@ def paged_attention_decode_window(out, q, k_pool, v_pool, block_table, seq_lens,
 
 def paged_attention_decode_path(shape: Shape) -> int:
     return int(load().paged_attention_decode_path(ctypes.byref(shape)))
+
+
+def paged_attention_decode_kernel(shape: Shape, window: int = 0, partition_tokens: int = 0) -> int:
+    """PA_KERNEL_* the decode of `shape` runs on the current device (single
+    pass, sliding window, or the split-KV partial pass when partition_tokens
+    is positive)."""
+    return load().paged_attention_decode_kernel(ctypes.byref(shape), window, partition_tokens)
 
 
 def paged_attention_partial_workspace(shape: Shape, partition_tokens: int) -> int:

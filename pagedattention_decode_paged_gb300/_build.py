@@ -23,7 +23,7 @@ LIB = LIBDIR / "libpagedattn.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "append.cu", "decode_simt.cu", "decode_gqa_tc.cu", "decode_balanced_simt.cu",
            "decode_balanced_tc.cu", "decode_int8.cu", "decode_prefix_tc.cu", "reduce.cu",
-           "decode_int8_tc.cu"]
+           "decode_int8_tc.cu", "decode_gqa_umma.cu"]
 
 
 def _nvcc() -> str:

@@ -81,7 +81,7 @@ bool tc_eligible(const pa_shape *s) {
 
 // View a pool as a [rows][head_dim] matrix; boxes of 64 x box_rows elements,
 // 128-byte swizzle.
-bool encode_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
+bool encode_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const int64_t rows_per_block = s->block_stride / s->head_dim;
@@ -89,13 +89,37 @@ bool encode_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool) {
                          (int64_t)s->num_kv_heads * s->block_size;
     cuuint64_t dims[2] = {(cuuint64_t)s->head_dim, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)s->head_dim * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows_for(s)};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     return fn(map, dt, 2, const_cast<void *>(pool), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// View a 16-bit pool with head_dim 128 as [row groups][2 halves][8 rows][64
+// elements]: dims {64, 8, 2, rows/8} with byte strides {256, 128, 2048} for
+// dims 1..3.  A box {64, 8, 2, box_rows/8} moves box_rows whole rows (both
+// 64-element halves) in one copy and lands as [group][half][8 rows][128 B]
+// with 128-byte swizzle: per half, 8-row groups 2048 bytes apart -- the
+// operand layout the tcgen05 kernel's MMAs read.  rows must be a multiple of
+// 8 (block_size a multiple of 8).
+bool encode_pool_map_groups(CUtensorMap *map, const pa_shape *s, const void *pool, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || s->head_dim != 128) return false;
+    const int64_t rows_per_block = s->block_stride / s->head_dim;
+    const int64_t rows = (s->num_blocks - 1) * rows_per_block + (int64_t)s->num_kv_heads * s->block_size;
+    if (rows % 8 != 0 || box_rows % 8 != 0) return false;
+    cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+    cuuint64_t strides[3] = {256, 128, 2048};
+    cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt =
+        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // View an int8 pool as a [rows][head_dim] byte matrix; boxes of the whole
@@ -206,7 +230,11 @@ struct MapKey {
     }
 };
 
-bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool int8 = false) {
+// kind 0: 16-bit [rows][head_dim] view, 1: int8 view, 2: 16-bit row-group view
+bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool int8 = false,
+                     int box_rows = 0, int kind = -1) {
+    if (box_rows == 0) box_rows = box_rows_for(s);
+    if (kind < 0) kind = int8 ? 1 : 0;
     constexpr int kSlots = 16;
     static std::mutex mu;
     static MapKey keys[kSlots];
@@ -216,42 +244,113 @@ bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const int64_t rows = (s->num_blocks - 1) * (s->block_stride / s->head_dim) +
                          (int64_t)s->num_kv_heads * s->block_size;
-    const MapKey key{pool, rows, s->head_dim, box_rows_for(s), int8 ? -1 - s->dtype : s->dtype, dev};
+    const MapKey key{pool, rows, s->head_dim, box_rows, kind * 16 + s->dtype, dev};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (keys[i] == key) {
             *map = maps[i];
             return true;
         }
-    if (!(int8 ? encode_int8_pool_map(map, s, pool) : encode_pool_map(map, s, pool))) return false;
+    const bool ok = kind == 1   ? encode_int8_pool_map(map, s, pool)
+                    : kind == 2 ? encode_pool_map_groups(map, s, pool, box_rows)
+                                : encode_pool_map(map, s, pool, box_rows);
+    if (!ok) return false;
     const int slot = used < kSlots ? used++ : (next++ % kSlots);
     keys[slot] = key;
     maps[slot] = *map;
     return true;
 }
 
+#ifndef PA_GQA_UMMA
+#define PA_GQA_UMMA 1   // grouped-query decode at head_dim 128 on tcgen05 (0: mma.sync kernel only)
+#endif
+
+// Shapes the tcgen05 kernel can run: tensor-core shapes at head_dim 128
+// with up to 16 query heads per CTA.
+bool umma_eligible(const pa_shape *s) {
+    // the row-group view needs every (block, kv head) chunk to start on a
+    // multiple of 8 rows
+    return PA_GQA_UMMA && (s->block_stride / s->head_dim) % 8 == 0 &&
+           s->block_size % 8 == 0 &&
+           pa::gqa_umma_supported(s->dtype, s->head_dim, s->num_heads / s->num_kv_heads);
+}
+
+// Box rows of the tcgen05 kernel's tensor maps: the largest power of two
+// (up to 128) that divides the block size, so a box never leaves a block.
+// Its tiles start on a grid of the box height (a sliding window's first tile
+// at or below the window start), so a box of a power-of-two height that
+// divides the block size never leaves its block; split partitions start
+// where the caller says, so their boxes are at most as tall as the largest
+// power of two dividing the partition size.
+int umma_box_rows(const pa_shape *s, const pa::DecodeParams &p, bool split) {
+    int rows = 128;
+    while (rows > 8 && s->block_size % rows != 0) rows >>= 1;
+    // split partitions start where the caller says (a multiple of 16)
+    while (split && rows > 16 && p.partition_tokens % rows != 0) rows >>= 1;
+    return rows;
+}
+
+// The kernel a single-pass (split == false) or split-KV decode of `s` runs
+// on this device, and the cluster size of a single pass.
+//
+// Tensor-core shapes at head_dim 128 choose between two kernels by the
+// number of units (sequence x kv head [x head group] [x partition]).  The
+// tcgen05 kernel runs at most one CTA per SM and gives every CTA the same
+// number of units, so each CTA pays its start-up and drain once: it is the
+// faster one from a third of the SM count up to the SM count (one unit per
+// CTA, where the mma.sync kernel would spread few long units over clusters)
+// and from three times the SM count up (measured on the grouped-query 70B-like
+// layer, batch 8-16 and 64-128).  In between, an equal share per CTA leaves
+// many SMs idle (e.g. 256 units: 128 CTAs of 2 units), and one mma.sync CTA
+// per unit is faster (batch 24-48).  Fewer units than a third of the SMs use
+// the clustered mma.sync kernel.
+struct DecodePlan {
+    pa_kernel kernel;
+    int cluster;
+};
+
+DecodePlan plan_decode(const pa_shape *s, int32_t window, bool split, int32_t partition_tokens) {
+    DecodePlan pl{PA_KERNEL_SIMT, 1};
+    const bool tc = tc_eligible(s);
+    const int g = s->num_heads / s->num_kv_heads;
+    int64_t units = tc ? (int64_t)s->batch * s->num_kv_heads * ((g + 15) / 16) : (int64_t)s->batch * s->num_heads;
+    if (split) units *= num_partitions(s, partition_tokens);
+    if (!split) {
+        const int tile = tc ? 16 : 4096 / (s->head_dim * elem_size(s->dtype));
+        int64_t max_len = (int64_t)s->max_blocks_per_seq * s->block_size;
+        if (window > 0 && window < max_len) max_len = window;
+        const int64_t max_tiles = (max_len + tile - 1) / tile;
+        pl.cluster = choose_cluster(units, max_tiles);
+    }
+    if (!tc) return pl;
+    pl.kernel = PA_KERNEL_MMA_SYNC;
+    const int64_t sms = sm_count();
+    if (umma_eligible(s) && sms > 0 && (units >= 3 * sms || (units < sms && 3 * units >= sms))) {
+        pl.kernel = PA_KERNEL_TCGEN05;
+        pl.cluster = 1;
+    }
+    return pl;
+}
+
 // Launch the decode kernel family chosen for `s` (final or split mode).
 pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cudaStream_t stream) {
     cudaError_t e;
-    p.cluster = 1;
-    if (!split) {
-        const bool tc = tc_eligible(s);
-        const int g = s->num_heads / s->num_kv_heads;
-        const int64_t units = tc ? (int64_t)s->batch * s->num_kv_heads * ((g + 15) / 16)
-                                 : (int64_t)s->batch * s->num_heads;
-        const int tile = tc ? 16 : 4096 / (s->head_dim * elem_size(s->dtype));
-        int64_t max_len = (int64_t)s->max_blocks_per_seq * s->block_size;
-        if (p.window > 0 && p.window < max_len) max_len = p.window;
-        const int64_t max_tiles = (max_len + tile - 1) / tile;
-        p.cluster = choose_cluster(units, max_tiles);
-    }
-    if (tc_eligible(s)) {
-        CUtensorMap kmap, vmap;
-        if (!cached_pool_map(&kmap, s, p.k_pool) || !cached_pool_map(&vmap, s, p.v_pool))
-            return PA_ERR_CUDA;
-        e = pa::launch_decode_gqa_tc(s->dtype, p, kmap, vmap, box_rows_for(s), split, stream);
-    } else {
+    const DecodePlan pl = plan_decode(s, p.window, split, p.partition_tokens);
+    p.cluster = split ? 1 : pl.cluster;
+    if (pl.kernel == PA_KERNEL_SIMT) {
         e = pa::launch_decode_simt(s->dtype, p, split, stream);
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+    CUtensorMap kmap, vmap;
+    const int rows = umma_box_rows(s, p, split);
+    if (pl.kernel == PA_KERNEL_TCGEN05 && cached_pool_map(&kmap, s, p.k_pool, false, rows, 2) &&
+        cached_pool_map(&vmap, s, p.v_pool, false, rows, 2)) {
+        // the tcgen05 kernel reads whole rows in boxes as tall as the block
+        // allows, up to a whole tile
+        e = pa::launch_decode_gqa_umma(s->dtype, p, kmap, vmap, rows, split, stream);
+    } else {
+        if (!cached_pool_map(&kmap, s, p.k_pool) || !cached_pool_map(&vmap, s, p.v_pool)) return PA_ERR_CUDA;
+        e = pa::launch_decode_gqa_tc(s->dtype, p, kmap, vmap, box_rows_for(s), split, stream);
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -363,6 +462,14 @@ pa_path paged_attention_decode_path(const pa_shape *shape) {
     if (check_shape(shape) != PA_OK || !pa::simt_supported(shape->dtype, shape->head_dim))
         return PA_PATH_INVALID;
     return tc_eligible(shape) ? PA_PATH_TENSOR_GQA : PA_PATH_SIMT;
+}
+
+pa_kernel paged_attention_decode_kernel(const pa_shape *shape, int32_t window, int32_t partition_tokens) {
+    if (check_shape(shape) != PA_OK || !pa::simt_supported(shape->dtype, shape->head_dim))
+        return PA_KERNEL_INVALID;
+    if (partition_tokens < 0 || (partition_tokens > 0 && partition_tokens % 16 != 0) || window < 0)
+        return PA_KERNEL_INVALID;
+    return plan_decode(shape, window, partition_tokens > 0, partition_tokens).kernel;
 }
 
 pa_status paged_attention_decode(const pa_shape *shape, void *out, const void *q,

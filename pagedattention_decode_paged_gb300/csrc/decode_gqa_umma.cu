@@ -1,0 +1,856 @@
+// decode_gqa_umma.cu -- grouped-query decode attention on the fifth-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory), head_dim 128,
+// 16-bit caches.
+//
+// Per (sequence, kv head[, group of up to 16 query heads][, partition]) unit
+// the work is two dense contractions per tile of 128 tokens:
+//     S^T[t][h]  = sum_d K[t][d] Q[h][d]       M = 128 tokens, N = 16, K = 128
+//     O^T[d][h] += sum_t V[t][d] P^T[t][h]     M = 128 dims,   N = 2 x heads, K = 128
+// with the online softmax down each head column in between ("KV Cache paging
+// in LLM inference", intelliparadigm.com, s2.2: scores per block, softmax
+// over the aggregated block results, weighted sum of the V blocks; "A strange
+// KV Cache bug", dpshk.com/news/5937191, s2.4: only the valid length is
+// attended).  K and V arrive by TMA as 128-byte swizzled [tokens][64-element]
+// slabs, which are at once the K-major A operand of the first MMA and the
+// MN-major A operand of the second; Q^T and P^T are the B operands, staged
+// in shared memory in the same swizzled form; S^T and O^T live in tensor
+// memory.  P is carried as a high and a low 16-bit part (the N columns of the
+// second MMA are the heads twice), which keeps the weights good to about 16
+// bits even in bf16.
+//
+// Roles (192 threads): warps 0-3 run the softmax (thread i owns token row i of
+// S^T and head_dim row i of O^T, the tensor-memory lane of its warp quarter),
+// warp 4 issues the TMA copies of a 3-stage ring, warp 5 owns the tensor
+// memory and issues the MMAs from one thread.  The grid is persistent: each
+// CTA takes an equal share of the units, one after another, so the copy
+// stream never drains between units.  O^T is rescaled in tensor memory only
+// when a head's running maximum grows by more than 2^8 (the weights of the
+// other tiles stay below 2^8, far inside 16-bit range), which after the first
+// tile almost never happens.
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "umma.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kUD = 128;                  // head_dim
+constexpr int kUTile = 128;               // tokens per tile
+#ifndef PA_UMMA_KSTAGES
+#define PA_UMMA_KSTAGES 3          // K tiles in flight or waiting
+#endif
+#ifndef PA_UMMA_VSTAGES
+#define PA_UMMA_VSTAGES 3          // V tiles in flight or waiting
+#endif
+#ifndef PA_UMMA_EQUAL_SHARES
+#define PA_UMMA_EQUAL_SHARES 1     // 1: equal unit counts per CTA; 0: one CTA per SM
+#endif
+constexpr int kSK = PA_UMMA_KSTAGES;
+constexpr int kSV = PA_UMMA_VSTAGES;
+constexpr int kUThreads = 192;
+constexpr int kUProducerWarp = 4;
+constexpr int kUMmaWarp = 5;
+constexpr int kUMaxUnits = 64;            // units one CTA takes
+constexpr float kULazy = 8.f;             // rescale O^T when a max grows by more (log2 units)
+constexpr int kRowsRing = 8;              // tiles whose box rows the producer remembers (K ahead of V)
+constexpr int kVNewRing = 4;              // appended V rows kept for the P.V step
+
+// A K (or V) tile in shared memory: [16 groups of 8 tokens][2 halves of 64
+// elements][8 rows][128 bytes], 128-byte swizzled -- the layout one box of
+// the row-group tensor map lands in.  Per half, token groups are kGroup bytes
+// apart; the two halves of a group kHalf bytes apart.
+constexpr uint32_t kHalf = 8 * 128;
+constexpr uint32_t kGroup = 2 * kHalf;
+constexpr uint32_t kTileBytes = (kUTile / 8) * kGroup;
+
+// byte offset of 16-byte chunk c (0..15) of token row r inside a tile
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
+    return (uint32_t)((r >> 3) * kGroup + (c >> 3) * kHalf + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int NT>
+struct ULayout {
+    static constexpr int NH = 8 * NT;                 // head columns (the MMA N of S^T is 16)
+    static constexpr int N2 = 2 * NH;                 // P^T rows: high parts, then low parts
+    static constexpr uint32_t kKRing = 0;                         // K tiles [kSK]
+    static constexpr uint32_t kVRing = kSK * kTileBytes;          // V tiles [kSV]
+    static constexpr uint32_t kQ = (kSK + kSV) * kTileBytes;      // Q^T: 2 buffers x 2 slabs x 16 rows
+    static constexpr uint32_t kQBuf = 2 * 16 * 128;
+    static constexpr uint32_t kP = kQ + 2 * kQBuf;                // P^T: 2 buffers x 2 slabs x N2 rows
+    static constexpr uint32_t kPSlab = N2 * 128;
+    static constexpr uint32_t kPBuf = 2 * kPSlab;
+    static constexpr uint32_t kRed = kP + 2 * kPBuf;              // tile maxima [2][4][16]
+    static constexpr uint32_t kLsum = kRed + 2 * 4 * 16 * 4;      // epilogue sums [4][16]
+    static constexpr uint32_t kRows = kLsum + 4 * 16 * 4;         // box rows [kRowsRing][32]
+    static constexpr uint32_t kVNew = kRows + kRowsRing * 32 * 4; // appended V rows [kVNewRing][256 B]
+    static constexpr uint32_t kBars = kVNew + kVNewRing * 256;
+    enum {
+        K_FULL = 0,
+        K_EMPTY = K_FULL + kSK,
+        V_FULL = K_EMPTY + kSK,
+        V_EMPTY = V_FULL + kSV,
+        S_FULL = V_EMPTY + kSV,
+        S_FREE = S_FULL + 2,
+        P_FULL = S_FREE + 2,
+        P_EMPTY = P_FULL + 2,
+        Q_FREE = P_EMPTY + 2,
+        SYNC = Q_FREE + 2,     // the softmax warps' own barrier
+        END = SYNC + 1,
+        NBARS = END + 1
+    };
+    static constexpr uint32_t kTmemSlot = kBars + NBARS * 8;
+    static constexpr uint32_t kFlags = (kTmemSlot + 4 + 15) & ~15u;   // bad table entry per unit
+    static constexpr uint32_t kLens = kFlags + kUMaxUnits * 4;        // valid tokens per unit
+    static constexpr uint32_t kTbl = kLens + kUMaxUnits * 4;          // table entries, an equal slot per unit
+    static constexpr int kTblCap = NT == 1 ? 2048 : 1536;
+    static constexpr uint32_t kEnd = kTbl + kTblCap * 4;
+    static constexpr size_t kBytes = 1024 + kEnd;
+    // tensor memory: S^T in two buffers of 16 columns, O^T in two of N2
+    static constexpr uint32_t kColO = 32;
+    static constexpr uint32_t kCols = 32 + 2 * N2 <= 64 ? 64 : 128;
+};
+
+static_assert(ULayout<1>::kBytes <= 232448 && ULayout<2>::kBytes <= 232448, "shared memory per CTA");
+
+struct UUnit {
+    int b, hk, hg, part, h0, nh;
+    int len;            // valid tokens of the sequence (after the fused append)
+    int t_begin, t_end; // tokens of this unit; tiles start at t_begin
+    int t_win;          // first attended token (sliding window), else t_begin
+    int t_pool;         // tokens below this come from the pool (the fused token does not)
+    int ntiles;
+    int bad_len;        // PA_DEVERR bit for a length outside the table row, else 0
+};
+
+// Valid tokens of unit u's sequence: the fused append's position + 1, else
+// its length.
+template <bool SPLIT>
+__device__ __forceinline__ int unit_len(const DecodeParams &p, int u) {
+    const int b = u % p.B;
+    return (!SPLIT && p.positions != nullptr) ? p.positions[b] + 1 : p.seq_lens[b];
+}
+
+// align: the box height, a multiple of 16 that tiles must start on (a
+// sliding window's first tile starts at or below the window on that grid)
+template <bool SPLIT>
+__device__ __forceinline__ UUnit unit_of(const DecodeParams &p, int u, int len, int align) {
+    UUnit x;
+    const int g = p.H / p.Hkv;
+    const int ngroups = (g + 15) / 16;
+    x.b = u % p.B;
+    u /= p.B;
+    x.hg = u % ngroups;
+    u /= ngroups;
+    x.hk = u % p.Hkv;
+    x.part = u / p.Hkv;
+    x.h0 = x.hk * g + x.hg * 16;
+    x.nh = min(16, g - x.hg * 16);
+    const bool fused = !SPLIT && p.positions != nullptr;
+    x.len = len;
+    x.bad_len = 0;
+    if (x.len < (fused ? 1 : 0) || (int64_t)x.len > (int64_t)p.MB * p.bs) {
+        x.bad_len = fused ? PA_DEVERR_BAD_POS : PA_DEVERR_BAD_LEN;
+        x.t_begin = x.t_end = x.t_win = x.t_pool = x.ntiles = 0;
+        return x;
+    }
+    const int t_win = (!SPLIT && p.window > 0) ? max(0, x.len - p.window) : 0;
+    x.t_begin = SPLIT ? x.part * p.partition_tokens : t_win / align * align;
+    x.t_end = SPLIT ? min(x.len, x.t_begin + p.partition_tokens) : x.len;
+    x.t_win = SPLIT ? x.t_begin : t_win;
+    x.t_pool = fused ? x.t_end - 1 : x.t_end;
+    x.ntiles = x.t_end > x.t_begin ? (x.t_end - x.t_begin + kUTile - 1) / kUTile : 0;
+    return x;
+}
+
+// byte offset of 16-byte chunk c (0..7) of row r inside 128-byte swizzled
+// rows whose 8-row groups are 1024-byte aligned
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Position in the sequence of tiles of one CTA: tile i of its k-th unit, the
+// g-th tile overall, kact units with tiles before this one.
+struct UIter {
+    int k, i, g, kact;
+    UUnit x;
+};
+
+}  // namespace
+
+template <typename T, int NT, bool SPLIT>
+__global__ void __launch_bounds__(kUThreads, 1)
+    decode_gqa_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           DecodeParams p, int box_rows, int units) {
+    using L = ULayout<NT>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdesc1 = f16_idesc(kBf16, false, false, 128, 16);
+    constexpr uint32_t kIdesc2 = f16_idesc(kBf16, true, false, 128, L::N2);
+    grid_dependency_wait();
+    allow_dependents();
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlags);   // bad table entry per unit
+    float *red = reinterpret_cast<float *>(smem + L::kRed);
+    float *lsum = reinterpret_cast<float *>(smem + L::kLsum);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // this CTA's units: a contiguous range, the ranges of all CTAs as equal as
+    // the grid allows (at most kUMaxUnits each)
+    const int tile_align = box_rows < 16 ? 16 : box_rows;
+    const int u_first = (int)(((int64_t)blockIdx.x * units) / gridDim.x);
+    const int nunits = (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x) - u_first;
+    int *lens = reinterpret_cast<int *>(smem + L::kLens);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < L::NBARS; ++i) {
+            int count = 1;
+            // the softmax warps arrive once per warp (lane 0, after __syncwarp)
+            if (i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL || i == L::P_FULL + 1 || i == L::SYNC)
+                count = 4;
+            if (i == L::P_EMPTY || i == L::P_EMPTY + 1) count = 2;   // the MMA commit and a plain arrival
+            mbar_init(bar(i), count);
+        }
+        for (int i = 0; i < kUMaxUnits; ++i) flags[i] = 0;
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    // Stage the block-table entries the units' boxes will read, one slot of
+    // tbl_slot entries per unit (a unit that needs more reads them from
+    // global memory).  The entries a unit starts at do not depend on its
+    // length (block 0, or its split partition's first block), so they are
+    // loaded in the same round trip as the lengths; a sliding window starts
+    // at a length-dependent block and is staged after the lengths.
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kTbl);
+    const int tbl_slot = nunits > 0 ? L::kTblCap / nunits : 0;
+    const bool spec = SPLIT || p.window <= 0;
+    auto first_block = [&](int u) {
+        if (!SPLIT) return 0;
+        const int g = p.H / p.Hkv;
+        return (int)((int64_t)(u / (p.B * ((g + 15) / 16) * p.Hkv)) * p.partition_tokens / p.bs);
+    };
+    if ((int)threadIdx.x < nunits) lens[threadIdx.x] = unit_len<SPLIT>(p, u_first + threadIdx.x);
+    if (spec)
+        for (int k = warp; k < nunits; k += kUThreads / 32) {
+            const int j0 = first_block(u_first + k);
+            const int n = min(tbl_slot, p.MB - j0);
+            const int b = (u_first + k) % p.B;
+            for (int e = lane; e < n; e += 32) tbl[k * tbl_slot + e] = p.block_table[(int64_t)b * p.MB + j0 + e];
+        }
+    mbar_init_fence();
+    if (warp == kUMmaWarp) {
+        tmem_alloc(sbase + L::kTmemSlot, L::kCols);
+        tmem_relinquish();
+        tc05_fence_before_sync();
+    }
+    __syncthreads();
+    // entries [j0, j0 + n) of unit x sit at tbl[k * tbl_slot + j - j0] when
+    // n <= tbl_slot (n = 0: the unit reads nothing from the pool)
+    auto staged_entries = [&](int k, const UUnit &x, int &j0) {
+        j0 = spec ? first_block(u_first + k) : x.t_begin / p.bs;
+        const int n = x.t_pool > x.t_begin ? (x.t_pool - 1) / p.bs + 1 - j0 : 0;
+        return n <= (spec ? min(tbl_slot, p.MB - j0) : tbl_slot);
+    };
+    if (!spec) {
+        for (int k = warp; k < nunits; k += kUThreads / 32) {
+            const UUnit x = unit_of<SPLIT>(p, u_first + k, lens[k], tile_align);
+            int j0;
+            if (!staged_entries(k, x, j0)) continue;
+            const int n = x.t_pool > x.t_begin ? (x.t_pool - 1) / p.bs + 1 - j0 : 0;
+            for (int e = lane; e < n; e += 32) tbl[k * tbl_slot + e] = p.block_table[(int64_t)x.b * p.MB + j0 + e];
+        }
+        __syncthreads();
+    }
+    tc05_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    T *out = reinterpret_cast<T *>(p.out);
+    const bool fused = !SPLIT && p.positions != nullptr;
+    auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
+    auto block_of = [&](int t) { return p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs; };
+    auto unit_at = [&](int k) { return unit_of<SPLIT>(p, u_first + k, lens[k], tile_align); };
+    // tile iteration shared by the producer and the MMA warp
+    auto it_skip = [&](UIter &it) {
+        while (it.k < nunits && it.i >= it.x.ntiles) {
+            if (it.x.ntiles > 0) ++it.kact;
+            ++it.k;
+            it.i = 0;
+            if (it.k < nunits) it.x = unit_at(it.k);
+        }
+    };
+    auto it_init = [&](UIter &it) {
+        it.k = it.i = it.g = it.kact = 0;
+        it.x = unit_at(0);
+        it_skip(it);
+    };
+    auto it_next = [&](UIter &it) {
+        ++it.i;
+        ++it.g;
+        it_skip(it);
+    };
+
+    if (warp == kUProducerWarp) {
+        // ------------------------------------------------------------------
+        // TMA producer: lane s fetches box s (box_rows tokens) of each tile,
+        // K into the K ring as soon as a K stage is free, V into the V ring
+        // as soon as a V stage is free (K runs ahead: it is consumed first);
+        // the table entries of the next K tile are loaded one tile ahead
+        // ------------------------------------------------------------------
+        const int subs = kUTile / box_rows;
+        const uint32_t box_bytes = (uint32_t)box_rows * 256;    // both halves of box_rows rows
+        int32_t *rows = reinterpret_cast<int32_t *>(smem + L::kRows);
+        UIter kq, vq;
+        if (nunits > 0) {
+            it_init(kq);
+            it_init(vq);
+        } else {
+            kq.k = vq.k = 0;
+            kq.g = vq.g = 0;
+        }
+        int32_t blk = -1;
+        int j = 0, t = 0;
+        bool act = false;
+        auto load_entry = [&]() {
+            act = false;
+            if (kq.k >= nunits) return;
+            t = kq.x.t_begin + kq.i * kUTile + lane * box_rows;
+            act = lane < subs && t < kq.x.t_pool;
+            if (act) {
+                j = block_of(t);
+                int j0;
+                const bool staged = staged_entries(kq.k, kq.x, j0);
+                blk = staged ? tbl[kq.k * tbl_slot + j - j0] : p.block_table[(int64_t)kq.x.b * p.MB + j];
+            }
+        };
+        load_entry();
+        uint32_t idle = 0;
+        bool abort = false;
+        while (vq.k < nunits) {
+            bool progress = false;
+            if (kq.k < nunits && kq.g - vq.g < kRowsRing) {
+                const int g = kq.g, st = g % kSK;
+                if (g < kSK || __all_sync(0xffffffffu, mbar_test(bar(L::K_EMPTY + st), ((g / kSK) - 1) & 1))) {
+                    const bool bad = act && !good(blk);
+                    const bool active = act && !bad;
+                    const int32_t y = active ? blk * p.rows_per_block + kq.x.hk * p.bs + (t - j * p.bs) : -1;
+                    rows[(g % kRowsRing) * 32 + lane] = y;
+                    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+                        flags[kq.k] = 1;
+                        report(p.err_word, PA_DEVERR_BAD_BLOCK);
+                    }
+                    const uint32_t bytes = __reduce_add_sync(0xffffffffu, active ? box_bytes : 0u);
+                    const uint32_t full = bar(L::K_FULL + st);
+                    if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+                    __syncwarp();
+                    if (active) {
+                        const uint32_t dk = sbase + L::kKRing + st * kTileBytes + lane * box_bytes;
+                        tma_4d_g2s(dk, &kmap, 0, 0, 0, y >> 3, full);
+                    }
+                    it_next(kq);
+                    load_entry();
+                    progress = true;
+                }
+            }
+            if (vq.g < kq.g) {
+                const int g = vq.g, st = g % kSV;
+                if (g < kSV || __all_sync(0xffffffffu, mbar_test(bar(L::V_EMPTY + st), ((g / kSV) - 1) & 1))) {
+                    __syncwarp();
+                    const int32_t y = rows[(g % kRowsRing) * 32 + lane];
+                    const bool active = y >= 0;
+                    const uint32_t bytes = __reduce_add_sync(0xffffffffu, active ? box_bytes : 0u);
+                    const uint32_t full = bar(L::V_FULL + st);
+                    if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+                    __syncwarp();
+                    if (active) {
+                        const uint32_t dv = sbase + L::kVRing + st * kTileBytes + lane * box_bytes;
+                        tma_4d_g2s(dv, &vmap, 0, 0, 0, y >> 3, full);
+                    }
+                    it_next(vq);
+                    progress = true;
+                }
+            }
+            if (progress) {
+                idle = 0;
+            } else if (++idle > kWaitLimit) {
+                abort = true;
+                break;
+            }
+        }
+        if (abort && lane == 0) report(p.err_word, PA_DEVERR_TIMEOUT);
+        // every copy this warp issued has landed before the CTA may exit
+        for (int gg = max(0, kq.g - kSK); gg < kq.g; ++gg) mbar_wait(bar(L::K_FULL + gg % kSK), (gg / kSK) & 1);
+        for (int gg = max(0, vq.g - kSV); gg < vq.g; ++gg) mbar_wait(bar(L::V_FULL + gg % kSV), (gg / kSV) & 1);
+    } else if (warp == kUMmaWarp) {
+        // ------------------------------------------------------------------
+        // MMA issue (one thread) and tile preparation (the whole warp): O^T +=
+        // V^T P^T as soon as a V tile and the softmax's P^T are ready (first:
+        // it frees a V stage and lets the softmax move on), S^T = K Q^T as
+        // soon as a K tile and an S buffer are ready; the first product runs
+        // at most 3 tiles ahead of the second
+        // ------------------------------------------------------------------
+        UIter m1, m2;
+        if (nunits > 0) {
+            it_init(m1);
+            it_init(m2);
+        } else {
+            m1.k = m2.k = 0;
+            m1.g = m2.g = 0;
+        }
+        unsigned char *vnew = smem + L::kVNew;
+        // Q rows, the fused new row and its pool block of the next unit with
+        // tiles, fetched one unit ahead: chunk c = lane + 32 i is 16-byte
+        // piece c % 16 of head c / 16 (heads 0-7 in qn, 8-15 in qn2)
+        uint4 qn[4], qn2[4];
+        uint4 kn_new = make_uint4(0, 0, 0, 0), vn_new = make_uint4(0, 0, 0, 0);
+        int32_t nb_new = -1;
+        auto fetch_unit = [&](int k) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qn[i] = qn2[i] = make_uint4(0, 0, 0, 0);
+            while (k < nunits && unit_at(k).ntiles == 0) ++k;
+            if (k >= nunits) return;
+            const UUnit x = unit_at(k);
+            const char *qp = reinterpret_cast<const char *>(p.q) + ((int64_t)x.b * p.H + x.h0) * (kUD * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane + 32 * i;
+                const int h = c >> 4;
+                if (h < x.nh) qn[i] = *reinterpret_cast<const uint4 *>(qp + h * (kUD * 2) + (c & 15) * 16);
+                if (NT == 2 && 8 + h < x.nh)
+                    qn2[i] = *reinterpret_cast<const uint4 *>(qp + (8 + h) * (kUD * 2) + (c & 15) * 16);
+            }
+            if (fused && lane < 16) {
+                const int64_t src = ((int64_t)x.b * p.Hkv + x.hk) * (kUD * 2) + lane * 16;
+                kn_new = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                vn_new = *reinterpret_cast<const uint4 *>(p.v_new + src);
+                nb_new = p.block_table[(int64_t)x.b * p.MB + block_of(x.t_end - 1)];
+            }
+        };
+        if (nunits > 0) fetch_unit(m1.k);
+        uint4 k_new_row = make_uint4(0, 0, 0, 0);
+        uint32_t idle = 0;
+        bool abort = false;
+        while (m2.k < nunits) {
+            bool progress = false;
+            if (m2.g < m1.g) {
+                const int g = m2.g;
+                bool ready = __all_sync(0xffffffffu, mbar_test(bar(L::V_FULL + g % kSV), (g / kSV) & 1));
+                if (ready) ready = __all_sync(0xffffffffu, mbar_test(bar(L::P_FULL + (g & 1)), (g >> 1) & 1));
+                if (ready) {
+                    const UUnit &x = m2.x;
+                    const int t0 = x.t_begin + m2.i * kUTile;
+                    const int nvalid = min(kUTile, x.t_end - t0);
+                    const bool last = m2.i == x.ntiles - 1;
+                    unsigned char *vs = smem + L::kVRing + (g % kSV) * kTileBytes;
+                    // rows past the length hold padding, poison or another unit's
+                    // rows: their weight is 0 and V must be finite so that 0 * V
+                    // stays 0.  Swizzling permutes chunks inside a row only, so a
+                    // row is whole 128-byte lines, one per half.
+                    const int zend = kUTile;
+                    if (nvalid < zend) {
+                        for (uint32_t o = (nvalid >> 3) * kGroup + lane * 16; o < kTileBytes; o += 32 * 16) {
+                            const int r = (int)((o / kGroup) * 8 + (o % kHalf) / 128);
+                            if (r >= nvalid) *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    if (fused && last && lane < 16)
+                        *reinterpret_cast<uint4 *>(vs + tile_chunk(nvalid - 1, lane)) =
+                            *reinterpret_cast<const uint4 *>(vnew + (m2.kact % kVNewRing) * 256 + lane * 16);
+                    if (nvalid < zend || (fused && last)) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc05_fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t vb = sbase + L::kVRing + (g % kSV) * kTileBytes;
+                        const uint32_t pb = sbase + L::kP + (g & 1) * L::kPBuf;
+                        const uint32_t d = tmem + L::kColO + (m2.kact & 1) * L::N2;
+#pragma unroll
+                        for (int kk = 0; kk < kUTile / 16; ++kk) {
+                            // V^T: 64-dim atoms kHalf apart, 8-token groups kGroup apart
+                            const uint64_t a = sw128_desc(vb + kk * 2 * kGroup, kHalf, kGroup);
+                            const uint64_t bd = sw128_desc(pb + (kk >> 2) * L::kPSlab + (kk & 3) * 32, 0, 1024);
+                            umma_f16(d, a, bd, kIdesc2, !(m2.i == 0 && kk == 0));
+                        }
+                        umma_commit(bar(L::P_EMPTY + (g & 1)));
+                        umma_commit(bar(L::V_EMPTY + g % kSV));
+                        // the plain arrival carries this warp's view of the unit
+                        // flags to the softmax warps that wait on the same barrier
+                        mbar_arrive(bar(L::P_EMPTY + (g & 1)));
+                    }
+                    __syncwarp();
+                    it_next(m2);
+                    progress = true;
+                }
+            }
+            if (m1.k < nunits && m1.g - m2.g < 4) {
+                const int g = m1.g;
+                const int qb = m1.kact & 1;
+                bool ready = __all_sync(0xffffffffu, mbar_test(bar(L::K_FULL + g % kSK), (g / kSK) & 1));
+                if (ready && g >= 2)
+                    ready = __all_sync(0xffffffffu, mbar_test(bar(L::S_FREE + (g & 1)), ((g >> 1) - 1) & 1));
+                if (ready && m1.i == 0 && m1.kact >= 2)
+                    ready = __all_sync(0xffffffffu, mbar_test(bar(L::Q_FREE + qb), ((m1.kact >> 1) - 1) & 1));
+                if (ready) {
+                    const UUnit &x = m1.x;
+                    if (m1.i == 0) {
+                        // Q^T of this unit: rows = heads (zero past nh)
+                        unsigned char *qs = smem + L::kQ + qb * L::kQBuf;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int c = lane + 32 * i;
+                            const int h = c >> 4, piece = c & 15;
+                            *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(h, piece & 7)) = qn[i];
+                            *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(8 + h, piece & 7)) = qn2[i];
+                        }
+                        if (fused) {
+                            k_new_row = kn_new;
+                            // the V row waits in shared memory for this unit's last P.V step
+                            if (lane < 16)
+                                *reinterpret_cast<uint4 *>(vnew + (m1.kact % kVNewRing) * 256 + lane * 16) = vn_new;
+                            if (x.hg == 0) {
+                                // the step's new row goes to its pool slot (one unit per
+                                // (sequence, kv head) writes it); the arrival on P_EMPTY
+                                // after this unit's P.V steps publishes a bad target's flag
+                                const int pos = x.t_end - 1;
+                                if (!good(nb_new)) {
+                                    if (lane == 0) {
+                                        flags[m1.k] = 1;
+                                        report(p.err_word, PA_DEVERR_BAD_BLOCK);
+                                    }
+                                } else if (lane < 16) {
+                                    const int64_t dst = (int64_t)nb_new * p.block_stride_bytes +
+                                                        ((int64_t)x.hk * p.bs + (pos - block_of(pos) * p.bs)) * (kUD * 2) +
+                                                        lane * 16;
+                                    *reinterpret_cast<uint4 *>(p.k_pool_w + dst) = kn_new;
+                                    *reinterpret_cast<uint4 *>(p.v_pool_w + dst) = vn_new;
+                                }
+                            }
+                        }
+                        fetch_unit(m1.k + 1);
+                    }
+                    const int t0 = x.t_begin + m1.i * kUTile;
+                    const int nvalid = min(kUTile, x.t_end - t0);
+                    const bool last = m1.i == x.ntiles - 1;
+                    if (fused && last && lane < 16) {
+                        // the appended token: its K row comes from k_new
+                        unsigned char *ks = smem + L::kKRing + (g % kSK) * kTileBytes;
+                        *reinterpret_cast<uint4 *>(ks + tile_chunk(nvalid - 1, lane)) = k_new_row;
+                    }
+                    if (m1.i == 0 || (fused && last)) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc05_fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t kb = sbase + L::kKRing + (g % kSK) * kTileBytes;
+                        const uint32_t qbase = sbase + L::kQ + qb * L::kQBuf;
+                        const uint32_t d = tmem + (g & 1) * 16;
+#pragma unroll
+                        for (int kk = 0; kk < kUD / 16; ++kk) {
+                            // K: K step kk in half kk / 4, 8-token groups kGroup apart
+                            const uint64_t a = sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 0, kGroup);
+                            const uint64_t bd = sw128_desc(qbase + (kk >> 2) * 2048 + (kk & 3) * 32, 0, 1024);
+                            umma_f16(d, a, bd, kIdesc1, kk > 0);
+                        }
+                        umma_commit(bar(L::S_FULL + (g & 1)));
+                        umma_commit(bar(L::K_EMPTY + g % kSK));
+                        if (last) umma_commit(bar(L::Q_FREE + qb));
+                    }
+                    __syncwarp();
+                    it_next(m1);
+                    progress = true;
+                }
+            }
+            if (progress) {
+                idle = 0;
+            } else if (++idle > kWaitLimit) {
+                abort = true;
+                break;
+            }
+        }
+        if (abort && lane == 0) report(p.err_word, PA_DEVERR_TIMEOUT);
+        // every MMA this warp issued has completed before tensor memory is freed
+        if (lane == 0) umma_commit(bar(L::END));
+        __syncwarp();
+        mbar_wait(bar(L::END), 0);
+    } else {
+        // ------------------------------------------------------------------
+        // softmax (warps 0-3): thread r owns token row r of S^T and head_dim
+        // row r of O^T (tensor-memory lane r)
+        // ------------------------------------------------------------------
+        const int r = threadIdx.x;
+        const int q4 = warp;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        constexpr int NH = L::NH;
+        int g = 0, kact = 0;
+        bool abort = false;
+        // barrier of the 128 softmax threads with a bounded wait (a bar.sync
+        // would wait forever for a warp that gave up)
+        uint32_t rounds = 0;
+        auto sync128 = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::SYNC));
+            return __all_sync(0xffffffffu, mbar_wait(bar(L::SYNC), (rounds++) & 1));
+        };
+        // The epilogue of a unit runs after the next unit's first tile, so that
+        // the wait for the unit's last P.V product overlaps useful work.
+        bool pend = false;
+        int pk = 0, pgl = 0, pob = 0;
+        UUnit px;
+        float pmu[NH], pmt[NH], plp[NH];
+        auto epilogue = [&]() -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(L::P_EMPTY + (pgl & 1)), (pgl >> 1) & 1))) return false;
+            tc05_fence_after_sync();
+            float o[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) o[h] = 0.f;
+#pragma unroll
+            for (int part = 0; part < L::N2 / 8; ++part) {
+                float v[8];
+                tmem_ld8(tmem + lane_base + L::kColO + pob * L::N2 + part * 8, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[(part * 8 + e) % NH] += v[e];
+            }
+            tc05_fence_before_sync();
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                float v = plp[h];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                if (lane == 0) lsum[q4 * 16 + h] = v;
+            }
+            if (!sync128()) return false;
+            const bool bad = flags[pk] != 0;
+            const int64_t pbh0 = (int64_t)px.b * p.H + px.h0;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                if (h >= px.nh) break;
+                const float lt = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+                if (!SPLIT) {
+                    out[(pbh0 + h) * kUD + r] = Elem<T>::from_float(bad ? 0.f : o[h] / lt);
+                } else {
+                    // the workspace keeps the state relative to the true maximum
+                    const float f = merge_weight(pmu[h], pmt[h]);
+                    const int64_t ws = (pbh0 + h) * p.num_partitions + px.part;
+                    p.ws_acc[ws * kUD + r] = o[h] * f;
+                    if (r == 0) {
+                        p.ws_m[ws] = pmt[h];
+                        p.ws_l[ws] = bad ? -1.f : lt * f;
+                    }
+                }
+            }
+            // the sums of this unit are read before the next unit's are written
+            return sync128();
+        };
+        for (int k = 0; k < nunits && !abort; ++k) {
+            const UUnit x = unit_at(k);
+            const int64_t bh0 = (int64_t)x.b * p.H + x.h0;
+            if (x.bad_len || x.ntiles == 0) {
+                if (x.bad_len && r == 0) report(p.err_word, x.bad_len);
+                if (!SPLIT)
+                    for (int h = 0; h < x.nh; ++h) out[(bh0 + h) * kUD + r] = Elem<T>::from_float(0.f);
+                continue;
+            }
+            const int ob = kact & 1;
+            float m_used[NH], m_true[NH], l_part[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                m_used[h] = -INFINITY;
+                m_true[h] = -INFINITY;
+                l_part[h] = 0.f;
+            }
+            for (int i = 0; i < x.ntiles; ++i, ++g) {
+                const int sb = g & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(L::S_FULL + sb), (g >> 1) & 1))) {
+                    abort = true;
+                    break;
+                }
+                tc05_fence_after_sync();
+                float s[NH];
+                {
+                    float v[8];
+                    tmem_ld8(tmem + lane_base + sb * 16, v);
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) s[h] = v[h];
+                    if constexpr (NT == 2) {
+                        float w[8];
+                        tmem_ld8(tmem + lane_base + sb * 16 + 8, w);
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) s[8 + h] = w[h];
+                    }
+                }
+                tmem_wait_ld();
+                tc05_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::S_FREE + sb));
+                const int t = x.t_begin + i * kUTile + r;
+                const bool valid = t >= x.t_win && t < x.t_end;
+                float xs[NH];
+#pragma unroll
+                for (int h = 0; h < NH; ++h) xs[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+                float *rb = red + (g & 1) * 64;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const float wm = warp_max_f32(xs[h]);
+                    if (lane == 0) rb[q4 * 16 + h] = wm;
+                }
+                if (!sync128()) {
+                    abort = true;
+                    break;
+                }
+                bool need = false;
+                float tmax[NH];
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    tmax[h] = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
+                    m_true[h] = fmaxf(m_true[h], tmax[h]);
+                    need |= tmax[h] > m_used[h] + kULazy;
+                }
+                if (need) {
+                    float corr[NH];
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        const float mn = fmaxf(m_used[h], tmax[h]);
+                        corr[h] = merge_weight(m_used[h], mn);
+                        l_part[h] *= corr[h];
+                        m_used[h] = mn;
+                    }
+                    if (i > 0) {
+                        // O^T holds the earlier tiles: wait for the last P.V
+                        // MMA, then rescale this thread's head_dim row
+                        const int gp = g - 1;
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar(L::P_EMPTY + (gp & 1)), (gp >> 1) & 1))) {
+                            abort = true;
+                            break;
+                        }
+                        tc05_fence_after_sync();
+#pragma unroll
+                        for (int part = 0; part < L::N2 / 8; ++part) {
+                            float v[8];
+                            const uint32_t ta = tmem + lane_base + L::kColO + ob * L::N2 + part * 8;
+                            tmem_ld8(ta, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] *= corr[(part * 8 + e) % NH];
+                            tmem_st8(ta, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                float pv[NH];
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    pv[h] = valid ? ex2_approx(xs[h] - m_used[h]) : 0.f;
+                    l_part[h] += pv[h];
+                }
+                // P^T buffer g & 1 is free once the P.V MMA of tile g - 2 is done
+                if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(L::P_EMPTY + (g & 1)), ((g >> 1) - 1) & 1))) {
+                    abort = true;
+                    break;
+                }
+                unsigned char *pbuf = smem + L::kP + (g & 1) * L::kPBuf + (r >> 6) * L::kPSlab;
+                const int rc = (r & 63) >> 3, re = (r & 7) * 2;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const T hi = Elem<T>::from_float(pv[h]);
+                    const T lo = Elem<T>::from_float(pv[h] - Elem<T>::to_float(hi));
+                    *reinterpret_cast<T *>(pbuf + sw128(h, rc) + re) = hi;
+                    *reinterpret_cast<T *>(pbuf + sw128(NH + h, rc) + re) = lo;
+                }
+                fence_proxy_async_smem();
+                tc05_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::P_FULL + (g & 1)));
+                if (i == 0 && pend) {
+                    pend = false;
+                    if (!epilogue()) {
+                        abort = true;
+                        break;
+                    }
+                }
+            }
+            if (abort) break;
+            // this unit's epilogue waits for the next unit's first tile
+            pend = true;
+            pk = k;
+            pgl = g - 1;
+            pob = kact & 1;
+            px = x;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                pmu[h] = m_used[h];
+                pmt[h] = m_true[h];
+                plp[h] = l_part[h];
+            }
+            ++kact;
+        }
+        if (!abort && pend && !epilogue()) abort = true;
+        if (abort && r == 0) report(p.err_word, PA_DEVERR_TIMEOUT);
+    }
+
+    tc05_fence_before_sync();
+    __syncthreads();
+    if (warp == kUMmaWarp) {
+        tc05_fence_after_sync();
+        tmem_dealloc(tmem, L::kCols);
+    }
+}
+
+template <typename T, int NT, bool SPLIT>
+static cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                 int box_rows, cudaStream_t stream) {
+    using Lay = ULayout<NT>;
+    auto kern = decode_gqa_umma_kernel<T, NT, SPLIT>;
+    static std::atomic<int> configured[64];
+    cudaError_t e = ensure_smem_limit(kern, Lay::kBytes, configured);
+    if (e != cudaSuccess) return e;
+    const int g = p.H / p.Hkv;
+    const int64_t units = (int64_t)p.B * p.Hkv * ((g + 15) / 16) * (SPLIT ? p.num_partitions : 1);
+    if (units == 0) return cudaSuccess;
+    if (units > INT32_MAX) return cudaErrorInvalidValue;
+    int sms = 0;
+    e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+#if PA_UMMA_EQUAL_SHARES
+    // the same number of units for every CTA (some SMs may stay idle)
+    const int64_t per = (units + sms - 1) / sms;
+    int64_t grid = (units + per - 1) / per;
+#else
+    // one CTA per SM, unit counts differing by at most one
+    int64_t grid = units < sms ? units : sms;
+#endif
+    if (grid < (units + kUMaxUnits - 1) / kUMaxUnits) grid = (units + kUMaxUnits - 1) / kUMaxUnits;
+    return launch_clustered(kern, grid, kUThreads, Lay::kBytes, 1, stream, kmap, vmap, p, box_rows, (int)units);
+}
+
+bool gqa_umma_supported(int dtype, int head_dim, int group) {
+    return (dtype == PA_F16 || dtype == PA_BF16) && head_dim == 128 && group >= 1 && group <= 16;
+}
+
+cudaError_t launch_decode_gqa_umma(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
+                                   const CUtensorMap &vmap, int box_rows, bool split, cudaStream_t stream) {
+    const int g = p.H / p.Hkv;
+    if (!gqa_umma_supported(dtype, p.D, g)) return cudaErrorInvalidValue;
+    const bool two = g > 8;
+    if (dtype == PA_BF16) {
+        if (split)
+            return two ? launch_umma_t<__nv_bfloat16, 2, true>(p, kmap, vmap, box_rows, stream)
+                       : launch_umma_t<__nv_bfloat16, 1, true>(p, kmap, vmap, box_rows, stream);
+        return two ? launch_umma_t<__nv_bfloat16, 2, false>(p, kmap, vmap, box_rows, stream)
+                   : launch_umma_t<__nv_bfloat16, 1, false>(p, kmap, vmap, box_rows, stream);
+    }
+    if (split)
+        return two ? launch_umma_t<__half, 2, true>(p, kmap, vmap, box_rows, stream)
+                   : launch_umma_t<__half, 1, true>(p, kmap, vmap, box_rows, stream);
+    return two ? launch_umma_t<__half, 2, false>(p, kmap, vmap, box_rows, stream)
+               : launch_umma_t<__half, 1, false>(p, kmap, vmap, box_rows, stream);
+}
+
+}  // namespace pa

@@ -219,6 +219,14 @@ cudaError_t launch_decode_gqa_tc(int dtype, const DecodeParams &p, const CUtenso
                                  cudaStream_t stream);
 bool gqa_tc_supported(int dtype, int head_dim);
 
+// Tensor-core GQA decode on tcgen05 (head_dim 128, up to 16 query heads per
+// kv head and CTA, 16-bit caches): a persistent grid of at most one CTA per
+// SM, each taking an equal share of the B*Hkv*ceil(g/16)*P units.  Same
+// tensor maps, parameters and results as launch_decode_gqa_tc (no clusters).
+bool gqa_umma_supported(int dtype, int head_dim, int group);
+cudaError_t launch_decode_gqa_umma(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
+                                   const CUtensorMap &vmap, int box_rows, bool split, cudaStream_t stream);
+
 cudaError_t launch_reduce(int dtype, const ReduceParams &p, cudaStream_t stream);
 
 // Shared-prefix partials (split mode, tensor-core shapes): one CTA per

@@ -392,3 +392,15 @@ def test_workload_blocks_start_on_128_byte_boundaries():
         starts = [(blk * w.block_stride + half * w.v_offset + hk * w.bs * w.D) * es
                   for blk in (0, 1, w.NB - 1) for half in (0, 1) for hk in range(w.Hkv)]
         assert all(s % 128 == 0 for s in starts), what
+
+
+def test_kernel_query_rejects_bad_arguments(lib):
+    """paged_attention_decode_kernel validates like the launches it
+    describes (no device is needed for a rejection)."""
+    s = base_shape()
+    assert pa.paged_attention_decode_kernel(base_shape(num_heads=7)) == pa.PA_KERNEL_INVALID
+    assert pa.paged_attention_decode_kernel(s, -1, 0) == pa.PA_KERNEL_INVALID       # window
+    assert pa.paged_attention_decode_kernel(s, 0, 24) == pa.PA_KERNEL_INVALID       # partition size
+    assert pa.paged_attention_decode_kernel(s, 0, -16) == pa.PA_KERNEL_INVALID
+    # a CUDA-core shape never reaches a tensor-core kernel
+    assert pa.paged_attention_decode_kernel(base_shape(dtype=pa.PA_F32)) == pa.PA_KERNEL_SIMT
