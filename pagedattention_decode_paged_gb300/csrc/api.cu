@@ -222,17 +222,65 @@ int choose_cluster(int64_t units, int64_t max_tiles) {
 // repeated call on the same pool (every decode step) skips the driver call.
 struct MapKey {
     const void *pool;
-    int64_t rows;
+    int64_t rows, v_off;
     int32_t head_dim, box_rows, dtype, device;
     bool operator==(const MapKey &o) const {
-        return pool == o.pool && rows == o.rows && head_dim == o.head_dim &&
+        return pool == o.pool && rows == o.rows && v_off == o.v_off && head_dim == o.head_dim &&
                box_rows == o.box_rows && dtype == o.dtype && device == o.device;
     }
 };
 
-// kind 0: 16-bit [rows][head_dim] view, 1: int8 view, 2: 16-bit row-group view
+// A joint K+V view: the K pool's [rows][head_dim] view with a last
+// dimension of extent 2 whose stride is v_off bytes (the V pool's distance
+// from the K pool), so that one box holds a tile's K rows then its V rows,
+// in the order the mma.sync and code kernels keep a ring slot.  16-bit at
+// head_dim 128 also splits a row into its two 128-byte halves (dims {64,
+// rows, 2, 2}); head_dim 64 and one-byte codes keep a row whole.  The boxes
+// fetch the same bytes the separate K and V maps would.
+bool encode_pool_map_kv(CUtensorMap *map, const pa_shape *s, const void *k_pool, int64_t v_off, bool codes,
+                        int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const int64_t rows_per_block = s->block_stride / s->head_dim;
+    const int64_t rows = (s->num_blocks - 1) * rows_per_block + (int64_t)s->num_kv_heads * s->block_size;
+    const int64_t row_bytes = (int64_t)s->head_dim * (codes ? 1 : 2);
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (!codes && s->head_dim == 128) {
+        cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, 2};
+        cuuint64_t strides[3] = {256, 128, (cuuint64_t)v_off};
+        cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 2, 2};
+        const CUtensorMapDataType dt =
+            s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        return fn(map, dt, 4, const_cast<void *>(k_pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t inner = codes ? (cuuint64_t)s->head_dim : 64;
+    cuuint64_t dims[3] = {inner, (cuuint64_t)rows, 2};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)v_off};
+    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)box_rows, 2};
+    const CUtensorMapDataType dt = codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    return fn(map, dt, 3, const_cast<void *>(k_pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Byte distance from the K pool to the V pool when a joint K+V map can
+// serve the tile kernels (V after K, a multiple of 16 bytes, 16-row boxes
+// filling a whole tile), else 0.
+int64_t kv_joint_offset(const pa_shape *s, const void *k_pool, const void *v_pool) {
+    const int64_t d = static_cast<const char *>(v_pool) - static_cast<const char *>(k_pool);
+    if (box_rows_for(s) != 16 || d <= 0 || d % 16 != 0 || d >= ((int64_t)1 << 39)) return 0;
+    return d;
+}
+
+// kind 0: 16-bit [rows][head_dim] view, 1: int8 view, 2: 16-bit row-group
+// view, 3: 16-bit joint K+V view, 4: one-byte-code joint K+V view (v_off: the
+// V pool's byte offset, kinds 3 and 4)
 bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool int8 = false,
-                     int box_rows = 0, int kind = -1) {
+                     int box_rows = 0, int kind = -1, int64_t v_off = 0) {
     if (box_rows == 0) box_rows = box_rows_for(s);
     if (kind < 0) kind = int8 ? 1 : 0;
     constexpr int kSlots = 16;
@@ -244,7 +292,7 @@ bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const int64_t rows = (s->num_blocks - 1) * (s->block_stride / s->head_dim) +
                          (int64_t)s->num_kv_heads * s->block_size;
-    const MapKey key{pool, rows, s->head_dim, box_rows, kind * 16 + s->dtype, dev};
+    const MapKey key{pool, rows, v_off, s->head_dim, box_rows, kind * 16 + s->dtype, dev};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (keys[i] == key) {
@@ -253,6 +301,7 @@ bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool
         }
     const bool ok = kind == 1   ? encode_int8_pool_map(map, s, pool)
                     : kind == 2 ? encode_pool_map_groups(map, s, pool, box_rows)
+                    : kind >= 3 ? encode_pool_map_kv(map, s, pool, v_off, kind == 4, box_rows)
                                 : encode_pool_map(map, s, pool, box_rows);
     if (!ok) return false;
     const int slot = used < kSlots ? used++ : (next++ % kSlots);
@@ -260,6 +309,21 @@ bool cached_pool_map(CUtensorMap *map, const pa_shape *s, const void *pool, bool
     maps[slot] = *map;
     return true;
 }
+
+// Tensor maps of the code kernels' tiles: one joint K+V map when the pools
+// allow it (p->kv_joint set), else one map per pool.
+bool code_maps(const pa_shape *s, const void *k_pool, const void *v_pool, CUtensorMap *kmap, CUtensorMap *vmap,
+               pa::DecodeParams *p) {
+    const int64_t v_off = kv_joint_offset(s, k_pool, v_pool);
+    if (v_off > 0 && cached_pool_map(kmap, s, k_pool, true, 16, 4, v_off)) {
+        *vmap = *kmap;
+        p->kv_joint = 1;
+        return true;
+    }
+    p->kv_joint = 0;
+    return cached_pool_map(kmap, s, k_pool, true) && cached_pool_map(vmap, s, v_pool, true);
+}
+
 
 #ifndef PA_GQA_UMMA
 #define PA_GQA_UMMA 1   // grouped-query decode at head_dim 128 on tcgen05 (0: mma.sync kernel only)
@@ -349,7 +413,10 @@ pa_status launch_decode(const pa_shape *s, pa::DecodeParams &p, bool split, cuda
         // allows, up to a whole tile
         e = pa::launch_decode_gqa_umma(s->dtype, p, kmap, vmap, rows, split, stream);
     } else {
-        if (!cached_pool_map(&kmap, s, p.k_pool) || !cached_pool_map(&vmap, s, p.v_pool)) return PA_ERR_CUDA;
+        const int64_t v_off = kv_joint_offset(s, p.k_pool, p.v_pool);
+        p.kv_joint = v_off > 0 && cached_pool_map(&kmap, s, p.k_pool, false, 16, 3, v_off) ? 1 : 0;
+        if (p.kv_joint) vmap = kmap;
+        else if (!cached_pool_map(&kmap, s, p.k_pool) || !cached_pool_map(&vmap, s, p.v_pool)) return PA_ERR_CUDA;
         e = pa::launch_decode_gqa_tc(s->dtype, p, kmap, vmap, box_rows_for(s), split, stream);
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -912,8 +979,7 @@ pa_status paged_attention_decode_int8(const pa_shape *shape, void *out, const vo
     }
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
-    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
-        return PA_ERR_CUDA;
+    if (boxes && !code_maps(shape, k_pool, v_pool, &kmap, &vmap, &p)) return PA_ERR_CUDA;
     const cudaError_t e = pa::launch_decode_int8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
                                                     boxes ? &vmap : nullptr, box_rows_for(shape), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -982,8 +1048,7 @@ pa_status paged_attention_decode_fp8(const pa_shape *shape, void *out, const voi
     }
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
-    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
-        return PA_ERR_CUDA;
+    if (boxes && !code_maps(shape, k_pool, v_pool, &kmap, &vmap, &p)) return PA_ERR_CUDA;
     const cudaError_t e = pa::launch_decode_fp8_tc(shape->dtype, p, kv_scales, boxes ? &kmap : nullptr,
                                                    boxes ? &vmap : nullptr, box_rows_for(shape), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -1020,8 +1085,7 @@ static pa_status shared_prefix_codes(bool fp8, const pa_shape *shape, void *out,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap kmap{}, vmap{};
     const bool boxes = int8_tc_boxes_ok(shape);
-    if (boxes && (!cached_pool_map(&kmap, shape, k_pool, true) || !cached_pool_map(&vmap, shape, v_pool, true)))
-        return PA_ERR_CUDA;
+    if (boxes && !code_maps(shape, k_pool, v_pool, &kmap, &vmap, &p)) return PA_ERR_CUDA;
     if (pa::launch_prefix_codes_tc(shape->dtype, fp8, p, kv_scales, boxes ? &kmap : nullptr,
                                    boxes ? &vmap : nullptr, box_rows_for(shape), widest, s) != cudaSuccess)
         return PA_ERR_CUDA;

@@ -321,6 +321,12 @@ __device__ __forceinline__ void codes_tc_body(const CUtensorMap &kmap, const CUt
                 if (!good(blk)) continue;
                 const int32_t y = blk * p.rows_per_block + hk * p.bs + (t - j * p.bs);
                 const uint32_t o = (uint32_t)(sb * box_rows * C::ROW);
+                if (p.kv_joint) {
+                    // one box holds the whole tile (16-row boxes): K rows, then
+                    // V rows, as the slot keeps them
+                    tma_3d_g2s(dst_k, &kmap, 0, y, 0, bar);
+                    continue;
+                }
                 tma_2d_g2s(dst_k + o, &kmap, 0, y, bar);
                 tma_2d_g2s(dst_v + o, &vmap, 0, y, bar);
             }

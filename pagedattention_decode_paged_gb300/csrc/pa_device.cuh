@@ -98,6 +98,17 @@ __device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap *map,
         : "memory");
 }
 
+// One box of a 3-D tensor map at coordinates (x, y, z); x as for the 2-D
+// copy.
+__device__ __forceinline__ void tma_3d_g2s(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                           int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // One box of a 4-D tensor map at coordinates (x, y, z, w); x as for the 2-D
 // copy.
 __device__ __forceinline__ void tma_4d_g2s(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,

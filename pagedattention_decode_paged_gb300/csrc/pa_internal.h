@@ -63,6 +63,10 @@ struct DecodeParams {
     char *k_pool_w;
     char *v_pool_w;
     int32_t window;            // > 0: attend to the last `window` tokens only (final mode)
+    // 1: the K tensor map also covers V (a last dimension of extent 2 whose
+    // stride is the V pool's byte offset), so one box fetches K and V of a
+    // tile in the ring slot's [K][V] order; the V map is then unused
+    int32_t kv_joint;
     float scale_log2;          // scale * log2(e)
     // Load-balanced schedule: a warp's partial state for an item it shares
     // with other warps goes to records[(warp * 2 + slot) * rec_floats ...];
@@ -175,9 +179,11 @@ inline cudaError_t resident_ctas(Kern kern, int block, size_t smem, int64_t (&ca
     return cudaSuccess;
 }
 
+// `pdl` false launches without programmatic stream serialization: the kernel
+// then starts only once the previous kernel of the stream has completed.
 template <typename Kern, typename... Args>
-inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
-                                    cudaStream_t stream, Args... args) {
+inline cudaError_t launch_clustered_pdl(bool pdl, Kern kern, int64_t grid, int block, size_t smem, int cluster,
+                                        cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(block, 1, 1);
@@ -185,7 +191,7 @@ inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t s
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
-    if (PA_PDL) {
+    if (PA_PDL && pdl) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
@@ -200,6 +206,12 @@ inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+inline cudaError_t launch_clustered(Kern kern, int64_t grid, int block, size_t smem, int cluster,
+                                    cudaStream_t stream, Args... args) {
+    return launch_clustered_pdl(true, kern, grid, block, smem, cluster, stream, args...);
 }
 
 // Launchers (return the launch's cudaError_t).  `split` selects the partial
