@@ -389,7 +389,12 @@ DecodePlan plan_decode(const pa_shape *s, int32_t window, bool split, int32_t pa
     if (!tc) return pl;
     pl.kernel = PA_KERNEL_MMA_SYNC;
     const int64_t sms = sm_count();
-    if (umma_eligible(s) && sms > 0 && (units >= 3 * sms || (units < sms && 3 * units >= sms))) {
+#ifdef PA_UMMA_ALWAYS   // tuning: every eligible shape on tcgen05
+    const bool by_units = true;
+#else
+    const bool by_units = units >= 3 * sms || (units < sms && 3 * units >= sms);
+#endif
+    if (umma_eligible(s) && sms > 0 && by_units) {
         pl.kernel = PA_KERNEL_TCGEN05;
         pl.cluster = 1;
     }

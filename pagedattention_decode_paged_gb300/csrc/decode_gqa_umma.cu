@@ -32,13 +32,14 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "umma.cuh"
+#include "umma_units.cuh"
 
 namespace pa {
 
+using namespace umma;
+
 namespace {
 
-constexpr int kUD = 128;                  // head_dim
-constexpr int kUTile = 128;               // tokens per tile
 #ifndef PA_UMMA_KSTAGES
 #define PA_UMMA_KSTAGES 3          // K tiles in flight or waiting
 #endif
@@ -50,26 +51,13 @@ constexpr int kUTile = 128;               // tokens per tile
 #endif
 constexpr int kSK = PA_UMMA_KSTAGES;
 constexpr int kSV = PA_UMMA_VSTAGES;
-constexpr int kUThreads = 192;
+constexpr int kUThreads = 224;
 constexpr int kUProducerWarp = 4;
-constexpr int kUMmaWarp = 5;
+constexpr int kUMmaWarp = 5;              // S^T = K Q^T; owns tensor memory
+constexpr int kUMma2Warp = 6;             // O^T += V^T P^T
 constexpr int kUMaxUnits = 64;            // units one CTA takes
 constexpr float kULazy = 8.f;             // rescale O^T when a max grows by more (log2 units)
 constexpr int kRowsRing = 8;              // tiles whose box rows the producer remembers (K ahead of V)
-constexpr int kVNewRing = 4;              // appended V rows kept for the P.V step
-
-// A K (or V) tile in shared memory: [16 groups of 8 tokens][2 halves of 64
-// elements][8 rows][128 bytes], 128-byte swizzled -- the layout one box of
-// the row-group tensor map lands in.  Per half, token groups are kGroup bytes
-// apart; the two halves of a group kHalf bytes apart.
-constexpr uint32_t kHalf = 8 * 128;
-constexpr uint32_t kGroup = 2 * kHalf;
-constexpr uint32_t kTileBytes = (kUTile / 8) * kGroup;
-
-// byte offset of 16-byte chunk c (0..15) of token row r inside a tile
-__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
-    return (uint32_t)((r >> 3) * kGroup + (c >> 3) * kHalf + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 template <int NT>
 struct ULayout {
@@ -85,8 +73,7 @@ struct ULayout {
     static constexpr uint32_t kRed = kP + 2 * kPBuf;              // tile maxima [2][4][16]
     static constexpr uint32_t kLsum = kRed + 2 * 4 * 16 * 4;      // epilogue sums [4][16]
     static constexpr uint32_t kRows = kLsum + 4 * 16 * 4;         // box rows [kRowsRing][32]
-    static constexpr uint32_t kVNew = kRows + kRowsRing * 32 * 4; // appended V rows [kVNewRing][256 B]
-    static constexpr uint32_t kBars = kVNew + kVNewRing * 256;
+    static constexpr uint32_t kBars = kRows + kRowsRing * 32 * 4;
     enum {
         K_FULL = 0,
         K_EMPTY = K_FULL + kSK,
@@ -99,7 +86,8 @@ struct ULayout {
         Q_FREE = P_EMPTY + 2,
         SYNC = Q_FREE + 2,     // the softmax warps' own barrier
         END = SYNC + 1,
-        NBARS = END + 1
+        END2 = END + 1,
+        NBARS = END2 + 1
     };
     static constexpr uint32_t kTmemSlot = kBars + NBARS * 8;
     static constexpr uint32_t kFlags = (kTmemSlot + 4 + 15) & ~15u;   // bad table entry per unit
@@ -114,67 +102,6 @@ struct ULayout {
 };
 
 static_assert(ULayout<1>::kBytes <= 232448 && ULayout<2>::kBytes <= 232448, "shared memory per CTA");
-
-struct UUnit {
-    int b, hk, hg, part, h0, nh;
-    int len;            // valid tokens of the sequence (after the fused append)
-    int t_begin, t_end; // tokens of this unit; tiles start at t_begin
-    int t_win;          // first attended token (sliding window), else t_begin
-    int t_pool;         // tokens below this come from the pool (the fused token does not)
-    int ntiles;
-    int bad_len;        // PA_DEVERR bit for a length outside the table row, else 0
-};
-
-// Valid tokens of unit u's sequence: the fused append's position + 1, else
-// its length.
-template <bool SPLIT>
-__device__ __forceinline__ int unit_len(const DecodeParams &p, int u) {
-    const int b = u % p.B;
-    return (!SPLIT && p.positions != nullptr) ? p.positions[b] + 1 : p.seq_lens[b];
-}
-
-// align: the box height, a multiple of 16 that tiles must start on (a
-// sliding window's first tile starts at or below the window on that grid)
-template <bool SPLIT>
-__device__ __forceinline__ UUnit unit_of(const DecodeParams &p, int u, int len, int align) {
-    UUnit x;
-    const int g = p.H / p.Hkv;
-    const int ngroups = (g + 15) / 16;
-    x.b = u % p.B;
-    u /= p.B;
-    x.hg = u % ngroups;
-    u /= ngroups;
-    x.hk = u % p.Hkv;
-    x.part = u / p.Hkv;
-    x.h0 = x.hk * g + x.hg * 16;
-    x.nh = min(16, g - x.hg * 16);
-    const bool fused = !SPLIT && p.positions != nullptr;
-    x.len = len;
-    x.bad_len = 0;
-    if (x.len < (fused ? 1 : 0) || (int64_t)x.len > (int64_t)p.MB * p.bs) {
-        x.bad_len = fused ? PA_DEVERR_BAD_POS : PA_DEVERR_BAD_LEN;
-        x.t_begin = x.t_end = x.t_win = x.t_pool = x.ntiles = 0;
-        return x;
-    }
-    const int t_win = (!SPLIT && p.window > 0) ? max(0, x.len - p.window) : 0;
-    x.t_begin = SPLIT ? x.part * p.partition_tokens : t_win / align * align;
-    x.t_end = SPLIT ? min(x.len, x.t_begin + p.partition_tokens) : x.len;
-    x.t_win = SPLIT ? x.t_begin : t_win;
-    x.t_pool = fused ? x.t_end - 1 : x.t_end;
-    x.ntiles = x.t_end > x.t_begin ? (x.t_end - x.t_begin + kUTile - 1) / kUTile : 0;
-    return x;
-}
-
-// byte offset of 16-byte chunk c (0..7) of row r inside 128-byte swizzled
-// rows whose 8-row groups are 1024-byte aligned
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-// Position in the sequence of tiles of one CTA: tile i of its k-th unit, the
-// g-th tile overall, kact units with tiles before this one.
-struct UIter {
-    int k, i, g, kact;
-    UUnit x;
-};
 
 }  // namespace
 
@@ -212,7 +139,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             // the softmax warps arrive once per warp (lane 0, after __syncwarp)
             if (i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL || i == L::P_FULL + 1 || i == L::SYNC)
                 count = 4;
-            if (i == L::P_EMPTY || i == L::P_EMPTY + 1) count = 2;   // the MMA commit and a plain arrival
+            // the MMA commit and a plain arrival (which publishes the issuing
+            // warp's unit flags)
+            if (i == L::P_EMPTY || i == L::P_EMPTY + 1 || i == L::S_FULL || i == L::S_FULL + 1) count = 2;
             mbar_init(bar(i), count);
         }
         for (int i = 0; i < kUMaxUnits; ++i) flags[i] = 0;
@@ -385,21 +314,15 @@ __global__ void __launch_bounds__(kUThreads, 1)
         for (int gg = max(0, vq.g - kSV); gg < vq.g; ++gg) mbar_wait(bar(L::V_FULL + gg % kSV), (gg / kSV) & 1);
     } else if (warp == kUMmaWarp) {
         // ------------------------------------------------------------------
-        // MMA issue (one thread) and tile preparation (the whole warp): O^T +=
-        // V^T P^T as soon as a V tile and the softmax's P^T are ready (first:
-        // it frees a V stage and lets the softmax move on), S^T = K Q^T as
-        // soon as a K tile and an S buffer are ready; the first product runs
-        // at most 3 tiles ahead of the second
+        // S^T = K Q^T, tile by tile, as soon as a K tile and an S buffer are
+        // ready (one thread issues, the warp prepares the tile).  A
+        // tcgen05.mma costs its issuing thread far longer than the tensor
+        // core takes for these thin shapes, so the two products of a tile
+        // are issued by two warps.
         // ------------------------------------------------------------------
-        UIter m1, m2;
-        if (nunits > 0) {
-            it_init(m1);
-            it_init(m2);
-        } else {
-            m1.k = m2.k = 0;
-            m1.g = m2.g = 0;
-        }
-        unsigned char *vnew = smem + L::kVNew;
+        UIter m1;
+        if (nunits > 0) it_init(m1);
+        else m1.k = m1.g = 0;
         // Q rows, the fused new row and its pool block of the next unit with
         // tiles, fetched one unit ahead: chunk c = lane + 32 i is 16-byte
         // piece c % 16 of head c / 16 (heads 0-7 in qn, 8-15 in qn2)
@@ -430,152 +353,151 @@ __global__ void __launch_bounds__(kUThreads, 1)
         };
         if (nunits > 0) fetch_unit(m1.k);
         uint4 k_new_row = make_uint4(0, 0, 0, 0);
-        uint32_t idle = 0;
         bool abort = false;
-        while (m2.k < nunits) {
-            bool progress = false;
-            if (m2.g < m1.g) {
-                const int g = m2.g;
-                bool ready = __all_sync(0xffffffffu, mbar_test(bar(L::V_FULL + g % kSV), (g / kSV) & 1));
-                if (ready) ready = __all_sync(0xffffffffu, mbar_test(bar(L::P_FULL + (g & 1)), (g >> 1) & 1));
-                if (ready) {
-                    const UUnit &x = m2.x;
-                    const int t0 = x.t_begin + m2.i * kUTile;
-                    const int nvalid = min(kUTile, x.t_end - t0);
-                    const bool last = m2.i == x.ntiles - 1;
-                    unsigned char *vs = smem + L::kVRing + (g % kSV) * kTileBytes;
-                    // rows past the length hold padding, poison or another unit's
-                    // rows: their weight is 0 and V must be finite so that 0 * V
-                    // stays 0.  Swizzling permutes chunks inside a row only, so a
-                    // row is whole 128-byte lines, one per half.
-                    const int zend = kUTile;
-                    if (nvalid < zend) {
-                        for (uint32_t o = (nvalid >> 3) * kGroup + lane * 16; o < kTileBytes; o += 32 * 16) {
-                            const int r = (int)((o / kGroup) * 8 + (o % kHalf) / 128);
-                            if (r >= nvalid) *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    if (fused && last && lane < 16)
-                        *reinterpret_cast<uint4 *>(vs + tile_chunk(nvalid - 1, lane)) =
-                            *reinterpret_cast<const uint4 *>(vnew + (m2.kact % kVNewRing) * 256 + lane * 16);
-                    if (nvalid < zend || (fused && last)) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    tc05_fence_after_sync();
-                    if (lane == 0) {
-                        const uint32_t vb = sbase + L::kVRing + (g % kSV) * kTileBytes;
-                        const uint32_t pb = sbase + L::kP + (g & 1) * L::kPBuf;
-                        const uint32_t d = tmem + L::kColO + (m2.kact & 1) * L::N2;
-#pragma unroll
-                        for (int kk = 0; kk < kUTile / 16; ++kk) {
-                            // V^T: 64-dim atoms kHalf apart, 8-token groups kGroup apart
-                            const uint64_t a = sw128_desc(vb + kk * 2 * kGroup, kHalf, kGroup);
-                            const uint64_t bd = sw128_desc(pb + (kk >> 2) * L::kPSlab + (kk & 3) * 32, 0, 1024);
-                            umma_f16(d, a, bd, kIdesc2, !(m2.i == 0 && kk == 0));
-                        }
-                        umma_commit(bar(L::P_EMPTY + (g & 1)));
-                        umma_commit(bar(L::V_EMPTY + g % kSV));
-                        // the plain arrival carries this warp's view of the unit
-                        // flags to the softmax warps that wait on the same barrier
-                        mbar_arrive(bar(L::P_EMPTY + (g & 1)));
-                    }
-                    __syncwarp();
-                    it_next(m2);
-                    progress = true;
-                }
-            }
-            if (m1.k < nunits && m1.g - m2.g < 4) {
-                const int g = m1.g;
-                const int qb = m1.kact & 1;
-                bool ready = __all_sync(0xffffffffu, mbar_test(bar(L::K_FULL + g % kSK), (g / kSK) & 1));
-                if (ready && g >= 2)
-                    ready = __all_sync(0xffffffffu, mbar_test(bar(L::S_FREE + (g & 1)), ((g >> 1) - 1) & 1));
-                if (ready && m1.i == 0 && m1.kact >= 2)
-                    ready = __all_sync(0xffffffffu, mbar_test(bar(L::Q_FREE + qb), ((m1.kact >> 1) - 1) & 1));
-                if (ready) {
-                    const UUnit &x = m1.x;
-                    if (m1.i == 0) {
-                        // Q^T of this unit: rows = heads (zero past nh)
-                        unsigned char *qs = smem + L::kQ + qb * L::kQBuf;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int c = lane + 32 * i;
-                            const int h = c >> 4, piece = c & 15;
-                            *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(h, piece & 7)) = qn[i];
-                            *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(8 + h, piece & 7)) = qn2[i];
-                        }
-                        if (fused) {
-                            k_new_row = kn_new;
-                            // the V row waits in shared memory for this unit's last P.V step
-                            if (lane < 16)
-                                *reinterpret_cast<uint4 *>(vnew + (m1.kact % kVNewRing) * 256 + lane * 16) = vn_new;
-                            if (x.hg == 0) {
-                                // the step's new row goes to its pool slot (one unit per
-                                // (sequence, kv head) writes it); the arrival on P_EMPTY
-                                // after this unit's P.V steps publishes a bad target's flag
-                                const int pos = x.t_end - 1;
-                                if (!good(nb_new)) {
-                                    if (lane == 0) {
-                                        flags[m1.k] = 1;
-                                        report(p.err_word, PA_DEVERR_BAD_BLOCK);
-                                    }
-                                } else if (lane < 16) {
-                                    const int64_t dst = (int64_t)nb_new * p.block_stride_bytes +
-                                                        ((int64_t)x.hk * p.bs + (pos - block_of(pos) * p.bs)) * (kUD * 2) +
-                                                        lane * 16;
-                                    *reinterpret_cast<uint4 *>(p.k_pool_w + dst) = kn_new;
-                                    *reinterpret_cast<uint4 *>(p.v_pool_w + dst) = vn_new;
-                                }
-                            }
-                        }
-                        fetch_unit(m1.k + 1);
-                    }
-                    const int t0 = x.t_begin + m1.i * kUTile;
-                    const int nvalid = min(kUTile, x.t_end - t0);
-                    const bool last = m1.i == x.ntiles - 1;
-                    if (fused && last && lane < 16) {
-                        // the appended token: its K row comes from k_new
-                        unsigned char *ks = smem + L::kKRing + (g % kSK) * kTileBytes;
-                        *reinterpret_cast<uint4 *>(ks + tile_chunk(nvalid - 1, lane)) = k_new_row;
-                    }
-                    if (m1.i == 0 || (fused && last)) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    tc05_fence_after_sync();
-                    if (lane == 0) {
-                        const uint32_t kb = sbase + L::kKRing + (g % kSK) * kTileBytes;
-                        const uint32_t qbase = sbase + L::kQ + qb * L::kQBuf;
-                        const uint32_t d = tmem + (g & 1) * 16;
-#pragma unroll
-                        for (int kk = 0; kk < kUD / 16; ++kk) {
-                            // K: K step kk in half kk / 4, 8-token groups kGroup apart
-                            const uint64_t a = sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 0, kGroup);
-                            const uint64_t bd = sw128_desc(qbase + (kk >> 2) * 2048 + (kk & 3) * 32, 0, 1024);
-                            umma_f16(d, a, bd, kIdesc1, kk > 0);
-                        }
-                        umma_commit(bar(L::S_FULL + (g & 1)));
-                        umma_commit(bar(L::K_EMPTY + g % kSK));
-                        if (last) umma_commit(bar(L::Q_FREE + qb));
-                    }
-                    __syncwarp();
-                    it_next(m1);
-                    progress = true;
-                }
-            }
-            if (progress) {
-                idle = 0;
-            } else if (++idle > kWaitLimit) {
+        for (; m1.k < nunits; it_next(m1)) {
+            const int g = m1.g;
+            const int qb = m1.kact & 1;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::K_FULL + g % kSK), (g / kSK) & 1));
+            if (ok && g >= 2) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::S_FREE + (g & 1)), ((g >> 1) - 1) & 1));
+            if (ok && m1.i == 0 && m1.kact >= 2)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(L::Q_FREE + qb), ((m1.kact >> 1) - 1) & 1));
+            if (!ok) {
                 abort = true;
                 break;
             }
+            const UUnit &x = m1.x;
+            if (m1.i == 0) {
+                // Q^T of this unit: rows = heads (zero past nh)
+                unsigned char *qs = smem + L::kQ + qb * L::kQBuf;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = lane + 32 * i;
+                    const int h = c >> 4, piece = c & 15;
+                    *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(h, piece & 7)) = qn[i];
+                    *reinterpret_cast<uint4 *>(qs + (piece >> 3) * 2048 + sw128(8 + h, piece & 7)) = qn2[i];
+                }
+                if (fused) {
+                    k_new_row = kn_new;
+                    if (x.hg == 0) {
+                        // the step's new row goes to its pool slot (one unit per
+                        // (sequence, kv head) writes it); the plain arrival on
+                        // S_FULL publishes a bad target's flag
+                        const int pos = x.t_end - 1;
+                        if (!good(nb_new)) {
+                            if (lane == 0) {
+                                flags[m1.k] = 1;
+                                report(p.err_word, PA_DEVERR_BAD_BLOCK);
+                            }
+                        } else if (lane < 16) {
+                            const int64_t dst = (int64_t)nb_new * p.block_stride_bytes +
+                                                ((int64_t)x.hk * p.bs + (pos - block_of(pos) * p.bs)) * (kUD * 2) +
+                                                lane * 16;
+                            *reinterpret_cast<uint4 *>(p.k_pool_w + dst) = kn_new;
+                            *reinterpret_cast<uint4 *>(p.v_pool_w + dst) = vn_new;
+                        }
+                    }
+                }
+                fetch_unit(m1.k + 1);
+            }
+            const int t0 = x.t_begin + m1.i * kUTile;
+            const int nvalid = min(kUTile, x.t_end - t0);
+            const bool last = m1.i == x.ntiles - 1;
+            if (fused && last && lane < 16) {
+                // the appended token: its K row comes from k_new
+                unsigned char *ks = smem + L::kKRing + (g % kSK) * kTileBytes;
+                *reinterpret_cast<uint4 *>(ks + tile_chunk(nvalid - 1, lane)) = k_new_row;
+            }
+            if (m1.i == 0 || (fused && last)) {
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc05_fence_after_sync();
+            if (lane == 0) {
+                const uint32_t kb = sbase + L::kKRing + (g % kSK) * kTileBytes;
+                const uint32_t qbase = sbase + L::kQ + qb * L::kQBuf;
+                const uint32_t d = tmem + (g & 1) * 16;
+#pragma unroll
+                for (int kk = 0; kk < kUD / 16; ++kk) {
+                    // K: K step kk in half kk / 4, 8-token groups kGroup apart
+                    const uint64_t a = sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 0, kGroup);
+                    const uint64_t bd = sw128_desc(qbase + (kk >> 2) * 2048 + (kk & 3) * 32, 0, 1024);
+                    umma_f16(d, a, bd, kIdesc1, kk > 0);
+                }
+                umma_commit(bar(L::S_FULL + (g & 1)));
+                umma_commit(bar(L::K_EMPTY + g % kSK));
+                if (last) umma_commit(bar(L::Q_FREE + qb));
+                mbar_arrive(bar(L::S_FULL + (g & 1)));
+            }
+            __syncwarp();
         }
         if (abort && lane == 0) report(p.err_word, PA_DEVERR_TIMEOUT);
         // every MMA this warp issued has completed before tensor memory is freed
         if (lane == 0) umma_commit(bar(L::END));
         __syncwarp();
         mbar_wait(bar(L::END), 0);
+    } else if (warp == kUMma2Warp) {
+        // ------------------------------------------------------------------
+        // O^T += V^T P^T, tile by tile, as soon as a V tile and the softmax's
+        // P^T are ready (one thread issues, the warp prepares the tile)
+        // ------------------------------------------------------------------
+        UIter m2;
+        if (nunits > 0) it_init(m2);
+        else m2.k = m2.g = 0;
+        uint4 vn_row = make_uint4(0, 0, 0, 0);   // the fused new V row of the current unit
+        bool abort = false;
+        for (; m2.k < nunits; it_next(m2)) {
+            const int g = m2.g;
+            const UUnit &x = m2.x;
+            if (fused && m2.i == 0 && lane < 16)   // in flight while the unit's tiles run
+                vn_row = *reinterpret_cast<const uint4 *>(p.v_new + ((int64_t)x.b * p.Hkv + x.hk) * (kUD * 2) +
+                                                          lane * 16);
+            bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::V_FULL + g % kSV), (g / kSV) & 1));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::P_FULL + (g & 1)), (g >> 1) & 1));
+            if (!ok) {
+                abort = true;
+                break;
+            }
+            const int t0 = x.t_begin + m2.i * kUTile;
+            const int nvalid = min(kUTile, x.t_end - t0);
+            const bool last = m2.i == x.ntiles - 1;
+            unsigned char *vs = smem + L::kVRing + (g % kSV) * kTileBytes;
+            // rows past the length hold padding, poison or another unit's
+            // rows: their weight is 0 and V must be finite so that 0 * V
+            // stays 0.  Swizzling permutes chunks inside a row only, so a
+            // row is whole 128-byte lines, one per half.
+            if (nvalid < kUTile) {
+                for (uint32_t o = (nvalid >> 3) * kGroup + lane * 16; o < kTileBytes; o += 32 * 16) {
+                    const int r = (int)((o / kGroup) * 8 + (o % kHalf) / 128);
+                    if (r >= nvalid) *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            if (fused && last && lane < 16) *reinterpret_cast<uint4 *>(vs + tile_chunk(nvalid - 1, lane)) = vn_row;
+            if (nvalid < kUTile || (fused && last)) {
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc05_fence_after_sync();
+            if (lane == 0) {
+                const uint32_t vb = sbase + L::kVRing + (g % kSV) * kTileBytes;
+                const uint32_t pb = sbase + L::kP + (g & 1) * L::kPBuf;
+                const uint32_t d = tmem + L::kColO + (m2.kact & 1) * L::N2;
+#pragma unroll
+                for (int kk = 0; kk < kUTile / 16; ++kk) {
+                    // V^T: 64-dim atoms kHalf apart, 8-token groups kGroup apart
+                    const uint64_t a = sw128_desc(vb + kk * 2 * kGroup, kHalf, kGroup);
+                    const uint64_t bd = sw128_desc(pb + (kk >> 2) * L::kPSlab + (kk & 3) * 32, 0, 1024);
+                    umma_f16(d, a, bd, kIdesc2, !(m2.i == 0 && kk == 0));
+                }
+                umma_commit(bar(L::P_EMPTY + (g & 1)));
+                umma_commit(bar(L::V_EMPTY + g % kSV));
+                mbar_arrive(bar(L::P_EMPTY + (g & 1)));
+            }
+            __syncwarp();
+        }
+        if (abort && lane == 0) report(p.err_word, PA_DEVERR_TIMEOUT);
+        if (lane == 0) umma_commit(bar(L::END2));
+        __syncwarp();
+        mbar_wait(bar(L::END2), 0);
     } else {
         // ------------------------------------------------------------------
         // softmax (warps 0-3): thread r owns token row r of S^T and head_dim
@@ -629,25 +551,40 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!sync128()) return false;
             const bool bad = flags[pk] != 0;
             const int64_t pbh0 = (int64_t)px.b * p.H + px.h0;
+            // The rows go out through shared memory (the previous unit's last
+            // P^T buffer, free until two tiles on), as 16-byte stores: scattered
+            // 2- or 4-byte stores stall for microseconds behind the copy stream.
+            unsigned char *stage = smem + L::kP + (pgl & 1) * L::kPBuf;
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                if (h >= px.nh) break;
                 const float lt = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
                 if (!SPLIT) {
-                    out[(pbh0 + h) * kUD + r] = Elem<T>::from_float(bad ? 0.f : o[h] / lt);
+                    reinterpret_cast<T *>(stage)[h * kUD + r] = Elem<T>::from_float(bad ? 0.f : o[h] / lt);
                 } else {
                     // the workspace keeps the state relative to the true maximum
                     const float f = merge_weight(pmu[h], pmt[h]);
-                    const int64_t ws = (pbh0 + h) * p.num_partitions + px.part;
-                    p.ws_acc[ws * kUD + r] = o[h] * f;
-                    if (r == 0) {
+                    reinterpret_cast<float *>(stage)[h * kUD + r] = o[h] * f;
+                    if (r == 0 && h < px.nh) {
+                        const int64_t ws = (pbh0 + h) * p.num_partitions + px.part;
                         p.ws_m[ws] = pmt[h];
                         p.ws_l[ws] = bad ? -1.f : lt * f;
                     }
                 }
             }
             // the sums of this unit are read before the next unit's are written
-            return sync128();
+            if (!sync128()) return false;
+            const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+            if (!SPLIT) {
+                const int nchunks = px.nh * kUD * 2 / 16;   // the unit's heads are contiguous in out
+                uint4 *dst = reinterpret_cast<uint4 *>(out + pbh0 * kUD);
+                for (int c = r; c < nchunks; c += 128) dst[c] = src[c];
+            } else {
+                for (int c = r; c < px.nh * 32; c += 128) {   // 32 chunks per head's fp32 row
+                    const int64_t ws = (pbh0 + (c >> 5)) * p.num_partitions + px.part;
+                    reinterpret_cast<uint4 *>(p.ws_acc + ws * kUD)[c & 31] = src[c];
+                }
+            }
+            return true;
         };
         for (int k = 0; k < nunits && !abort; ++k) {
             const UUnit x = unit_at(k);
