@@ -290,15 +290,17 @@ def describe(w, index) -> dict:
 def step_options(**over) -> SimpleNamespace:
     """The step-shaping flags of the command line, with their defaults."""
     o = dict(unfused=False, window=0, balanced=False, prefill=False, split_tokens=None,
-             shared_prefix=None, int8=False, fp8=False, graph=0, long_seq=0, pool_offset=0)
+             shared_prefix=None, int8=False, fp8=False, graph=0, long_seq=0, pool_offset=0, batch=None)
     o.update(over)
     return SimpleNamespace(**o)
 
 
 def make_bench_workload(index, o, dev, rank=0, block_size=None, batch=None):
-    """Workload `index` on `dev` as the options shape it: a long request
-    beside the batch, an int8 or fp8 cache (codes drawn on the device), or a
-    pool moved `pool_offset` bytes off its 512-byte aligned allocation."""
+    """Workload `index` on `dev` as the options shape it: another batch size,
+    a long request beside the batch, an int8 or fp8 cache (codes drawn on the
+    device), or a pool moved `pool_offset` bytes off its 512-byte aligned
+    allocation."""
+    batch = o.batch if batch is None else batch
     w = workloads.make_workload(index, block_size=block_size, device=dev,
                                 seed=replica_seed(index, rank), batch=batch)
     if o.long_seq:
@@ -553,10 +555,13 @@ DEFAULT_BLOCK_SIZE = {1: 16, 2: 16, 3: 16, 4: 16, 5: 32}
 
 def workload_key(index, o, block_size=None) -> str:
     """The key profile summaries are filed under: workload, block size when
-    it is not the workload's default, cache variant, skew and pool offset."""
+    it is not the workload's default, batch when given, cache variant, skew
+    and pool offset."""
     key = f"w{index}"
     if block_size and block_size != DEFAULT_BLOCK_SIZE.get(index):
         key += f"_bs{block_size}"
+    if o.batch:
+        key += f"_b{o.batch}"
     if o.long_seq:
         key += f"_long{o.long_seq}"
     key += "_fp8" if o.fp8 else "_int8" if o.int8 else ""
@@ -565,13 +570,15 @@ def workload_key(index, o, block_size=None) -> str:
 
 # Configurations measured beside the headline step in the same run (one
 # entry each): the five workloads of the report, the block-size sweep of the
-# long tail and of the GQA layer, the quantised caches, and a pool that is
-# 16- but not 128-byte aligned.
+# long tail and of the GQA layer, the GQA layer at batch 16 and 64 (where the
+# tcgen05 kernel runs), the quantised caches, and a pool that is 16- but not
+# 128-byte aligned.
 PER_WORKLOAD = [
     ("w1", 1, None, {}),
     ("w2", 2, None, {}),
     ("w3_bs8", 3, 8, {}), ("w3_bs16", 3, 16, {}), ("w3_bs32", 3, 32, {}), ("w3_bs64", 3, 64, {}),
     ("w4_bs16", 4, 16, {}), ("w4_bs256", 4, 256, {}),
+    ("w4_b16", 4, 16, {"batch": 16}), ("w4_b64", 4, 16, {"batch": 64}),
     ("w5", 5, None, {}),
     ("w2_int8", 2, None, {"int8": True}), ("w4_int8", 4, 16, {"int8": True}),
     ("w5_int8", 5, None, {"int8": True}),
@@ -662,7 +669,8 @@ def run_gpu(args) -> None:
     o = step_options(unfused=args.unfused, window=args.window, balanced=args.balanced,
                      prefill=args.prefill, split_tokens=args.split_tokens,
                      shared_prefix=args.shared_prefix, int8=args.int8, fp8=args.fp8,
-                     graph=args.graph, long_seq=args.long_seq, pool_offset=args.pool_offset)
+                     graph=args.graph, long_seq=args.long_seq, pool_offset=args.pool_offset,
+                     batch=args.batch)
 
     # each rank holds its own replica of the workload (weak scaling)
     w = make_bench_workload(args.workload, o, dev, rank=rank, block_size=args.block_size,

@@ -131,12 +131,14 @@ def test_workload_keys_and_per_workload_table():
     """Profile keys drop the default block size and name the cache variant;
     the per_workload table has unique labels, covers workloads 1-5, the
     long tail at block sizes 8/16/32/64 and the GQA layer at 16/256, and each
-    label's key is distinct (no configuration measured twice)."""
+    label's key is distinct (no configuration measured twice); the GQA layer
+    also runs at batch 16 and 64."""
     o = bench.step_options()
     assert bench.workload_key(4, o, 16) == bench.workload_key(4, o) == "w4"
     assert bench.workload_key(4, o, 256) == "w4_bs256"
     assert bench.workload_key(3, bench.step_options(int8=True), 8) == "w3_bs8_int8"
     assert bench.workload_key(2, bench.step_options(pool_offset=16)) == "w2_pool_off16"
+    assert bench.workload_key(4, bench.step_options(batch=64), 16) == "w4_b64"
     labels = [e[0] for e in bench.PER_WORKLOAD]
     assert len(labels) == len(set(labels))
     keys = [bench.workload_key(i, bench.step_options(**over), bs) for _, i, bs, over in bench.PER_WORKLOAD]
@@ -144,6 +146,7 @@ def test_workload_keys_and_per_workload_table():
     assert {i for _, i, _, _ in bench.PER_WORKLOAD} == {1, 2, 3, 4, 5}
     assert {bs for _, i, bs, _ in bench.PER_WORKLOAD if i == 3} == {8, 16, 32, 64}
     assert {bs for _, i, bs, over in bench.PER_WORKLOAD if i == 4 and not over} == {16, 256}
+    assert {over.get("batch") for _, i, _, over in bench.PER_WORKLOAD if i == 4} >= {None, 16, 64}
 
 
 def test_per_workload_notes():
