@@ -18,10 +18,12 @@
 // second MMA are the heads twice), which keeps the weights good to about 16
 // bits even in bf16.
 //
-// Roles (192 threads): warps 0-3 run the softmax (thread i owns token row i of
+// Roles (224 threads): warps 0-3 run the softmax (thread i owns token row i of
 // S^T and head_dim row i of O^T, the tensor-memory lane of its warp quarter),
-// warp 4 issues the TMA copies of a 3-stage ring, warp 5 owns the tensor
-// memory and issues the MMAs from one thread.  The grid is persistent: each
+// warp 4 issues the TMA copies of the K and V rings, warp 5 owns the tensor
+// memory and issues S^T = K Q^T, warp 6 issues O^T += V^T P^T (one thread
+// each: a tcgen05.mma costs its issuing thread far longer than these thin
+// products take on the tensor core).  The grid is persistent: each
 // CTA takes an equal share of the units, one after another, so the copy
 // stream never drains between units.  O^T is rescaled in tensor memory only
 // when a head's running maximum grows by more than 2^8 (the weights of the
