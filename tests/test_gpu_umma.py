@@ -4,9 +4,9 @@ several units per CTA (the persistent grid gives each CTA an equal share),
 zero-length and bad-table units among a CTA's units, block sizes whose
 tiles are fetched as 128-row boxes, sliding windows and split-KV partitions
 on and off that box grid, the fused append on every tile position, 16 query
-heads per kv head (two head tiles), and the split-KV workspace against the
-oracle's partial sums.  Pools are poisoned in every slot the step must not
-read.
+heads per kv head (two head tiles), the split-KV workspace against the
+oracle's partial sums, and the full-size batches the benchmark times.  Pools
+are poisoned in every slot the step must not read.
 """
 import numpy as np
 import pytest
@@ -206,3 +206,13 @@ def test_large_scores_rescale_in_tensor_memory():
     workloads.poison_pool(w)
     w.q = (w.q.float() * 3.0).to(F16)
     hz.run_step_and_check(w)
+
+
+@pytest.mark.parametrize("batch", [16, 64])
+def test_workload4_batches_the_bench_times_on_tcgen05(batch):
+    """The GQA layer at batch 16 and 64 (full length, block size 16), as the
+    benchmark's per-workload entries run it: the tcgen05 kernel, fused append
+    + decode in one launch, every output against the oracle."""
+    w = workloads.make_workload(4, block_size=16, batch=batch, poison=True)
+    _assert_tcgen05(w)
+    hz.run_fused_step_and_check(w)
