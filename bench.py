@@ -570,15 +570,16 @@ def workload_key(index, o, block_size=None) -> str:
 
 # Configurations measured beside the headline step in the same run (one
 # entry each): the five workloads of the report, the block-size sweep of the
-# long tail and of the GQA layer, the GQA layer at batch 16 and 64 (where the
-# tcgen05 kernel runs), the quantised caches, and a pool that is 16- but not
-# 128-byte aligned.
+# long tail and of the GQA layer, the GQA layer at batch 4, 16 and 64 (where
+# the tcgen05 kernel runs: clusters of CTAs per unit, one CTA per unit, several
+# units per CTA), the quantised caches, and a pool that is 16- but not 128-byte
+# aligned.
 PER_WORKLOAD = [
     ("w1", 1, None, {}),
     ("w2", 2, None, {}),
     ("w3_bs8", 3, 8, {}), ("w3_bs16", 3, 16, {}), ("w3_bs32", 3, 32, {}), ("w3_bs64", 3, 64, {}),
     ("w4_bs16", 4, 16, {}), ("w4_bs256", 4, 256, {}),
-    ("w4_b16", 4, 16, {"batch": 16}), ("w4_b64", 4, 16, {"batch": 64}),
+    ("w4_b4", 4, 16, {"batch": 4}), ("w4_b16", 4, 16, {"batch": 16}), ("w4_b64", 4, 16, {"batch": 64}),
     ("w5", 5, None, {}),
     ("w2_int8", 2, None, {"int8": True}), ("w4_int8", 4, 16, {"int8": True}),
     ("w5_int8", 5, None, {"int8": True}),

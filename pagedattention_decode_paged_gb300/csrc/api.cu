@@ -389,6 +389,20 @@ DecodePlan plan_decode(const pa_shape *s, int32_t window, bool split, int32_t pa
     if (!tc) return pl;
     pl.kernel = PA_KERNEL_MMA_SYNC;
     const int64_t sms = sm_count();
+    if (umma_eligible(s) && sms > 0 && !split && units < sms) {
+        // few units: each spread over a cluster of 8, 4 or 2 tcgen05 CTAs
+        // when every cluster can be resident at once and each CTA gets at
+        // least 4 tiles of 128 tokens of the longest possible sequence
+        int64_t max_len = (int64_t)s->max_blocks_per_seq * s->block_size;
+        if (window > 0 && window < max_len) max_len = window;
+        const int64_t utiles = (max_len + 127) / 128;
+        for (int c = 8; c >= 2; c /= 2)
+            if (utiles >= 4 * c && units <= pa::umma_max_active_clusters(s->dtype, g, c)) {
+                pl.kernel = PA_KERNEL_TCGEN05;
+                pl.cluster = c;
+                return pl;
+            }
+    }
 #ifdef PA_UMMA_ALWAYS   // tuning: every eligible shape on tcgen05
     const bool by_units = true;
 #else

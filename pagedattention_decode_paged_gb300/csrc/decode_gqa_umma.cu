@@ -105,6 +105,12 @@ struct ULayout {
 
 static_assert(ULayout<1>::kBytes <= 232448 && ULayout<2>::kBytes <= 232448, "shared memory per CTA");
 
+// Store v at a shared-memory address of another CTA of the cluster (from
+// dsmem_addr).
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 }  // namespace
 
 template <typename T, int NT, bool SPLIT>
@@ -129,10 +135,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // this CTA's units: a contiguous range, the ranges of all CTAs as equal as
-    // the grid allows (at most kUMaxUnits each)
+    // the grid allows (at most kUMaxUnits each).  With fewer units than SMs a
+    // unit may instead be spread over the CTAs of a thread-block cluster (final
+    // mode): CTA crank takes an equal share of its tiles, and the cluster's
+    // first CTA merges the CTAs' softmax states through distributed shared
+    // memory at the end.
     const int tile_align = box_rows < 16 ? 16 : box_rows;
-    const int u_first = (int)(((int64_t)blockIdx.x * units) / gridDim.x);
-    const int nunits = (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x) - u_first;
+    const int csize = SPLIT ? 1 : (int)cluster_size();
+    const int crank = SPLIT ? 0 : (int)cluster_rank();
+    const int u_first = csize > 1 ? (int)(blockIdx.x / csize) : (int)(((int64_t)blockIdx.x * units) / gridDim.x);
+    const int nunits = csize > 1 ? 1 : (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x) - u_first;
     int *lens = reinterpret_cast<int *>(smem + L::kLens);
 
     if (threadIdx.x == 0) {
@@ -186,9 +198,22 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int n = x.t_pool > x.t_begin ? (x.t_pool - 1) / p.bs + 1 - j0 : 0;
         return n <= (spec ? min(tbl_slot, p.MB - j0) : tbl_slot);
     };
+    auto unit_at = [&](int k) {
+        UUnit x = unit_of<SPLIT>(p, u_first + k, lens[k], tile_align);
+        if (csize > 1 && x.ntiles > 0) {
+            // this CTA's share of the unit's tiles; rows before the window
+            // start stay masked, the appended row belongs to the last share
+            const int t0 = x.t_begin, a = crank * x.ntiles / csize, e = (crank + 1) * x.ntiles / csize;
+            x.t_begin = t0 + a * kUTile;
+            x.t_end = min(x.t_end, t0 + e * kUTile);
+            x.t_pool = min(x.t_pool, x.t_end);
+            x.ntiles = e - a;
+        }
+        return x;
+    };
     if (!spec) {
         for (int k = warp; k < nunits; k += kUThreads / 32) {
-            const UUnit x = unit_of<SPLIT>(p, u_first + k, lens[k], tile_align);
+            const UUnit x = unit_at(k);
             int j0;
             if (!staged_entries(k, x, j0)) continue;
             const int n = x.t_pool > x.t_begin ? (x.t_pool - 1) / p.bs + 1 - j0 : 0;
@@ -202,7 +227,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const bool fused = !SPLIT && p.positions != nullptr;
     auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
     auto block_of = [&](int t) { return p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs; };
-    auto unit_at = [&](int k) { return unit_of<SPLIT>(p, u_first + k, lens[k], tile_align); };
     // tile iteration shared by the producer and the MMA warp
     auto it_skip = [&](UIter &it) {
         while (it.k < nunits && it.i >= it.x.ntiles) {
@@ -380,7 +404,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 }
                 if (fused) {
                     k_new_row = kn_new;
-                    if (x.hg == 0) {
+                    if (x.hg == 0 && x.t_pool < x.t_end) {
                         // the step's new row goes to its pool slot (one unit per
                         // (sequence, kv head) writes it); the plain arrival on
                         // S_FULL publishes a bad target's flag
@@ -404,7 +428,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const int t0 = x.t_begin + m1.i * kUTile;
             const int nvalid = min(kUTile, x.t_end - t0);
             const bool last = m1.i == x.ntiles - 1;
-            if (fused && last && lane < 16) {
+            if (fused && last && x.t_pool < x.t_end && lane < 16) {
                 // the appended token: its K row comes from k_new
                 unsigned char *ks = smem + L::kKRing + (g % kSK) * kTileBytes;
                 *reinterpret_cast<uint4 *>(ks + tile_chunk(nvalid - 1, lane)) = k_new_row;
@@ -473,7 +497,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     if (r >= nvalid) *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0, 0, 0, 0);
                 }
             }
-            if (fused && last && lane < 16) *reinterpret_cast<uint4 *>(vs + tile_chunk(nvalid - 1, lane)) = vn_row;
+            if (fused && last && x.t_pool < x.t_end && lane < 16)
+                *reinterpret_cast<uint4 *>(vs + tile_chunk(nvalid - 1, lane)) = vn_row;
             if (nvalid < kUTile || (fused && last)) {
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -553,6 +578,23 @@ __global__ void __launch_bounds__(kUThreads, 1)
             if (!sync128()) return false;
             const bool bad = flags[pk] != 0;
             const int64_t pbh0 = (int64_t)px.b * p.H + px.h0;
+            if (csize > 1) {
+                // this CTA's share of the unit: O^T relative to m_used, the
+                // sum of the weights and the flag, for the cluster's merge (the
+                // K ring is idle: the last S^T product has completed)
+                float *part = reinterpret_cast<float *>(smem + L::kKRing);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) part[h * kUD + r] = o[h];
+                if (r == 0) {
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        part[NH * kUD + h] = pmu[h];
+                        part[NH * kUD + NH + h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+                    }
+                    part[NH * kUD + 2 * NH] = bad ? 1.f : 0.f;
+                }
+                return sync128();
+            }
             // The rows go out through shared memory (the previous unit's last
             // P^T buffer, free until two tiles on), as 16-byte stores: scattered
             // 2- or 4-byte stores stall for microseconds behind the copy stream.
@@ -593,8 +635,19 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const int64_t bh0 = (int64_t)x.b * p.H + x.h0;
             if (x.bad_len || x.ntiles == 0) {
                 if (x.bad_len && r == 0) report(p.err_word, x.bad_len);
-                if (!SPLIT)
+                if (csize > 1) {
+                    // an empty share: nothing to add to the merge
+                    float *part = reinterpret_cast<float *>(smem + L::kKRing);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) part[h * kUD + r] = 0.f;
+                    if (r < NH) {
+                        part[NH * kUD + r] = -INFINITY;
+                        part[NH * kUD + NH + r] = 0.f;
+                    }
+                    if (r == 0) part[NH * kUD + 2 * NH] = 0.f;
+                } else if (!SPLIT) {
                     for (int h = 0; h < x.nh; ++h) out[(bh0 + h) * kUD + r] = Elem<T>::from_float(0.f);
+                }
                 continue;
             }
             const int ob = kact & 1;
@@ -740,6 +793,65 @@ __global__ void __launch_bounds__(kUThreads, 1)
         tc05_fence_after_sync();
         tmem_dealloc(tmem, L::kCols);
     }
+    if (!SPLIT && csize > 1) {
+        // Every CTA's share sits in its own K ring; once all are done (the
+        // first barrier) the others store theirs into the first CTA's ring,
+        // and after the second barrier the first CTA merges them ([PG] s2.2's
+        // aggregation of per-block results, by the log-sum-exp rule) and
+        // writes the unit's rows.
+        constexpr int NH = L::NH;
+        constexpr int kRec = 2 * NH + 1;                        // m[NH], l[NH], flag of a share
+        constexpr int kShare = NH * kUD + kRec;                  // floats per share
+        float *shares = reinterpret_cast<float *>(smem + L::kKRing);   // [csize][kShare]; share 0 is this CTA's
+        cluster_sync();
+        if (crank > 0) {
+            const uint32_t dst = dsmem_addr(shares + crank * kShare, 0);
+            for (int i = threadIdx.x; i < kShare; i += kUThreads) dsmem_st_f32(dst + 4u * i, shares[i]);
+        }
+        cluster_sync();
+        if (crank == 0) {
+            const UUnit x = unit_of<SPLIT>(p, u_first, lens[0], tile_align);
+            float *wts = reinterpret_cast<float *>(smem + L::kP);        // [csize][NH], then the unit's flag at [8 * NH]
+            T *stage = reinterpret_cast<T *>(smem + L::kVRing);           // idle: the last P.V product has completed
+            if (threadIdx.x < NH) {
+                // per head: the weight of each share, 1/l folded in (0 for a bad unit)
+                const int h = threadIdx.x;
+                bool bad = false;
+                float M = -INFINITY, lt = 0.f;
+                for (int q = 0; q < csize; ++q) {
+                    const float *rec = shares + q * kShare + NH * kUD;
+                    bad |= rec[2 * NH] != 0.f;
+                    M = fmaxf(M, rec[h]);
+                }
+                for (int q = 0; q < csize; ++q) {
+                    const float *rec = shares + q * kShare + NH * kUD;
+                    lt = fmaf(rec[NH + h], merge_weight(rec[h], M), lt);
+                }
+                const float inv = !(lt > 0.f) ? 0.f : 1.f / lt;
+                for (int q = 0; q < csize; ++q) wts[q * NH + h] = merge_weight(shares[q * kShare + NH * kUD + h], M) * inv;
+                if (h == 0) wts[8 * NH] = bad ? 1.f : 0.f;
+            }
+            named_bar_sync(1, kUThreads);
+            if (threadIdx.x < kUD) {
+                // a flagged unit is zero (a share that met a bad entry may hold
+                // anything); a share of weight 0 adds nothing, whatever it holds
+                const int r = threadIdx.x;
+                const bool bad = wts[8 * NH] != 0.f;
+                for (int h = 0; h < x.nh; ++h) {
+                    float acc = 0.f;
+                    for (int q = 0; q < csize; ++q) {
+                        const float wq = wts[q * NH + h];
+                        if (wq != 0.f) acc = fmaf(shares[q * kShare + h * kUD + r], wq, acc);
+                    }
+                    stage[h * kUD + r] = Elem<T>::from_float(bad ? 0.f : acc);
+                }
+            }
+            named_bar_sync(1, kUThreads);
+            const int nchunks = x.nh * kUD * 2 / 16;   // the unit's heads are contiguous in out
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((int64_t)x.b * p.H + x.h0) * kUD);
+            for (int c = threadIdx.x; c < nchunks; c += kUThreads) dst[c] = reinterpret_cast<const uint4 *>(stage)[c];
+        }
+    }
 }
 
 template <typename T, int NT, bool SPLIT>
@@ -766,7 +878,55 @@ static cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kmap,
     int64_t grid = units < sms ? units : sms;
 #endif
     if (grid < (units + kUMaxUnits - 1) / kUMaxUnits) grid = (units + kUMaxUnits - 1) / kUMaxUnits;
-    return launch_clustered(kern, grid, kUThreads, Lay::kBytes, 1, stream, kmap, vmap, p, box_rows, (int)units);
+    int cluster = 1;
+    if (!SPLIT && p.cluster > 1) {
+        // one unit per cluster of p.cluster CTAs
+        cluster = p.cluster;
+        grid = units * cluster;
+    }
+    return launch_clustered(kern, grid, kUThreads, Lay::kBytes, cluster, stream, kmap, vmap, p, box_rows,
+                            (int)units);
+}
+
+// Clusters of `cluster` CTAs of the final-mode kernel for this dtype and
+// group size that can be resident at once on the current device (0 on
+// error); cached per device.
+int umma_max_active_clusters(int dtype, int group, int cluster) {
+    if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1)) != 0) return 0;
+    const bool two = group > 8;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    static std::atomic<int> cache[64][2][2][4];   // device, bf16, two head tiles, log2 cluster; value + 1
+    const int lc = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : 3;
+    std::atomic<int> &slot = cache[dev][dtype == PA_BF16][two][lc];
+    const int known = slot.load();
+    if (known > 0) return known - 1;
+    auto query = [&](auto kern, size_t smem) -> int {
+        static std::atomic<int> configured[64];
+        if (ensure_smem_limit(kern, smem, configured) != cudaSuccess) return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cluster * 64);
+        cfg.blockDim = dim3(kUThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : 0;
+    };
+    int n = 0;
+    if (dtype == PA_BF16)
+        n = two ? query(decode_gqa_umma_kernel<__nv_bfloat16, 2, false>, ULayout<2>::kBytes)
+                : query(decode_gqa_umma_kernel<__nv_bfloat16, 1, false>, ULayout<1>::kBytes);
+    else if (dtype == PA_F16)
+        n = two ? query(decode_gqa_umma_kernel<__half, 2, false>, ULayout<2>::kBytes)
+                : query(decode_gqa_umma_kernel<__half, 1, false>, ULayout<1>::kBytes);
+    slot.store(n + 1);
+    return n;
 }
 
 bool gqa_umma_supported(int dtype, int head_dim, int group) {

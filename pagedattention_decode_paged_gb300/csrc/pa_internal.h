@@ -235,7 +235,11 @@ bool gqa_tc_supported(int dtype, int head_dim);
 // kv head and CTA, 16-bit caches): a persistent grid of at most one CTA per
 // SM, each taking an equal share of the B*Hkv*ceil(g/16)*P units.  Same
 // tensor maps, parameters and results as launch_decode_gqa_tc (no clusters).
+// In final mode with p.cluster > 1, one unit per cluster of p.cluster CTAs,
+// each taking an equal share of its tiles, merged through distributed shared
+// memory; umma_max_active_clusters says how many such clusters fit at once.
 bool gqa_umma_supported(int dtype, int head_dim, int group);
+int umma_max_active_clusters(int dtype, int group, int cluster);
 cudaError_t launch_decode_gqa_umma(int dtype, const DecodeParams &p, const CUtensorMap &kmap,
                                    const CUtensorMap &vmap, int box_rows, bool split, cudaStream_t stream);
 

@@ -216,3 +216,65 @@ def test_workload4_batches_the_bench_times_on_tcgen05(batch):
     w = workloads.make_workload(4, block_size=16, batch=batch, poison=True)
     _assert_tcgen05(w)
     hz.run_fused_step_and_check(w)
+
+
+@pytest.mark.parametrize("H,Hkv,lens", [
+    (64, 8, [4500]),                                     # 8 units: clusters of 8
+    (64, 8, [4500, 1, 129, 0]),                          # 32 units: clusters of 4, some shares empty
+    (64, 8, [4500, 1, 129, 0, 700, 2047, 3000, 128]),   # 64 units: clusters of 2
+    (16, 1, [4200, 17, 2000]),                          # 16 heads per kv head (two head tiles)
+    (32, 4, [1100, 300, 1025]),                          # a short table row: clusters of 2
+])
+def test_few_units_spread_over_clusters(H, Hkv, lens):
+    """Fewer units than SMs: the CTAs of a cluster take equal shares of a
+    unit's tiles (shares of short sequences are empty, the appended row falls
+    in the last share) and the first CTA merges the shares through
+    distributed shared memory."""
+    assert len(lens) * Hkv < _sms() // 2, "the batch must have few units"
+    w = workloads.make_generic(B=len(lens), H=H, Hkv=Hkv, D=128, bs=16, dtype=BF16, lens=lens,
+                               seed=H + len(lens), poison=True)
+    _assert_tcgen05(w)
+    hz.run_step_and_check(w)
+    hz.run_fused_step_and_check(w)
+
+
+def test_bad_block_in_a_later_share():
+    """A bad table entry deep in a long sequence (in a share other than the
+    merging CTA's) zeroes that unit and raises the flag; the other units of
+    the launch stay exact."""
+    lens = [4000, 3900, 2500]
+    w = workloads.make_generic(B=len(lens), H=32, Hkv=4, D=128, bs=16, dtype=BF16, lens=lens, seed=21,
+                               poison=True)
+    _assert_tcgen05(w)
+    w.block_table[1, 200] = -1          # token 3200: the last shares of sequence 1
+    g = w.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = hz.gpu_decode(g, g.lens, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.DEVERR_BAD_BLOCK
+    assert not out[1].any()
+    ref, _ = hz.oracle_decode(w, w.pool, w.lens)
+    hz.assert_close(out[[0, 2]], ref[[0, 2]], BF16)
+
+
+@pytest.mark.parametrize("window", [1100, 2500])
+def test_window_across_cluster_shares(window):
+    """Sliding-window decodes long enough to be spread over a cluster: the
+    shares start at the window's tile and the rows before the window start
+    stay masked."""
+    lens = [4096, 3000, 1500]
+    w = workloads.make_generic(B=len(lens), H=16, Hkv=2, D=128, bs=16, dtype=F16, lens=lens,
+                               seed=window, poison=True)
+    _assert_tcgen05(w, window=window)
+    g = w.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(g.q)
+    pa.paged_attention_decode_window(out, g.q, g.k_flat(), g.v_flat(), g.block_table, g.lens, g.scale,
+                                     window, num_kv_heads=w.Hkv, err_word=err, **hz.kw(g))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    flat = w.pool.view(-1)
+    ref, e = oracle.attention_decode_window(w.q, flat, flat[w.v_offset:], w.block_table, w.lens, w.scale,
+                                            window, num_kv_heads=w.Hkv, **hz.kw(w))
+    assert not e.any()
+    hz.assert_close(out, ref, F16, f"window {window}")
