@@ -113,7 +113,9 @@ __device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
 
 }  // namespace
 
-template <typename T, int NT, bool SPLIT>
+// CL: one unit per thread-block cluster (final mode, few units); a separate
+// instantiation, so that the one-CTA path compiles without the merge.
+template <typename T, int NT, bool SPLIT, bool CL>
 __global__ void __launch_bounds__(kUThreads, 1)
     decode_gqa_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            DecodeParams p, int box_rows, int units) {
@@ -141,8 +143,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
     // first CTA merges the CTAs' softmax states through distributed shared
     // memory at the end.
     const int tile_align = box_rows < 16 ? 16 : box_rows;
-    const int csize = SPLIT ? 1 : (int)cluster_size();
-    const int crank = SPLIT ? 0 : (int)cluster_rank();
+    static_assert(!(SPLIT && CL), "clusters serve the final mode only");
+    const int csize = CL ? (int)cluster_size() : 1;
+    const int crank = CL ? (int)cluster_rank() : 0;
     const int u_first = csize > 1 ? (int)(blockIdx.x / csize) : (int)(((int64_t)blockIdx.x * units) / gridDim.x);
     const int nunits = csize > 1 ? 1 : (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x) - u_first;
     int *lens = reinterpret_cast<int *>(smem + L::kLens);
@@ -793,7 +796,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         tc05_fence_after_sync();
         tmem_dealloc(tmem, L::kCols);
     }
-    if (!SPLIT && csize > 1) {
+    if (CL && csize > 1) {
         // Every CTA's share sits in its own K ring; once all are done (the
         // first barrier) the others store theirs into the first CTA's ring,
         // and after the second barrier the first CTA merges them ([PG] s2.2's
@@ -858,9 +861,12 @@ template <typename T, int NT, bool SPLIT>
 static cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  int box_rows, cudaStream_t stream) {
     using Lay = ULayout<NT>;
-    auto kern = decode_gqa_umma_kernel<T, NT, SPLIT>;
-    static std::atomic<int> configured[64];
-    cudaError_t e = ensure_smem_limit(kern, Lay::kBytes, configured);
+    const bool cl = !SPLIT && p.cluster > 1;
+    auto kern = decode_gqa_umma_kernel<T, NT, SPLIT, false>;
+    auto kern_cl = decode_gqa_umma_kernel<T, NT, false, true>;
+    static std::atomic<int> configured[64], configured_cl[64];
+    cudaError_t e = cl ? ensure_smem_limit(kern_cl, Lay::kBytes, configured_cl)
+                       : ensure_smem_limit(kern, Lay::kBytes, configured);
     if (e != cudaSuccess) return e;
     const int g = p.H / p.Hkv;
     const int64_t units = (int64_t)p.B * p.Hkv * ((g + 15) / 16) * (SPLIT ? p.num_partitions : 1);
@@ -878,14 +884,10 @@ static cudaError_t launch_umma_t(const DecodeParams &p, const CUtensorMap &kmap,
     int64_t grid = units < sms ? units : sms;
 #endif
     if (grid < (units + kUMaxUnits - 1) / kUMaxUnits) grid = (units + kUMaxUnits - 1) / kUMaxUnits;
-    int cluster = 1;
-    if (!SPLIT && p.cluster > 1) {
-        // one unit per cluster of p.cluster CTAs
-        cluster = p.cluster;
-        grid = units * cluster;
-    }
-    return launch_clustered(kern, grid, kUThreads, Lay::kBytes, cluster, stream, kmap, vmap, p, box_rows,
-                            (int)units);
+    if (cl)   // one unit per cluster of p.cluster CTAs
+        return launch_clustered(kern_cl, units * p.cluster, kUThreads, Lay::kBytes, p.cluster, stream, kmap, vmap,
+                                p, box_rows, (int)units);
+    return launch_clustered(kern, grid, kUThreads, Lay::kBytes, 1, stream, kmap, vmap, p, box_rows, (int)units);
 }
 
 // Clusters of `cluster` CTAs of the final-mode kernel for this dtype and
@@ -901,9 +903,11 @@ int umma_max_active_clusters(int dtype, int group, int cluster) {
     std::atomic<int> &slot = cache[dev][dtype == PA_BF16][two][lc];
     const int known = slot.load();
     if (known > 0) return known - 1;
+    // (the kernels share one function-pointer type, so no per-kernel record
+    // of the raised limit can live here; the result is cached instead)
     auto query = [&](auto kern, size_t smem) -> int {
-        static std::atomic<int> configured[64];
-        if (ensure_smem_limit(kern, smem, configured) != cudaSuccess) return 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cluster * 64);
         cfg.blockDim = dim3(kUThreads);
@@ -920,11 +924,11 @@ int umma_max_active_clusters(int dtype, int group, int cluster) {
     };
     int n = 0;
     if (dtype == PA_BF16)
-        n = two ? query(decode_gqa_umma_kernel<__nv_bfloat16, 2, false>, ULayout<2>::kBytes)
-                : query(decode_gqa_umma_kernel<__nv_bfloat16, 1, false>, ULayout<1>::kBytes);
+        n = two ? query(decode_gqa_umma_kernel<__nv_bfloat16, 2, false, true>, ULayout<2>::kBytes)
+                : query(decode_gqa_umma_kernel<__nv_bfloat16, 1, false, true>, ULayout<1>::kBytes);
     else if (dtype == PA_F16)
-        n = two ? query(decode_gqa_umma_kernel<__half, 2, false>, ULayout<2>::kBytes)
-                : query(decode_gqa_umma_kernel<__half, 1, false>, ULayout<1>::kBytes);
+        n = two ? query(decode_gqa_umma_kernel<__half, 2, false, true>, ULayout<2>::kBytes)
+                : query(decode_gqa_umma_kernel<__half, 1, false, true>, ULayout<1>::kBytes);
     slot.store(n + 1);
     return n;
 }
