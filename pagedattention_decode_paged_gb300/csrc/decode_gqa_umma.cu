@@ -104,6 +104,11 @@ struct ULayout {
 };
 
 static_assert(ULayout<1>::kBytes <= 232448 && ULayout<2>::kBytes <= 232448, "shared memory per CTA");
+// the cluster merge: up to 8 shares (O^T, maxima, sums, flag) in the K ring,
+// the weights and the unit's flag in the P^T buffers, the rows in the V ring
+static_assert(8 * (ULayout<2>::NH * kUD + 2 * ULayout<2>::NH + 1) * 4 <= kSK * kTileBytes, "shares fit the K ring");
+static_assert((8 * ULayout<1>::NH + 1) * 4 <= 2 * ULayout<1>::kPBuf, "merge weights fit the P^T buffers");
+static_assert(ULayout<2>::NH * kUD * 2 <= kSV * kTileBytes, "rows fit the V ring");
 
 // Store v at a shared-memory address of another CTA of the cluster (from
 // dsmem_addr).
