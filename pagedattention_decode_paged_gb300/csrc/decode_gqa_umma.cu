@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const bool fused = !SPLIT && p.positions != nullptr;
     auto good = [&](int32_t blk) { return blk >= 0 && (int64_t)blk < p.num_blocks; };
     auto block_of = [&](int t) { return p.bs_shift >= 0 ? (t >> p.bs_shift) : t / p.bs; };
-    // tile iteration shared by the producer and the MMA warp
+    // tile iteration shared by the producer and the two MMA warps
     auto it_skip = [&](UIter &it) {
         while (it.k < nunits && it.i >= it.x.ntiles) {
             if (it.x.ntiles > 0) ++it.kact;
