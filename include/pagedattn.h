@@ -285,7 +285,8 @@ pa_path paged_attention_decode_path(const pa_shape *shape);
  * warp-level one (mma.sync; few long sequences also spread over
  * thread-block clusters) and, at head_dim 128, one on the fifth-generation
  * tensor cores (tcgen05.mma with accumulators in tensor memory, a
- * persistent grid of at most one CTA per SM); which one runs depends on how
+ * persistent grid of at most one CTA per SM, or with few units one unit per
+ * thread-block cluster of 2, 4 or 8 CTAs); which one runs depends on how
  * many (sequence, kv head) units the launch has against the SM count.
  * Results agree up to rounding order.  Returns PA_KERNEL_INVALID for a
  * rejected shape, window or partition size.  (An implementation query: no
