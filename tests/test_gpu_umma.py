@@ -278,3 +278,19 @@ def test_window_across_cluster_shares(window):
                                             window, num_kv_heads=w.Hkv, **hz.kw(w))
     assert not e.any()
     hz.assert_close(out, ref, F16, f"window {window}")
+
+
+@pytest.mark.parametrize("B", [1, 2, 5, 9, 12, 19, 24, 40, 57])
+def test_batch_sweep_across_dispatch_regimes(B):
+    """The GQA layer's shape (64 query heads on 8 kv heads) over a sweep of
+    batches that crosses every choice plan_decode makes: one unit per cluster
+    of 8, 4 or 2 tcgen05 CTAs, one tcgen05 CTA per unit, the mma.sync kernel,
+    and several units per tcgen05 CTA; a long first sequence sets the table
+    row length so that clusters apply, and zero-length and short sequences
+    sit among the others.  Fused append + decode against the oracle."""
+    pattern = [4200, 37, 600, 0, 250, 1500, 129]
+    lens = _repeat(pattern, B)
+    w = workloads.make_generic(B=B, H=64, Hkv=8, D=128, bs=16, dtype=BF16, lens=lens, seed=100 + B,
+                               poison=True)
+    assert pa.paged_attention_decode_kernel(hz.shape_of(w), 0, 0) in (pa.PA_KERNEL_TCGEN05, pa.PA_KERNEL_MMA_SYNC)
+    hz.run_fused_step_and_check(w)
